@@ -1,0 +1,135 @@
+"""The oracle: a plain float64 CPU reference of the attention forward pass.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path imports this package: only `tests/`,
+`__graft_entry__.smoke()` and `bench.py`'s CPU-baseline / reference arm call it. It shares no
+code with the CUDA path (see attn_oracle.c for the step-by-step definition and the passages
+of the pages each step follows).
+
+Every function takes q, k, v as bf16 tensors (CPU torch.bfloat16) or uint16 numpy arrays of
+bf16 bit patterns, in [B, T, H, D] layout, and returns float64 numpy arrays.
+
+Parity status: every function here is pinned by `tests/test_oracle_pins.py` (worked example,
+closed forms, invariants, library special cases, pure-Python brute force for T <= 8).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        ci, cd, cl = ctypes.c_int, ctypes.c_double, ctypes.c_long
+        lib.oracle_attn_fwd.argtypes = [u16p, u16p, u16p, f64p, f64p, ci, ci, ci, ci, ci, ci, cd, cd, ci, ci]
+        lib.oracle_attn_rows.argtypes = [u16p, u16p, u16p, i32p, cl, f64p, f64p, ci, ci, ci, ci, ci, ci,
+                                         cd, cd, ci, ci]
+        lib.oracle_attn_probs.argtypes = [u16p, u16p, u16p, ci, ci, f64p, ci, ci, ci, ci, ci, ci, cd, cd, ci]
+        lib.oracle_qk_prologue.argtypes = [u16p, f64p, ci, ci, ci, ci, cd, cd, ci, ci]
+        lib.oracle_round_bf16.argtypes = [cd]
+        lib.oracle_round_bf16.restype = cd
+        lib.oracle_num_threads.restype = ci
+        for f in (lib.oracle_attn_fwd, lib.oracle_attn_rows, lib.oracle_attn_probs, lib.oracle_qk_prologue):
+            f.restype = ci
+        _lib = lib
+    return _lib
+
+
+def _bits(x) -> np.ndarray:
+    """bf16 tensor / uint16 array -> contiguous uint16 numpy array (no copy of values)."""
+    if isinstance(x, np.ndarray):
+        assert x.dtype == np.uint16, x.dtype
+        return np.ascontiguousarray(x)
+    import torch
+
+    assert x.dtype == torch.bfloat16, x.dtype
+    return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _p(a, ct):
+    return a.ctypes.data_as(ctypes.POINTER(ct))
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bf16 value (ties to even), returned as float64."""
+    lib = _load()
+    flat = np.asarray(x, dtype=np.float64).ravel()
+    return np.array([lib.oracle_round_bf16(float(t)) for t in flat]).reshape(np.shape(x))
+
+
+def qk_prologue(x, rope_base: float = 10000.0, eps: float = 1e-6, round_qk: bool = True,
+                nthreads: int = 0) -> np.ndarray:
+    """RoPE then RMSNorm of every [.., D] row of x ([B, T, H, D]); float64 [B, T, H, D]."""
+    xb = _bits(x)
+    B, T, H, D = xb.shape
+    y = np.empty((B, T, H, D), dtype=np.float64)
+    _check(_load().oracle_qk_prologue(_p(xb, ctypes.c_uint16), _p(y, ctypes.c_double), B, T, H, D,
+                                      float(rope_base), float(eps), int(round_qk), int(nthreads)))
+    return y
+
+
+def attn_fwd(q, k, v, window: int = -1, causal: bool = True, rope_base: float = 10000.0,
+             eps: float = 1e-6, round_qk: bool = True, nthreads: int = 0):
+    """Full forward. Returns (out float64 [B, T, H, D], lse float64 [B, H, T], natural log)."""
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    B, T, H, D = qb.shape
+    assert kb.shape == qb.shape and vb.shape == qb.shape
+    out = np.empty((B, T, H, D), dtype=np.float64)
+    lse = np.empty((B, H, T), dtype=np.float64)
+    _check(_load().oracle_attn_fwd(_p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
+                                   _p(out, ctypes.c_double), _p(lse, ctypes.c_double), B, H, T, D,
+                                   int(window), int(bool(causal)), float(rope_base), float(eps),
+                                   int(round_qk), int(nthreads)))
+    return out, lse
+
+
+def attn_rows(q, k, v, rows, window: int = -1, causal: bool = True, rope_base: float = 10000.0,
+              eps: float = 1e-6, round_qk: bool = True, nthreads: int = 0):
+    """Selected query rows only. rows: int array [n, 3] of (b, h, i).
+    Returns (out float64 [n, D], lse float64 [n])."""
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    B, T, H, D = qb.shape
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+    n = r.shape[0]
+    out = np.empty((n, D), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    _check(_load().oracle_attn_rows(_p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
+                                    _p(r, ctypes.c_int32), n, _p(out, ctypes.c_double), _p(lse, ctypes.c_double),
+                                    B, H, T, D, int(window), int(bool(causal)), float(rope_base), float(eps),
+                                    int(round_qk), int(nthreads)))
+    return out, lse
+
+
+def attn_probs(q, k, v, b: int, h: int, window: int = -1, causal: bool = True, rope_base: float = 10000.0,
+               eps: float = 1e-6, round_qk: bool = True) -> np.ndarray:
+    """The attention weight matrix p [T, T] (queries x keys) of head (b, h)."""
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    B, T, H, D = qb.shape
+    p = np.empty((T, T), dtype=np.float64)
+    _check(_load().oracle_attn_probs(_p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
+                                     int(b), int(h), _p(p, ctypes.c_double), B, H, T, D, int(window),
+                                     int(bool(causal)), float(rope_base), float(eps), int(round_qk)))
+    return p
+
+
+__all__ = ["attn_fwd", "attn_rows", "attn_probs", "qk_prologue", "round_bf16", "num_threads"]

@@ -1,0 +1,310 @@
+"""Pins of the float64 oracle against what the pages and the mathematics fix (CPU only).
+
+Each test would fail for a plausible mistake somewhere in the oracle: a dropped eps, a wrong
+RoPE sign or pairing, an off-by-one in the window, a transposed operand, a wrong scale.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from oracle import brute
+from sliding_window_attention_04_b300.configs import n_allowed_keys, n_unmasked
+from sliding_window_attention_04_b300.inputs import make_qkv
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16(a):
+    return torch.tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+def f64(t):
+    return t.to(torch.float64).numpy()
+
+
+# ---------------------------------------------------------------------------------------------
+# Worked example ("geometry_of_andrea", "Lendo uma Projeção")
+
+
+def test_worked_example_r4():
+    g = json.load(open(os.path.join(GOLDEN, "worked_r4.json")))
+    q = np.array(g["q"], dtype=np.float64)
+    keys = np.array(g["keys"], dtype=np.float64)
+    # query at position 2 sees keys at positions 0, 1, 2 under the causal mask
+    Q = np.stack([q, q, q])[None, :, None, :]
+    K = keys[None, :, None, :]
+    V = np.eye(3, 4)[None, :, None, :]  # v_j = e_j, so out_2 holds the three weights
+    out, lse = oracle.attn_fwd(bf16(Q), bf16(K), bf16(V), window=-1, causal=True, rope_base=0.0, eps=-1.0)
+    w = [float(x) for x in g["weights"]]
+    np.testing.assert_allclose(out[0, 2, 0, :3], w, rtol=0, atol=1e-15)
+    assert out[0, 2, 0, 3] == 0.0
+    assert abs(lse[0, 0, 2] - float(g["lse"])) < 1e-15
+    # the scores themselves: lse - log(weight) = max score; log-weights differ by score gaps
+    s = np.log(out[0, 2, 0, :3]) + lse[0, 0, 2]
+    np.testing.assert_allclose(s, g["scaled_scores"], atol=1e-14)
+    # row 0 sees only k1: a single key gets weight 1 and lse = its score q.k1 / 2
+    np.testing.assert_allclose(out[0, 0, 0], [1, 0, 0, 0], atol=0)
+    assert abs(lse[0, 0, 0] - 0.5) < 1e-15
+    P = oracle.attn_probs(bf16(Q), bf16(K), bf16(V), 0, 0, window=-1, causal=True, rope_base=0.0, eps=-1.0)
+    np.testing.assert_allclose(P[2], w, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------------------------
+# Normalisation and masks ("O que a Atenção Calcula": weights sum to 1; "A Máscara Causal")
+
+
+@pytest.mark.parametrize("window,causal", [(-1, True), (3, True), (0, True), (2, False), (-1, False)])
+def test_weights_sum_to_one_and_mask_zero(window, causal):
+    T = 13
+    q, k, v = make_qkv(1, T, 2, 16, seed=7)
+    for h in range(2):
+        P = oracle.attn_probs(q, k, v, 0, h, window=window, causal=causal)
+        np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+        for i in range(T):
+            for j in range(T):
+                allowed = brute.visible(i, j, window, causal)
+                assert (P[i, j] > 0) == allowed, (i, j)
+
+
+def test_mask_literal_rows():
+    """Literal visible sets written out by hand for T = 6."""
+    T = 6
+    q, k, v = make_qkv(1, T, 1, 8, seed=3)
+    P = oracle.attn_probs(q, k, v, 0, 0, window=2, causal=True)
+    assert [j for j in range(T) if P[4, j] > 0] == [2, 3, 4]
+    assert [j for j in range(T) if P[0, j] > 0] == [0]
+    assert [j for j in range(T) if P[1, j] > 0] == [0, 1]
+    P = oracle.attn_probs(q, k, v, 0, 0, window=1, causal=False)
+    assert [j for j in range(T) if P[3, j] > 0] == [2, 3, 4]
+    assert [j for j in range(T) if P[5, j] > 0] == [4, 5]
+    P = oracle.attn_probs(q, k, v, 0, 0, window=-1, causal=True)
+    assert [j for j in range(T) if P[3, j] > 0] == [0, 1, 2, 3]
+    P = oracle.attn_probs(q, k, v, 0, 0, window=0, causal=True)
+    assert [j for j in range(T) if P[3, j] > 0] == [3]
+
+
+@pytest.mark.parametrize("window,causal", [(-1, True), (4, True), (3, False)])
+def test_masked_perturbation_invariance(window, causal):
+    B, T, H, D = 1, 20, 2, 16
+    q, k, v = make_qkv(B, T, H, D, seed=11)
+    out, lse = oracle.attn_fwd(q, k, v, window=window, causal=causal)
+    i = 9
+    k2, v2 = k.clone(), v.clone()
+    for j in range(T):
+        if not brute.visible(i, j, window, causal):
+            k2[:, j] = -k2[:, j] * 3
+            v2[:, j] = v2[:, j] + 5
+    out2, lse2 = oracle.attn_fwd(q, k2, v2, window=window, causal=causal)
+    assert np.array_equal(out[:, i], out2[:, i])
+    assert np.array_equal(lse[:, :, i], lse2[:, :, i])
+
+
+@pytest.mark.parametrize("T", [1, 7, 64])
+def test_window_ge_T_equals_full_causal(T):
+    q, k, v = make_qkv(2, T, 3, 16, seed=5)
+    ref_o, ref_l = oracle.attn_fwd(q, k, v, window=-1, causal=True)
+    for w in (T - 1, T, T + 3, 10 * T):
+        o, l = oracle.attn_fwd(q, k, v, window=w, causal=True)
+        assert np.array_equal(o, ref_o) and np.array_equal(l, ref_l)
+    if T > 2:
+        o, _ = oracle.attn_fwd(q, k, v, window=T - 2, causal=True)
+        assert not np.array_equal(o, ref_o)
+
+
+def test_constant_v_gives_constant_out():
+    B, T, H, D = 1, 33, 2, 16
+    q, k, _ = make_qkv(B, T, H, D, seed=9)
+    v = torch.full((B, T, H, D), 0.375, dtype=torch.bfloat16)
+    for window, causal in [(-1, True), (5, True), (4, False)]:
+        out, _ = oracle.attn_fwd(q, k, v, window=window, causal=causal)
+        np.testing.assert_allclose(out, 0.375, rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------------------------
+# Closed form: q = 0 gives uniform weights over J(i), so lse = ln|J(i)| (pins the mask counts)
+
+
+@pytest.mark.parametrize("window,causal,counts", [
+    (2, True, [1, 2, 3, 3, 3, 3, 3, 3]),
+    (0, True, [1] * 8),
+    (-1, True, [1, 2, 3, 4, 5, 6, 7, 8]),
+    (8, True, [1, 2, 3, 4, 5, 6, 7, 8]),
+    (2, False, [3, 4, 5, 5, 5, 5, 4, 3]),
+    (-1, False, [8] * 8),
+    (0, False, [1] * 8),
+])
+def test_zero_query_closed_form(window, causal, counts):
+    T, D = 8, 16
+    _, k, v = make_qkv(1, T, 1, D, seed=13)
+    q = torch.zeros((1, T, 1, D), dtype=torch.bfloat16)
+    out, lse = oracle.attn_fwd(q, k, v, window=window, causal=causal, eps=1e-6)
+    np.testing.assert_allclose(lse[0, 0], np.log(counts), rtol=0, atol=1e-15)
+    vv = f64(v)[0, :, 0]
+    lo_hi = [[j for j in range(T) if brute.visible(i, j, window, causal)] for i in range(T)]
+    assert [len(x) for x in lo_hi] == counts
+    for i in range(T):
+        np.testing.assert_allclose(out[0, i, 0], vv[lo_hi[i]].mean(axis=0), rtol=0, atol=1e-14)
+
+
+def test_zero_query_counts_large():
+    """Sum over rows of exp(lse) = number of unmasked entries, at the workload's T and window."""
+    T, D = 1024, 32
+    _, k, v = make_qkv(1, T, 1, D, seed=17)
+    q = torch.zeros((1, T, 1, D), dtype=torch.bfloat16)
+    for window in (512, 1024, -1):
+        _, lse = oracle.attn_fwd(q, k, v, window=window, causal=True)
+        total = np.exp(lse[0, 0]).sum()
+        assert abs(total - n_unmasked(T, window, True)) < 1e-6 * total
+    # the figures quoted for one (b, h) pair of the T = 1024 workloads
+    assert n_unmasked(1024, 512, True) == 393984
+    assert n_unmasked(1024, 1024, True) == 524800
+
+
+# ---------------------------------------------------------------------------------------------
+# RMSNorm and RoPE (habr "Autoresearch" deep dive, train.py listing: norm, apply_rotary_emb)
+
+
+def test_rmsnorm_values():
+    x = bf16(np.array([3.0, 4.0]).reshape(1, 1, 1, 2))
+    y = oracle.qk_prologue(x, rope_base=0.0, eps=0.0, round_qk=False)
+    np.testing.assert_allclose(y.ravel(), [3 / math.sqrt(12.5), 4 / math.sqrt(12.5)], rtol=1e-15)
+    ones = bf16(np.ones((1, 1, 1, 8)))
+    y = oracle.qk_prologue(ones, rope_base=0.0, eps=0.25, round_qk=False)
+    np.testing.assert_allclose(y.ravel(), 1 / math.sqrt(1.25), rtol=1e-15)
+
+
+def test_rmsnorm_identities():
+    B, T, H, D = 2, 5, 3, 32
+    x, _, _ = make_qkv(B, T, H, D, seed=21)
+    eps = 0.3
+    y = oracle.qk_prologue(x, rope_base=0.0, eps=eps, round_qk=False)
+    xx = f64(x)
+    ms = (xx ** 2).mean(-1)
+    np.testing.assert_allclose((y ** 2).sum(-1), D * ms / (ms + eps), rtol=1e-13)
+    # scale invariance with eps = 0 (2x is exact in bf16)
+    y1 = oracle.qk_prologue(x, rope_base=0.0, eps=0.0, round_qk=False)
+    y2 = oracle.qk_prologue((x.float() * 2).to(torch.bfloat16), rope_base=0.0, eps=0.0, round_qk=False)
+    assert np.array_equal(y1, y2)
+
+
+def test_rope_literal_values():
+    """D = 4, base 10000: pair 0 is (x0, x2) at angle t, pair 1 is (x1, x3) at angle t/100."""
+    def rot(vec, t):
+        x = np.zeros((1, t + 1, 1, 4))
+        x[0, t, 0] = vec
+        return oracle.qk_prologue(bf16(x), rope_base=10000.0, eps=-1.0, round_qk=False)[0, t, 0]
+
+    np.testing.assert_allclose(rot([1, 0, 0, 0], 1), [math.cos(1), 0, -math.sin(1), 0], atol=1e-15)
+    np.testing.assert_allclose(rot([0, 0, 1, 0], 1), [math.sin(1), 0, math.cos(1), 0], atol=1e-15)
+    np.testing.assert_allclose(rot([0, 1, 0, 0], 1), [0, math.cos(0.01), 0, -math.sin(0.01)], atol=1e-15)
+    np.testing.assert_allclose(rot([0, 0, 0, 1], 3), [0, math.sin(0.03), 0, math.cos(0.03)], atol=1e-15)
+    np.testing.assert_allclose(rot([0.5, -2, 1, 3], 0), [0.5, -2, 1, 3], atol=0)
+
+
+def test_rope_norm_preserving_and_commutes_with_norm():
+    B, T, H, D = 1, 40, 2, 64
+    x, _, _ = make_qkv(B, T, H, D, seed=23)
+    r = oracle.qk_prologue(x, rope_base=10000.0, eps=-1.0, round_qk=False)
+    np.testing.assert_allclose((r ** 2).sum(-1), (f64(x) ** 2).sum(-1), rtol=1e-13)
+    both = oracle.qk_prologue(x, rope_base=10000.0, eps=1e-6, round_qk=False)
+    # normalise first, then rotate: apply RoPE to the normalised row by solving with the
+    # rotation of the raw row (RoPE is linear, the norm is a per-row scale)
+    ms = (f64(x) ** 2).mean(-1, keepdims=True)
+    np.testing.assert_allclose(both, r / np.sqrt(ms + 1e-6), rtol=0, atol=1e-12)
+
+
+def test_rope_relative_position():
+    """With every q_t = a and every k_t = b, q_i . k_j depends only on i - j."""
+    T, D = 24, 32
+    a = np.random.default_rng(0).standard_normal(D)
+    b = np.random.default_rng(1).standard_normal(D)
+    qa = oracle.qk_prologue(bf16(np.tile(a, (1, T, 1, 1))), eps=1e-6, round_qk=False)[0, :, 0]
+    kb = oracle.qk_prologue(bf16(np.tile(b, (1, T, 1, 1))), eps=1e-6, round_qk=False)[0, :, 0]
+    S = qa @ kb.T
+    for off in range(-T + 1, T):
+        d = np.diagonal(S, offset=off)
+        assert np.ptp(d) < 1e-11, off
+    # and is not constant across offsets (positions do matter)
+    assert np.ptp([np.diagonal(S, offset=o)[0] for o in range(-5, 6)]) > 1e-3
+
+
+# ---------------------------------------------------------------------------------------------
+# Special cases that reduce to library routines
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_raw_mode_matches_scipy(causal):
+    B, T, H, D = 1, 37, 2, 16
+    q, k, v = make_qkv(B, T, H, D, seed=31)
+    out, lse = oracle.attn_fwd(q, k, v, window=-1, causal=causal, rope_base=0.0, eps=-1.0)
+    for h in range(H):
+        Q, K, V = f64(q)[0, :, h], f64(k)[0, :, h], f64(v)[0, :, h]
+        S = Q @ K.T / math.sqrt(D)
+        if causal:
+            S = np.where(np.tril(np.ones((T, T), dtype=bool)), S, -np.inf)
+        np.testing.assert_allclose(out[0, :, h], scipy.special.softmax(S, axis=1) @ V, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[0, h], scipy.special.logsumexp(S, axis=1), rtol=0, atol=1e-13)
+
+
+def test_round_bf16_matches_torch_and_brute():
+    rng = np.random.default_rng(5)
+    vals = np.concatenate([rng.standard_normal(2000) * 10.0 ** rng.integers(-30, 30, 2000),
+                           [1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 2 ** -130, 3.3895e38]])
+    f32 = vals.astype(np.float32).astype(np.float64)  # exactly representable in fp32
+    ours = oracle.round_bf16(f32)
+    ref = torch.tensor(f32.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(ours, ref)
+    assert all(brute.round_bf16(float(a)) == b for a, b in zip(f32, ours))
+    # ties go to the even neighbour
+    assert oracle.round_bf16(np.array([1 + 2 ** -8]))[0] == 1.0
+    assert oracle.round_bf16(np.array([1 + 3 * 2 ** -8]))[0] == 1 + 2 ** -6
+
+
+def test_round_qk_rounds_prologue_to_bf16():
+    x, _, _ = make_qkv(1, 9, 2, 32, seed=41)
+    a = oracle.qk_prologue(x, round_qk=True)
+    b = oracle.qk_prologue(x, round_qk=False)
+    assert np.array_equal(a, oracle.round_bf16(b))
+    assert not np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------------------------
+# Brute force for T <= 8 (every window, both mask modes, norm + RoPE on)
+
+
+@pytest.mark.parametrize("T", range(1, 9))
+def test_brute_force_small(T):
+    B, H, D = 1, 2, 8
+    q, k, v = make_qkv(B, T, H, D, seed=100 + T)
+    qn, kn, vn = (f64(t).tolist() for t in (q, k, v))
+    for window, causal in itertools.product(range(-1, 9), (True, False)):
+        out, lse = oracle.attn_fwd(q, k, v, window=window, causal=causal)
+        bo, bl = brute.forward(qn, kn, vn, window, causal, 10000.0, 1e-6)
+        np.testing.assert_allclose(out, np.array(bo), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse, np.array(bl), rtol=0, atol=1e-12)
+
+
+def test_brute_force_mask_counts():
+    for T in range(1, 9):
+        for window, causal in itertools.product(range(-1, 10), (True, False)):
+            for i in range(T):
+                assert n_allowed_keys(i, T, window, causal) == sum(brute.visible(i, j, window, causal)
+                                                                    for j in range(T))
+
+
+def test_rows_match_full():
+    B, T, H, D = 2, 70, 3, 32
+    q, k, v = make_qkv(B, T, H, D, seed=51)
+    out, lse = oracle.attn_fwd(q, k, v, window=20, causal=True)
+    rows = [(0, 0, 0), (1, 2, 69), (0, 1, 33), (1, 0, 21)]
+    o, l = oracle.attn_rows(q, k, v, rows, window=20, causal=True)
+    for n, (b, h, i) in enumerate(rows):
+        np.testing.assert_allclose(o[n], out[b, i, h], rtol=0, atol=1e-15)
+        assert abs(l[n] - lse[b, h, i]) < 1e-15
