@@ -8,6 +8,12 @@ of the pages each step follows).
 Every function takes q, k, v as bf16 tensors (CPU torch.bfloat16) or uint16 numpy arrays of
 bf16 bit patterns, in [B, T, H, D] layout, and returns float64 numpy arrays.
 
+`qk_precision` selects how the QK-norm + RoPE prologue is evaluated before q^ and k^ are
+rounded to bf16: "f32" (default, used for parity) takes that quantisation decision with the same
+fixed sequence of correctly rounded single-precision operations as the CUDA kernel (spelled out
+in attn_oracle.c), "f64" evaluates it in double. Everything after the rounding (scores, mask,
+softmax, weighted sum) is float64 in both modes.
+
 Parity status: every function here is pinned by `tests/test_oracle_pins.py` (worked example,
 closed forms, invariants, library special cases, pure-Python brute force for T <= 8).
 """
@@ -32,11 +38,11 @@ def _load():
         f64p = ctypes.POINTER(ctypes.c_double)
         i32p = ctypes.POINTER(ctypes.c_int32)
         ci, cd, cl = ctypes.c_int, ctypes.c_double, ctypes.c_long
-        lib.oracle_attn_fwd.argtypes = [u16p, u16p, u16p, f64p, f64p, ci, ci, ci, ci, ci, ci, cd, cd, ci, ci]
+        lib.oracle_attn_fwd.argtypes = [u16p, u16p, u16p, f64p, f64p, ci, ci, ci, ci, ci, ci, cd, cd, ci, ci, ci]
         lib.oracle_attn_rows.argtypes = [u16p, u16p, u16p, i32p, cl, f64p, f64p, ci, ci, ci, ci, ci, ci,
-                                         cd, cd, ci, ci]
-        lib.oracle_attn_probs.argtypes = [u16p, u16p, u16p, ci, ci, f64p, ci, ci, ci, ci, ci, ci, cd, cd, ci]
-        lib.oracle_qk_prologue.argtypes = [u16p, f64p, ci, ci, ci, ci, cd, cd, ci, ci]
+                                         cd, cd, ci, ci, ci]
+        lib.oracle_attn_probs.argtypes = [u16p, u16p, u16p, ci, ci, f64p, ci, ci, ci, ci, ci, ci, cd, cd, ci, ci]
+        lib.oracle_qk_prologue.argtypes = [u16p, f64p, ci, ci, ci, ci, cd, cd, ci, ci, ci]
         lib.oracle_round_bf16.argtypes = [cd]
         lib.oracle_round_bf16.restype = cd
         lib.oracle_num_threads.restype = ci
@@ -61,6 +67,15 @@ def _p(a, ct):
     return a.ctypes.data_as(ctypes.POINTER(ct))
 
 
+_PREC = {"f64": 0, "f32": 1}
+
+
+def _prec(p: str) -> int:
+    if p not in _PREC:
+        raise ValueError(f"qk_precision must be 'f32' or 'f64', not {p!r}")
+    return _PREC[p]
+
+
 def _check(rc: int):
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (code {rc})")
@@ -78,18 +93,19 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
 
 
 def qk_prologue(x, rope_base: float = 10000.0, eps: float = 1e-6, round_qk: bool = True,
-                nthreads: int = 0) -> np.ndarray:
+                nthreads: int = 0, qk_precision: str = "f32") -> np.ndarray:
     """RoPE then RMSNorm of every [.., D] row of x ([B, T, H, D]); float64 [B, T, H, D]."""
     xb = _bits(x)
     B, T, H, D = xb.shape
     y = np.empty((B, T, H, D), dtype=np.float64)
     _check(_load().oracle_qk_prologue(_p(xb, ctypes.c_uint16), _p(y, ctypes.c_double), B, T, H, D,
-                                      float(rope_base), float(eps), int(round_qk), int(nthreads)))
+                                      float(rope_base), float(eps), int(round_qk), _prec(qk_precision),
+                                      int(nthreads)))
     return y
 
 
 def attn_fwd(q, k, v, window: int = -1, causal: bool = True, rope_base: float = 10000.0,
-             eps: float = 1e-6, round_qk: bool = True, nthreads: int = 0):
+             eps: float = 1e-6, round_qk: bool = True, nthreads: int = 0, qk_precision: str = "f32"):
     """Full forward. Returns (out float64 [B, T, H, D], lse float64 [B, H, T], natural log)."""
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     B, T, H, D = qb.shape
@@ -99,12 +115,12 @@ def attn_fwd(q, k, v, window: int = -1, causal: bool = True, rope_base: float = 
     _check(_load().oracle_attn_fwd(_p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
                                    _p(out, ctypes.c_double), _p(lse, ctypes.c_double), B, H, T, D,
                                    int(window), int(bool(causal)), float(rope_base), float(eps),
-                                   int(round_qk), int(nthreads)))
+                                   int(round_qk), _prec(qk_precision), int(nthreads)))
     return out, lse
 
 
 def attn_rows(q, k, v, rows, window: int = -1, causal: bool = True, rope_base: float = 10000.0,
-              eps: float = 1e-6, round_qk: bool = True, nthreads: int = 0):
+              eps: float = 1e-6, round_qk: bool = True, nthreads: int = 0, qk_precision: str = "f32"):
     """Selected query rows only. rows: int array [n, 3] of (b, h, i).
     Returns (out float64 [n, D], lse float64 [n])."""
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
@@ -116,19 +132,20 @@ def attn_rows(q, k, v, rows, window: int = -1, causal: bool = True, rope_base: f
     _check(_load().oracle_attn_rows(_p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
                                     _p(r, ctypes.c_int32), n, _p(out, ctypes.c_double), _p(lse, ctypes.c_double),
                                     B, H, T, D, int(window), int(bool(causal)), float(rope_base), float(eps),
-                                    int(round_qk), int(nthreads)))
+                                    int(round_qk), _prec(qk_precision), int(nthreads)))
     return out, lse
 
 
 def attn_probs(q, k, v, b: int, h: int, window: int = -1, causal: bool = True, rope_base: float = 10000.0,
-               eps: float = 1e-6, round_qk: bool = True) -> np.ndarray:
+               eps: float = 1e-6, round_qk: bool = True, qk_precision: str = "f32") -> np.ndarray:
     """The attention weight matrix p [T, T] (queries x keys) of head (b, h)."""
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     B, T, H, D = qb.shape
     p = np.empty((T, T), dtype=np.float64)
     _check(_load().oracle_attn_probs(_p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
                                      int(b), int(h), _p(p, ctypes.c_double), B, H, T, D, int(window),
-                                     int(bool(causal)), float(rope_base), float(eps), int(round_qk)))
+                                     int(bool(causal)), float(rope_base), float(eps), int(round_qk),
+                                     _prec(qk_precision)))
     return p
 
 

@@ -19,6 +19,19 @@
  *  3. The rotated, normalised q and k are rounded once to bf16 (nearest, ties to even),
  *     because the listing runs under bf16 autocast and hands bf16 q, k to the attention call.
  *     round_qk = 0 skips this rounding (information only).
+ *
+ *     This rounding is a quantisation decision, so it is taken in the same precision as the
+ *     CUDA kernel takes it (prec = ORACLE_PREC_F32, the mode used for parity): steps 1-2 are
+ *     then evaluated with this fixed sequence of IEEE-754 single-precision operations, each
+ *     correctly rounded (fmaf, *, +, sqrtf, /):
+ *         ss = 0; for d = 0..D-1: ss = fmaf(x[d], x[d], ss)
+ *         r  = 1 / sqrtf(ss * (1/D) + eps)                      (r = 1 without the norm)
+ *         c  = cos32(theta_i) * r,  s = sin32(theta_i) * r       (c = r, s = 0 without RoPE)
+ *         y[i] = fmaf(x1, c, x2 * s),  y[i + D/2] = fmaf(x2, c, -(x1 * s))
+ *     where cos32 / sin32 are the double cos / sin of the double angle rounded to float. In
+ *     exact arithmetic this is the same function as steps 1-2 (the norm is a per-row scale and
+ *     commutes with the rotation). prec = ORACLE_PREC_F64 evaluates steps 1-2 in double, in the
+ *     listing's order; the pins use it.
  *  4. Allowed keys of query i ("geometry_of_andrea" page, "A Máscara Causal": token t sees
  *     tokens 0..t; habr listing, flash_attn_func(..., causal=True, window_size=(W, 0))):
  *     J(i) = { j in [0, T) : (causal => j <= i),
@@ -60,9 +73,48 @@ double oracle_round_bf16(double x) {
   return y;
 }
 
+#define ORACLE_PREC_F64 0
+#define ORACLE_PREC_F32 1
+
+/* Round a float to the nearest bf16 value (ties to even), returned as double (exact). */
+static double round_bf16_from_float(float f) { return oracle_round_bf16((double)f); }
+
+/* Steps 1-3 in the single-precision sequence described in the header comment. */
+static void prologue_row_f32(const double *x, double *y, int D, int t, double base, double eps,
+                             int round_qk) {
+  base = (double)(float)base; /* the kernel receives the base as a float */
+  float xf[1024];
+  for (int d = 0; d < D; ++d) xf[d] = (float)x[d]; /* x holds bf16 values: exact */
+  float r = 1.0f;
+  if (eps >= 0.0) {
+    float ss = 0.0f;
+    for (int d = 0; d < D; ++d) ss = fmaf(xf[d], xf[d], ss);
+    float ms = ss * (1.0f / (float)D);
+    float den = sqrtf(ms + (float)eps);
+    r = 1.0f / den;
+  }
+  if (base > 0.0) {
+    int half = D / 2;
+    for (int i = 0; i < half; ++i) {
+      double theta = (double)t * pow(base, -2.0 * (double)i / (double)D);
+      float c = (float)cos(theta) * r, s = (float)sin(theta) * r;
+      float x1 = xf[i], x2 = xf[i + half];
+      float y1 = fmaf(x1, c, x2 * s);
+      float y2 = fmaf(x2, c, -(x1 * s));
+      y[i] = round_qk ? round_bf16_from_float(y1) : (double)y1;
+      y[i + half] = round_qk ? round_bf16_from_float(y2) : (double)y2;
+    }
+  } else {
+    for (int d = 0; d < D; ++d) {
+      float v = xf[d] * r;
+      y[d] = round_qk ? round_bf16_from_float(v) : (double)v;
+    }
+  }
+}
+
 /* Step 1 and 2 for one row x[0..D) at position t; the result goes to y[0..D). */
-static void prologue_row(const double *x, double *y, int D, int t, double base, double eps,
-                         int round_qk) {
+static void prologue_row_f64(const double *x, double *y, int D, int t, double base, double eps,
+                             int round_qk) {
   double tmp[1024];
   for (int d = 0; d < D; ++d) tmp[d] = x[d];
   if (base > 0.0) {
@@ -88,6 +140,14 @@ static void prologue_row(const double *x, double *y, int D, int t, double base, 
   }
 }
 
+static void prologue_row(const double *x, double *y, int D, int t, double base, double eps,
+                         int round_qk, int prec) {
+  if (prec == ORACLE_PREC_F32)
+    prologue_row_f32(x, y, D, t, base, eps, round_qk);
+  else
+    prologue_row_f64(x, y, D, t, base, eps, round_qk);
+}
+
 static int key_allowed(int i, int j, int T, int window, int causal) {
   if (j < 0 || j >= T) return 0;
   if (causal && j > i) return 0;
@@ -111,7 +171,7 @@ static size_t idx4(int b, int t, int h, int d, int T, int H, int D) {
 
 /* Steps 1-3 for a whole [B, T, H, D] tensor of bf16 bits; y is [B, T, H, D] doubles. */
 int oracle_qk_prologue(const uint16_t *x, double *y, int B, int T, int H, int D,
-                       double rope_base, double eps, int round_qk, int nthreads) {
+                       double rope_base, double eps, int round_qk, int prec, int nthreads) {
   if (!x || !y || !check_dims(B, H, T, D, rope_base)) return ORACLE_EINVAL;
   long n = (long)B * T * H;
 #pragma omp parallel for schedule(static) num_threads(nthreads > 0 ? nthreads : omp_get_max_threads())
@@ -119,7 +179,7 @@ int oracle_qk_prologue(const uint16_t *x, double *y, int B, int T, int H, int D,
     int t = (int)((row / H) % T);
     double xr[1024];
     for (int d = 0; d < D; ++d) xr[d] = bf16_to_double(x[row * D + d]);
-    prologue_row(xr, y + row * D, D, t, rope_base, eps, round_qk);
+    prologue_row(xr, y + row * D, D, t, rope_base, eps, round_qk, prec);
   }
   return ORACLE_OK;
 }
@@ -167,7 +227,7 @@ static void attend_row(const double *qh, const double *kh, const uint16_t *v, in
 /* Full forward: out is [B, T, H, D] doubles, lse is [B, H, T] doubles (either may be NULL). */
 int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, double *out,
                     double *lse, int B, int H, int T, int D, int window, int causal,
-                    double rope_base, double eps, int round_qk, int nthreads) {
+                    double rope_base, double eps, int round_qk, int prec, int nthreads) {
   if (!q || !k || !v || !check_dims(B, H, T, D, rope_base)) return ORACLE_EINVAL;
   size_t n = (size_t)B * T * H * D;
   double *qh = (double *)malloc(sizeof(double) * n);
@@ -178,8 +238,8 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, dou
     return ORACLE_ENOMEM;
   }
   int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
-  oracle_qk_prologue(q, qh, B, T, H, D, rope_base, eps, round_qk, nt);
-  oracle_qk_prologue(k, kh, B, T, H, D, rope_base, eps, round_qk, nt);
+  oracle_qk_prologue(q, qh, B, T, H, D, rope_base, eps, round_qk, prec, nt);
+  oracle_qk_prologue(k, kh, B, T, H, D, rope_base, eps, round_qk, prec, nt);
   long rows = (long)B * H * T;
 #pragma omp parallel for schedule(dynamic, 16) num_threads(nt)
   for (long r = 0; r < rows; ++r) {
@@ -201,7 +261,8 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, dou
  * The prologue is evaluated for the query row and for every allowed key of it. */
 int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *rows,
                      long n, double *out, double *lse, int B, int H, int T, int D, int window,
-                     int causal, double rope_base, double eps, int round_qk, int nthreads) {
+                     int causal, double rope_base, double eps, int round_qk, int prec,
+                     int nthreads) {
   if (!q || !k || !v || !rows || n < 0 || !check_dims(B, H, T, D, rope_base)) return ORACLE_EINVAL;
   for (long r = 0; r < n; ++r) {
     const int32_t *t3 = rows + 3 * r;
@@ -217,11 +278,11 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, co
     double *kh = (double *)calloc((size_t)T * D, sizeof(double));
     double xr[1024];
     for (int d = 0; d < D; ++d) xr[d] = bf16_to_double(q[idx4(b, i, h, d, T, H, D)]);
-    prologue_row(xr, qh + (size_t)i * D, D, i, rope_base, eps, round_qk);
+    prologue_row(xr, qh + (size_t)i * D, D, i, rope_base, eps, round_qk, prec);
     for (int j = 0; j < T; ++j) {
       if (!key_allowed(i, j, T, window, causal)) continue;
       for (int d = 0; d < D; ++d) xr[d] = bf16_to_double(k[idx4(b, j, h, d, T, H, D)]);
-      prologue_row(xr, kh + (size_t)j * D, D, j, rope_base, eps, round_qk);
+      prologue_row(xr, kh + (size_t)j * D, D, j, rope_base, eps, round_qk, prec);
     }
     /* attend_row indexes a [B, T, H, D] tensor; view the private copy as B = H = 1 and
        gather v into the same [1, T, 1, D] view. */
@@ -239,7 +300,7 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, co
 /* The full weight matrix p[T][T] of head (b, h) (rows: queries, columns: keys). */
 int oracle_attn_probs(const uint16_t *q, const uint16_t *k, const uint16_t *v, int b, int h,
                       double *p, int B, int H, int T, int D, int window, int causal,
-                      double rope_base, double eps, int round_qk) {
+                      double rope_base, double eps, int round_qk, int prec) {
   if (!q || !k || !v || !p || !check_dims(B, H, T, D, rope_base) || b < 0 || b >= B || h < 0 ||
       h >= H)
     return ORACLE_EINVAL;
@@ -251,8 +312,8 @@ int oracle_attn_probs(const uint16_t *q, const uint16_t *k, const uint16_t *v, i
     free(kh);
     return ORACLE_ENOMEM;
   }
-  oracle_qk_prologue(q, qh, B, T, H, D, rope_base, eps, round_qk, 1);
-  oracle_qk_prologue(k, kh, B, T, H, D, rope_base, eps, round_qk, 1);
+  oracle_qk_prologue(q, qh, B, T, H, D, rope_base, eps, round_qk, prec, 1);
+  oracle_qk_prologue(k, kh, B, T, H, D, rope_base, eps, round_qk, prec, 1);
   double o[1024], l;
   for (int i = 0; i < T; ++i)
     attend_row(qh, kh, v, b, h, i, T, H, D, window, causal, o, &l, p + (size_t)i * T);

@@ -173,47 +173,54 @@ def test_zero_query_counts_large():
 
 def test_rmsnorm_values():
     x = bf16(np.array([3.0, 4.0]).reshape(1, 1, 1, 2))
-    y = oracle.qk_prologue(x, rope_base=0.0, eps=0.0, round_qk=False)
+    y = oracle.qk_prologue(x, rope_base=0.0, eps=0.0, round_qk=False, qk_precision="f64")
     np.testing.assert_allclose(y.ravel(), [3 / math.sqrt(12.5), 4 / math.sqrt(12.5)], rtol=1e-15)
+    y = oracle.qk_prologue(x, rope_base=0.0, eps=0.0, round_qk=False, qk_precision="f32")
+    np.testing.assert_allclose(y.ravel(), [3 / math.sqrt(12.5), 4 / math.sqrt(12.5)], rtol=2e-7)
     ones = bf16(np.ones((1, 1, 1, 8)))
-    y = oracle.qk_prologue(ones, rope_base=0.0, eps=0.25, round_qk=False)
-    np.testing.assert_allclose(y.ravel(), 1 / math.sqrt(1.25), rtol=1e-15)
+    for prec, tol in (("f64", 1e-15), ("f32", 2e-7)):
+        y = oracle.qk_prologue(ones, rope_base=0.0, eps=0.25, round_qk=False, qk_precision=prec)
+        np.testing.assert_allclose(y.ravel(), 1 / math.sqrt(1.25), rtol=tol)
 
 
 def test_rmsnorm_identities():
     B, T, H, D = 2, 5, 3, 32
     x, _, _ = make_qkv(B, T, H, D, seed=21)
     eps = 0.3
-    y = oracle.qk_prologue(x, rope_base=0.0, eps=eps, round_qk=False)
+    y = oracle.qk_prologue(x, rope_base=0.0, eps=eps, round_qk=False, qk_precision="f64")
     xx = f64(x)
     ms = (xx ** 2).mean(-1)
     np.testing.assert_allclose((y ** 2).sum(-1), D * ms / (ms + eps), rtol=1e-13)
     # scale invariance with eps = 0 (2x is exact in bf16)
-    y1 = oracle.qk_prologue(x, rope_base=0.0, eps=0.0, round_qk=False)
-    y2 = oracle.qk_prologue((x.float() * 2).to(torch.bfloat16), rope_base=0.0, eps=0.0, round_qk=False)
-    assert np.array_equal(y1, y2)
+    for prec in ("f64", "f32"):
+        y1 = oracle.qk_prologue(x, rope_base=0.0, eps=0.0, round_qk=False, qk_precision=prec)
+        y2 = oracle.qk_prologue((x.float() * 2).to(torch.bfloat16), rope_base=0.0, eps=0.0, round_qk=False,
+                                qk_precision=prec)
+        assert np.array_equal(y1, y2)
 
 
 def test_rope_literal_values():
     """D = 4, base 10000: pair 0 is (x0, x2) at angle t, pair 1 is (x1, x3) at angle t/100."""
-    def rot(vec, t):
-        x = np.zeros((1, t + 1, 1, 4))
-        x[0, t, 0] = vec
-        return oracle.qk_prologue(bf16(x), rope_base=10000.0, eps=-1.0, round_qk=False)[0, t, 0]
+    for prec, tol in (("f64", 1e-15), ("f32", 1e-7)):
+        def rot(vec, t):
+            x = np.zeros((1, t + 1, 1, 4))
+            x[0, t, 0] = vec
+            return oracle.qk_prologue(bf16(x), rope_base=10000.0, eps=-1.0, round_qk=False,
+                                      qk_precision=prec)[0, t, 0]
 
-    np.testing.assert_allclose(rot([1, 0, 0, 0], 1), [math.cos(1), 0, -math.sin(1), 0], atol=1e-15)
-    np.testing.assert_allclose(rot([0, 0, 1, 0], 1), [math.sin(1), 0, math.cos(1), 0], atol=1e-15)
-    np.testing.assert_allclose(rot([0, 1, 0, 0], 1), [0, math.cos(0.01), 0, -math.sin(0.01)], atol=1e-15)
-    np.testing.assert_allclose(rot([0, 0, 0, 1], 3), [0, math.sin(0.03), 0, math.cos(0.03)], atol=1e-15)
-    np.testing.assert_allclose(rot([0.5, -2, 1, 3], 0), [0.5, -2, 1, 3], atol=0)
+        np.testing.assert_allclose(rot([1, 0, 0, 0], 1), [math.cos(1), 0, -math.sin(1), 0], atol=tol)
+        np.testing.assert_allclose(rot([0, 0, 1, 0], 1), [math.sin(1), 0, math.cos(1), 0], atol=tol)
+        np.testing.assert_allclose(rot([0, 1, 0, 0], 1), [0, math.cos(0.01), 0, -math.sin(0.01)], atol=tol)
+        np.testing.assert_allclose(rot([0, 0, 0, 1], 3), [0, math.sin(0.03), 0, math.cos(0.03)], atol=tol)
+        np.testing.assert_allclose(rot([0.5, -2, 1, 3], 0), [0.5, -2, 1, 3], atol=0)
 
 
 def test_rope_norm_preserving_and_commutes_with_norm():
     B, T, H, D = 1, 40, 2, 64
     x, _, _ = make_qkv(B, T, H, D, seed=23)
-    r = oracle.qk_prologue(x, rope_base=10000.0, eps=-1.0, round_qk=False)
+    r = oracle.qk_prologue(x, rope_base=10000.0, eps=-1.0, round_qk=False, qk_precision="f64")
     np.testing.assert_allclose((r ** 2).sum(-1), (f64(x) ** 2).sum(-1), rtol=1e-13)
-    both = oracle.qk_prologue(x, rope_base=10000.0, eps=1e-6, round_qk=False)
+    both = oracle.qk_prologue(x, rope_base=10000.0, eps=1e-6, round_qk=False, qk_precision="f64")
     # normalise first, then rotate: apply RoPE to the normalised row by solving with the
     # rotation of the raw row (RoPE is linear, the norm is a per-row scale)
     ms = (f64(x) ** 2).mean(-1, keepdims=True)
@@ -225,8 +232,8 @@ def test_rope_relative_position():
     T, D = 24, 32
     a = np.random.default_rng(0).standard_normal(D)
     b = np.random.default_rng(1).standard_normal(D)
-    qa = oracle.qk_prologue(bf16(np.tile(a, (1, T, 1, 1))), eps=1e-6, round_qk=False)[0, :, 0]
-    kb = oracle.qk_prologue(bf16(np.tile(b, (1, T, 1, 1))), eps=1e-6, round_qk=False)[0, :, 0]
+    qa = oracle.qk_prologue(bf16(np.tile(a, (1, T, 1, 1))), eps=1e-6, round_qk=False, qk_precision="f64")[0, :, 0]
+    kb = oracle.qk_prologue(bf16(np.tile(b, (1, T, 1, 1))), eps=1e-6, round_qk=False, qk_precision="f64")[0, :, 0]
     S = qa @ kb.T
     for off in range(-T + 1, T):
         d = np.diagonal(S, offset=off)
@@ -269,8 +276,8 @@ def test_round_bf16_matches_torch_and_brute():
 
 def test_round_qk_rounds_prologue_to_bf16():
     x, _, _ = make_qkv(1, 9, 2, 32, seed=41)
-    a = oracle.qk_prologue(x, round_qk=True)
-    b = oracle.qk_prologue(x, round_qk=False)
+    a = oracle.qk_prologue(x, round_qk=True, qk_precision="f64")
+    b = oracle.qk_prologue(x, round_qk=False, qk_precision="f64")
     assert np.array_equal(a, oracle.round_bf16(b))
     assert not np.array_equal(a, b)
 
@@ -285,7 +292,7 @@ def test_brute_force_small(T):
     q, k, v = make_qkv(B, T, H, D, seed=100 + T)
     qn, kn, vn = (f64(t).tolist() for t in (q, k, v))
     for window, causal in itertools.product(range(-1, 9), (True, False)):
-        out, lse = oracle.attn_fwd(q, k, v, window=window, causal=causal)
+        out, lse = oracle.attn_fwd(q, k, v, window=window, causal=causal, qk_precision="f64")
         bo, bl = brute.forward(qn, kn, vn, window, causal, 10000.0, 1e-6)
         np.testing.assert_allclose(out, np.array(bo), rtol=0, atol=1e-12)
         np.testing.assert_allclose(lse, np.array(bl), rtol=0, atol=1e-12)
@@ -308,3 +315,54 @@ def test_rows_match_full():
     for n, (b, h, i) in enumerate(rows):
         np.testing.assert_allclose(o[n], out[b, i, h], rtol=0, atol=1e-15)
         assert abs(l[n] - lse[b, h, i]) < 1e-15
+
+
+# ---------------------------------------------------------------------------------------------
+# The single-precision prologue (the precision in which q^, k^ are quantised to bf16) computes
+# the same function as the double one, up to its rounding.
+
+
+@pytest.mark.parametrize("D,rope_base,eps", [(32, 10000.0, 1e-6), (64, 10000.0, 1e-6), (128, 10000.0, 1e-6),
+                                             (64, 0.0, 1e-6), (64, 10000.0, -1.0), (64, 500.0, 0.3)])
+def test_f32_prologue_tracks_f64(D, rope_base, eps):
+    """Error bound of the fp32 sequence: the sum of D squares carries a relative error of at most
+    (D - 1) 2^-24, so r is within about D 2^-25 + 2^-23 relative, and each output, a sum of two
+    products of |x| with |c|, |s| <= r, is within 2^-16 (|x1| + |x2|) r of the exact value."""
+    T = 300
+    x, _, _ = make_qkv(1, T, 2, D, seed=61 + D)
+    x = (x.float() * 3).to(torch.bfloat16)
+    y32 = oracle.qk_prologue(x, rope_base=rope_base, eps=eps, round_qk=False, qk_precision="f32")
+    y64 = oracle.qk_prologue(x, rope_base=rope_base, eps=eps, round_qk=False, qk_precision="f64")
+    xx = f64(x)
+    r = 1 / np.sqrt((xx ** 2).mean(-1, keepdims=True) + eps) if eps >= 0 else np.ones_like(xx[..., :1])
+    if rope_base > 0:
+        half = D // 2
+        mag = np.abs(xx[..., :half]) + np.abs(xx[..., half:])
+        mag = np.concatenate([mag, mag], axis=-1)
+    else:
+        mag = np.abs(xx)
+    bound = 2.0 ** -16 * mag * r + 1e-30
+    assert (np.abs(y32 - y64) <= bound).all()
+    assert np.abs(y32 - y64).max() > 0  # the two modes are genuinely different evaluations
+
+
+def test_f32_rounding_agrees_with_f64_except_near_ties():
+    D, T = 64, 512
+    x, _, _ = make_qkv(2, T, 4, D, seed=71)
+    a32 = oracle.qk_prologue(x, round_qk=True, qk_precision="f32")
+    a64 = oracle.qk_prologue(x, round_qk=True, qk_precision="f64")
+    y64 = oracle.qk_prologue(x, round_qk=False, qk_precision="f64")
+    y32 = oracle.qk_prologue(x, round_qk=False, qk_precision="f32")
+    assert np.array_equal(a32, oracle.round_bf16(y32))
+    diff = a32 != a64
+    # where they differ, the two roundings are neighbouring bf16 values and the midpoint between
+    # them lies between the fp32 and the double evaluation (a near-tie, nothing else)
+    if diff.any():
+        lo = np.minimum(a32[diff], a64[diff])
+        hi = np.maximum(a32[diff], a64[diff])
+        mid = (lo + hi) / 2
+        assert (oracle.round_bf16(mid + (hi - lo) / 4) == hi).all()
+        assert (oracle.round_bf16(mid - (hi - lo) / 4) == lo).all()
+        a, b = np.minimum(y32[diff], y64[diff]), np.maximum(y32[diff], y64[diff])
+        assert ((a <= mid) & (mid <= b)).all()
+    assert diff.mean() < 1e-3
