@@ -1,0 +1,375 @@
+#!/usr/bin/env python
+"""Benchmark of the attention forward path on the ANDREA-120M-shaped SSSL workload.
+
+One step = one forward call per layer of the 12-layer stack (B=32, H=12, T=1024, D=64; windows
+512, 512, 512, 1024 repeated three times), each layer with its own seeded inputs. The metric is
+TFLOP/s over unmasked score entries only (4*D FLOPs per entry), summed over the layers.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). `--impl reference` times the float64 CPU oracle on the host
+cores on a bounded sample of the same workload (the reference arm of this comparison).
+Multi-GPU (torchrun): every rank runs its own replica of the workload (weak scaling, no
+collective on the data path); the timed region is bracketed by barriers and the slowest rank's
+time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from sliding_window_attention_04_b300 import configs  # noqa: E402
+from sliding_window_attention_04_b300.inputs import layer_seed, make_qkv  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (unmasked FLOPs, SSSL mix) and % of B300 dense-BF16 peak"
+WORKLOAD_INDEX = 2  # ANDREA-120M shape
+FALLBACK_PEAK_TFLOPS = 1800.0
+
+
+def kernel_hash() -> str:
+    """Hash of the CUDA sources: ties committed ncu counters to the kernel they were taken on."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sliding_window_attention_04_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            h.update(name.encode())
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0.0)), "measured"
+    return FALLBACK_PEAK_TFLOPS, 1400.0, "fallback"
+
+
+def traffic_per_launch():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel."""
+    p = os.path.join(ROOT, "profiles", "attn_fwd_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons in the background during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def build_inputs(w, device):
+    """Per-layer seeded inputs: pinned host copies (for the end-to-end leg) and device copies."""
+    host, dev = [], []
+    for li, _ in enumerate(w.layers):
+        q, k, v = make_qkv(w.B, w.T, w.H, w.D, seed=layer_seed(w.index, li))
+        hq = [t.pin_memory() for t in (q, k, v)]
+        host.append(hq)
+        dev.append([t.to(device, non_blocking=True) for t in hq])
+    torch.cuda.synchronize(device)
+    return host, dev
+
+
+def oracle_sample_rows(w, budget_s: float) -> int:
+    """How many batch rows of every layer the float64 oracle can do in about `budget_s` seconds
+    (calibrated on one batch row of the first layer)."""
+    import oracle
+
+    q, k, v = make_qkv(1, w.T, w.H, w.D, seed=layer_seed(w.index, 0))
+    t0 = time.perf_counter()
+    oracle.attn_fwd(q, k, v, window=w.layers[0].window, causal=True, rope_base=w.rope_base, eps=w.eps)
+    per_row = time.perf_counter() - t0
+    return int(max(1, min(w.B, budget_s / max(per_row * len(w.layers), 1e-9))))
+
+
+def config_dict(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "D": w.D,
+            "layers": "SSSL x3: windows " + ",".join(str(l.window) for l in w.layers),
+            "qk_norm_eps": w.eps, "rope_base": w.rope_base, "mask": "causal + sliding window (W=T/2 on S)",
+            "l2": "no flush: inputs larger than L2 (each layer reads 151 MB, a step 1.8 GB)",
+            "parallelism": "replicas (one full workload per GPU)"}
+
+
+def run_reference(args, w, rank):
+    """The reference arm: the float64 oracle on the host cores, a bounded sample per step."""
+    import oracle
+
+    if rank != 0:
+        return
+    cores = oracle.num_threads()
+    per_step_budget = max(0.05, 120.0 / max(1, args.steps + args.warmup))
+    # sample unit: one batch row (all 12 heads, full T) of one layer, cycling through the layers
+    inputs = []
+    for li, layer in enumerate(w.layers):
+        q, k, v = make_qkv(w.B, w.T, w.H, w.D, seed=layer_seed(w.index, li))
+        inputs.append((q[:1].clone(), k[:1].clone(), v[:1].clone(), layer))
+    q, k, v, layer = inputs[0]
+    oracle.attn_fwd(q, k, v, window=layer.window, causal=True, rope_base=w.rope_base, eps=w.eps)
+    t0 = time.perf_counter()
+    oracle.attn_fwd(q, k, v, window=layer.window, causal=True, rope_base=w.rope_base, eps=w.eps)
+    unit_s = time.perf_counter() - t0
+    n_units = max(1, int(per_step_budget / max(unit_s, 1e-9)))
+    total_flops, total_s = 0, 0.0
+    for step in range(args.warmup + args.steps):
+        flops = 0
+        t0 = time.perf_counter()
+        for u in range(n_units):
+            q, k, v, layer = inputs[(step * n_units + u) % len(inputs)]
+            oracle.attn_fwd(q, k, v, window=layer.window, causal=layer.causal, rope_base=w.rope_base, eps=w.eps)
+            flops += configs.attn_flops(1, w.H, w.T, w.D, layer.window, layer.causal)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            total_flops += flops
+            total_s += dt
+    value = total_flops / total_s / 1e12
+    sample = (f"{n_units} x (one batch row, all {w.H} heads, T={w.T}) per step, cycling through the "
+              f"{len(w.layers)} layers of the workload")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = configs.workloads()[WORKLOAD_INDEX]
+
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+
+    from sliding_window_attention_04_b300 import attn
+
+    attn.attn_init(local_rank)
+    host, dev = build_inputs(w, device)
+    outs = [torch.empty_like(d[0]) for d in dev]
+    lses = [torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=device) for _ in dev]
+    stream = torch.cuda.current_stream(device)
+    step_flops = sum(configs.attn_flops(w.B, w.H, w.T, w.D, l.window, l.causal) for l in w.layers)
+
+    def step(ev=None):
+        for li, layer in enumerate(w.layers):
+            if ev is not None:
+                ev[2 * li].record(stream)
+            attn.attn_fwd(dev[li][0], dev[li][1], dev[li][2], window=layer.window, causal=layer.causal,
+                          rope_base=w.rope_base, eps=w.eps, out=outs[li], lse=lses[li], stream=stream)
+            if ev is not None:
+                ev[2 * li + 1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    st = attn.attn_device_status()
+    if st != 0:
+        raise SystemExit(f"device status after warm-up: {attn.status_string(st)}")
+
+    # ---- timed region: K steps, device-resident inputs ----
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(w.layers))] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    t_start.record(stream)
+    for kstep in range(args.steps):
+        step(events[kstep])
+    t_end.record(stream)
+    torch.cuda.synchronize(device)
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    kernel_ms = sum(ev[2 * li].elapsed_time(ev[2 * li + 1]) for ev in events for li in range(len(w.layers)))
+    st = attn.attn_device_status()
+    if st != 0:
+        raise SystemExit(f"device status after the timed region: {attn.status_string(st)}")
+    if dist:
+        t = torch.tensor([elapsed_ms, kernel_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms, kernel_ms = float(t[0]), float(t[1])
+
+    n_launch = args.steps * len(w.layers)
+    value = step_flops * args.steps * world / (elapsed_ms / 1e3) / 1e12
+    achieved = step_flops * args.steps / (kernel_ms / 1e3) / 1e12  # per GPU, kernel time only
+    peak, peak_sustained, peak_kind = peaks()
+
+    # ---- end to end through the public API: pinned host -> device, compute, device -> host ----
+    h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h_lse = [torch.empty(l.shape, dtype=l.dtype, pin_memory=True) for l in lses]
+    d_in = [torch.empty_like(dev[0][i]) for i in range(3)]
+    d_out, d_lse = torch.empty_like(outs[0]), torch.empty_like(lses[0])
+
+    def e2e_step():
+        for li, layer in enumerate(w.layers):
+            for i in range(3):
+                d_in[i].copy_(host[li][i], non_blocking=True)
+            attn.attn_fwd(d_in[0], d_in[1], d_in[2], window=layer.window, causal=layer.causal,
+                          rope_base=w.rope_base, eps=w.eps, out=d_out, lse=d_lse, stream=stream)
+            h_out[li].copy_(d_out, non_blocking=True)
+            h_lse[li].copy_(d_lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(device)
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+        dist.barrier()
+    e2e_value = step_flops * args.e2e_steps * world / (e2e_ms / 1e3) / 1e12
+    h2d = sum(t.numel() * t.element_size() for hl in host for t in hl)
+    d2h = sum(t.numel() * t.element_size() for t in h_out + h_lse)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        import oracle
+
+        nb = oracle_sample_rows(w, args.cpu_budget_s)
+        cores = oracle.num_threads()
+        flops = sum(configs.attn_flops(nb, w.H, w.T, w.D, l.window, l.causal) for l in w.layers)
+        samples = []  # inputs generated outside the timed part
+        for li, layer in enumerate(w.layers):
+            q, k, v = make_qkv(w.B, w.T, w.H, w.D, seed=layer_seed(w.index, li))
+            samples.append((q[:nb].clone(), k[:nb].clone(), v[:nb].clone(), layer))
+        t0 = time.perf_counter()
+        for q, k, v, layer in samples:
+            oracle.attn_fwd(q, k, v, window=layer.window, causal=layer.causal, rope_base=w.rope_base, eps=w.eps)
+        cpu_s = time.perf_counter() - t0
+        cpu = {"value": flops / cpu_s / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"batch rows 0..{nb - 1} of every layer (all {w.H} heads, T={w.T}); "
+                         f"{flops / 1e9:.2f} GFLOP in {cpu_s:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(w),
+        "pct_of_peak": value / world / peak * 100.0,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic_per_launch(),
+                     "peak_kind": f"{peak_kind} dense bf16 burst (sustained {peak_sustained})",
+                     "kernel": "attn_fwd (one launch per layer)",
+                     "achieved_basis": "algorithmic unmasked FLOPs per launch / mean CUDA-event launch time"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": args.e2e_steps},
+        "gpu_launches": n_launch,
+        "clocks": clocks,
+        "kernel_hash": kernel_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

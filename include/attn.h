@@ -1,0 +1,104 @@
+/*
+ * attn.h — C ABI of the B300 (sm_103a) attention forward library (libswa_attn.so).
+ *
+ * The one operation is the forward pass of a decoder's multi-head attention as the pages
+ * define it:
+ *   out = softmax(Q^ K^^T / sqrt(D)) V                ("geometry_of_andrea" page,
+ *                                                      "O que a Atenção Calcula",
+ *                                                      "Escalonamento por sqrt(d_k)")
+ * where Q^ and K^ are q and k after rotary position embedding and a parameter-free RMSNorm
+ * over the head dimension (habr "Autoresearch" deep dive, train.py listing: apply_rotary_emb,
+ * norm, CausalSelfAttention.forward), under a causal mask ("A Máscara Causal") and an optional
+ * sliding window passed the way the listing passes window_size=(W, 0) to FlashAttention: query i
+ * sees keys j with i - W <= j <= i. The "SSSL" layer pattern (three layers with W = T/2, then one
+ * with W = T; listing, _compute_window_sizes) is a per-call `window` choice made by the caller.
+ *
+ * Conventions shared by every call:
+ *  - Tensors are device pointers, row-major, contiguous, owned by the caller.
+ *  - q, k, v, out: bf16, layout [B, T, H, D] (element (b, t, h, d) at ((b*T + t)*H + h)*D + d).
+ *  - lse: fp32, layout [B, H, T].
+ *  - Positions are 0..T-1 for every batch row. The softmax scale is fixed at 1/sqrt(D).
+ *  - Q^ and K^ are rounded to bf16 before the products (as the listing's bf16 autocast does);
+ *    the norm and rotation before that rounding are evaluated in fp32 with a fixed sequence of
+ *    correctly rounded operations, so the rounded values are reproducible.
+ *  - Return value: ATTN_OK (0) or one of the negative ATTN_ERR_* codes below. Argument errors
+ *    are detected on the host before anything is launched.
+ *  - Calls are asynchronous on the given stream; results are ready when the stream is.
+ *  - Results are deterministic: the same inputs give bit-identical outputs.
+ */
+#ifndef SWA_ATTN_H
+#define SWA_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_OK 0
+#define ATTN_ERR_NOT_INITIALIZED (-1) /* attn_init has not succeeded yet (or attn_destroy ran) */
+#define ATTN_ERR_INVALID_ARG (-2)     /* null / misaligned pointer, bad size, aliasing, bad float */
+#define ATTN_ERR_UNSUPPORTED (-3)     /* valid request this build does not implement (e.g. D) */
+#define ATTN_ERR_CUDA (-4)            /* a CUDA runtime / driver call failed */
+#define ATTN_ERR_DEVICE_TIMEOUT (-5)  /* a kernel gave up on a bounded wait (see attn_device_status) */
+#define ATTN_ERR_NO_DEVICE (-6)       /* no usable sm_103 device */
+
+/*
+ * attn_init — prepare the library for CUDA device `device`.
+ * Checks the device (compute capability 10.3), records its SM count, raises the kernels'
+ * shared-memory limits, resolves the driver's tensor-map encoder, and allocates the device
+ * error word. Idempotent for the same device; a different device returns ATTN_ERR_INVALID_ARG
+ * until attn_destroy. Thread-safe. Does not change the calling thread's current device.
+ */
+int attn_init(int device);
+
+/*
+ * attn_fwd — one attention forward call.
+ *
+ *  q, k, v   [in]  bf16 [B, T, H, D], 16-byte aligned device pointers.
+ *  out       [out] bf16 [B, T, H, D], 16-byte aligned; must not overlap q, k, v or lse.
+ *  lse       [out] fp32 [B, H, T], natural-log log-sum-exp of the scaled scores of each query
+ *                  row (ln sum_j exp(q^_i . k^_j / sqrt(D))); may be NULL (not written).
+ *  B, H, T         >= 1; B*T*H*D < 2^31.
+ *  D               head dimension: 32, 64 or 128 (other values: ATTN_ERR_UNSUPPORTED).
+ *  window          < 0: no window. >= 0: query i sees keys j >= i - window (and, when
+ *                  causal == 0, also j <= i + window). window >= T - 1 equals no window.
+ *  causal          1: keys j <= i only ("A Máscara Causal"); 0: no causal cap.
+ *  rope_base       > 0: rotary embedding with this base (the pages use 10000); 0: RoPE off.
+ *                  Angle of pair i at position t: t * rope_base^(-2i/D), pairs (d, d + D/2).
+ *  eps             >= 0: parameter-free RMSNorm of q and k rows with this epsilon;
+ *                  < 0: no norm. (eps < 0 together with rope_base = 0 gives plain
+ *                  softmax(Q K^T / sqrt(D)) V.)
+ *  stream          a cudaStream_t (NULL = the legacy default stream) on the initialised device.
+ *
+ * The first call for a new (D, rope_base) pair, or for a T longer than any seen before with
+ * that pair, builds the cos/sin table on the device (a cudaMalloc and a synchronous copy);
+ * every later call allocates nothing and does not synchronise the host.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int T, int D,
+             int window, int causal, float rope_base, float eps, void* stream);
+
+/* attn_destroy — free the cos/sin tables and the error word; idempotent. The caller must make
+ * sure no attn_fwd work is still running. After it, attn_init may be called again. */
+void attn_destroy(void);
+
+/* attn_status_string — a static, human-readable name for a status code. Never NULL. */
+const char* attn_status_string(int status);
+
+/* attn_device_status — synchronise the device, read and clear the device error word.
+ * Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait since the last
+ * call, ATTN_ERR_NOT_INITIALIZED or ATTN_ERR_CUDA. */
+int attn_device_status(void);
+
+/* attn_selftest_wait_timeout — exercise the kernels' bounded-wait path without any fault.
+ * Launches one small kernel on `stream` that waits on a shared-memory barrier nothing will ever
+ * arrive on, using the same bounded wait (about 1.5 s of %globaltimer) as the attention kernels.
+ * The wait gives up, the kernel writes the timeout code to the device error word and returns
+ * normally; the context stays usable. A following attn_device_status() then returns
+ * ATTN_ERR_DEVICE_TIMEOUT. Not part of the computation (the pages have no counterpart); it
+ * exists so the failure-reporting path can be tested on real hardware. */
+int attn_selftest_wait_timeout(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWA_ATTN_H */

@@ -1,0 +1,140 @@
+"""Python binding of the C ABI in include/attn.h (libswa_attn.so), argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module only checks
+tensor properties, passes raw device pointers and the current CUDA stream, and turns status
+codes into exceptions. There is no fallback: if the library is missing, importing this module
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libswa_attn.so")
+
+ATTN_OK = 0
+ATTN_ERR_NOT_INITIALIZED = -1
+ATTN_ERR_INVALID_ARG = -2
+ATTN_ERR_UNSUPPORTED = -3
+ATTN_ERR_CUDA = -4
+ATTN_ERR_DEVICE_TIMEOUT = -5
+ATTN_ERR_NO_DEVICE = -6
+
+EXPORTED = ("attn_init", "attn_fwd", "attn_destroy", "attn_status_string", "attn_device_status",
+            "attn_selftest_wait_timeout")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"CUDA attention library not built: {LIB_PATH} is missing "
+                          "(run __graft_entry__.build() or sliding_window_attention_04_b300/csrc/build.py)")
+    lib = ctypes.CDLL(LIB_PATH)
+    c_int, c_float, c_void_p = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+    lib.attn_init.argtypes = [c_int]
+    lib.attn_init.restype = c_int
+    lib.attn_fwd.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                             c_int, c_int, c_float, c_float, c_void_p]
+    lib.attn_fwd.restype = c_int
+    lib.attn_destroy.argtypes = []
+    lib.attn_destroy.restype = None
+    lib.attn_status_string.argtypes = [c_int]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_device_status.argtypes = []
+    lib.attn_device_status.restype = c_int
+    lib.attn_selftest_wait_timeout.argtypes = [c_void_p]
+    lib.attn_selftest_wait_timeout.restype = c_int
+    return lib
+
+
+lib = _load()
+
+
+def status_string(code: int) -> str:
+    return lib.attn_status_string(int(code)).decode()
+
+
+def attn_init(device: int = 0) -> None:
+    rc = lib.attn_init(int(device))
+    if rc != ATTN_OK:
+        raise AttnError(rc, f"attn_init({device})")
+
+
+def attn_destroy() -> None:
+    lib.attn_destroy()
+
+
+def attn_device_status() -> int:
+    """Synchronise, read and clear the device error word; returns the status code."""
+    return int(lib.attn_device_status())
+
+
+def attn_selftest_wait_timeout(stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Launch the bounded-wait self test (see include/attn.h); check with attn_device_status()."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    rc = int(lib.attn_selftest_wait_timeout(ctypes.c_void_p(s.cuda_stream or None)))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_selftest_wait_timeout")
+
+
+def attn_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, lse_ptr: Optional[int], B: int, H: int, T: int,
+                 D: int, window: int, causal: int, rope_base: float, eps: float, stream: Optional[int]) -> int:
+    """Direct pass-through of the C call (pointers as integers); returns the status code."""
+    return int(lib.attn_fwd(ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+                            ctypes.c_void_p(out_ptr), ctypes.c_void_p(lse_ptr or None), int(B), int(H), int(T),
+                            int(D), int(window), int(causal), float(rope_base), float(eps),
+                            ctypes.c_void_p(stream or None)))
+
+
+def _check_input(name: str, t: torch.Tensor, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16 (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: int = -1, causal: bool = True,
+             rope_base: float = 10000.0, eps: float = 1e-6, out: Optional[torch.Tensor] = None,
+             lse: Optional[torch.Tensor] = None, return_lse: bool = True,
+             stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Attention forward on [B, T, H, D] bf16 CUDA tensors. Returns (out, lse [B, H, T] fp32 or None).
+
+    The call is asynchronous on `stream` (default: the current stream of q's device).
+    """
+    _check_input("q", q)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, D]")
+    B, T, H, D = q.shape
+    _check_input("k", k, q.shape)
+    _check_input("v", v, q.shape)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check_input("out", out, q.shape)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, T):
+            raise ValueError("lse must be a contiguous float32 [B, H, T] tensor")
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    rc = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                      lse.data_ptr() if lse is not None else None, B, H, T, D, int(window), int(bool(causal)),
+                      float(rope_base), float(eps), s.cuda_stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return out, lse

@@ -1,0 +1,289 @@
+// Host side of the C ABI declared in include/attn.h: argument validation, the cached cos/sin
+// tables, the device error word and kernel launches on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "attn.h"
+#include "attn_fwd_simple.cuh"
+
+namespace {
+
+struct RopeTable {
+  float2* ptr = nullptr;
+  int T = 0;  // positions covered
+};
+
+struct State {
+  std::mutex mu;
+  bool inited = false;
+  int device = -1;
+  int sm_count = 0;
+  int* d_err = nullptr;
+  std::map<std::pair<int, float>, RopeTable> tables;  // (D, base) -> table
+  std::vector<float2*> retired;                       // outgrown tables, freed at destroy
+  PFN_cuTensorMapEncodeTiled_v12000 encode_tiled = nullptr;
+};
+
+State& state() {
+  static State s;
+  return s;
+}
+
+// Runs `f` with `dev` as the current device and restores the caller's device afterwards.
+template <typename F>
+cudaError_t with_device(int dev, F&& f) {
+  int prev = -1;
+  cudaError_t e = cudaGetDevice(&prev);
+  if (e != cudaSuccess) return e;
+  if (prev != dev && (e = cudaSetDevice(dev)) != cudaSuccess) return e;
+  cudaError_t r = f();
+  if (prev != dev) cudaSetDevice(prev);
+  return r;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+template <int D>
+cudaError_t set_kernel_attrs() {
+  return cudaFuncSetAttribute(swa::attn_fwd_simple_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              swa::SimpleCfg<D>::kSmemBytes);
+}
+
+// cos / sin of t * base^(-2i/D) for t < T, i < D/2, evaluated in double, stored as fp32 pairs.
+cudaError_t build_table(int D, float base, int T, float2** out) {
+  std::vector<float2> h(static_cast<size_t>(T) * (D / 2));
+  for (int t = 0; t < T; ++t)
+    for (int i = 0; i < D / 2; ++i) {
+      const double theta = static_cast<double>(t) * std::pow(static_cast<double>(base), -2.0 * i / D);
+      h[static_cast<size_t>(t) * (D / 2) + i] = make_float2(static_cast<float>(std::cos(theta)),
+                                                            static_cast<float>(std::sin(theta)));
+    }
+  float2* d = nullptr;
+  cudaError_t e = cudaMalloc(&d, h.size() * sizeof(float2));
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpy(d, h.data(), h.size() * sizeof(float2), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(d);
+    return e;
+  }
+  *out = d;
+  return cudaSuccess;
+}
+
+// One CTA waits on an mbarrier that nothing arrives on; the bounded wait gives up and the
+// kernel records the timeout in the error word, then returns.
+__global__ void selftest_wait_timeout_kernel(int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    swa::mbar_init(&bar, 1);
+    swa::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !swa::mbar_wait(&bar, 0)) swa::report_error(err, swa::kDevErrTimeout);
+}
+
+template <int D>
+cudaError_t launch_simple(const swa::AttnParams& p, cudaStream_t stream) {
+  const int grid = p.B * p.H * p.n_qtiles;
+  swa::attn_fwd_simple_kernel<D><<<grid, swa::SimpleCfg<D>::kThreads, swa::SimpleCfg<D>::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_init(int device) {
+  State& s = state();
+  std::lock_guard<std::mutex> lock(s.mu);
+  if (s.inited) return device == s.device ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || count <= 0) {
+    cudaGetLastError();
+    return ATTN_ERR_NO_DEVICE;
+  }
+  if (device < 0 || device >= count) return ATTN_ERR_INVALID_ARG;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return ATTN_ERR_NO_DEVICE;
+  int* d_err = nullptr;
+  cudaError_t e = with_device(device, [&]() -> cudaError_t {
+    cudaError_t r;
+    if ((r = set_kernel_attrs<32>()) != cudaSuccess) return r;
+    if ((r = set_kernel_attrs<64>()) != cudaSuccess) return r;
+    if ((r = set_kernel_attrs<128>()) != cudaSuccess) return r;
+    if ((r = cudaMalloc(&d_err, sizeof(int))) != cudaSuccess) return r;
+    return cudaMemset(d_err, 0, sizeof(int));
+  });
+  if (e != cudaSuccess) {
+    if (d_err) cudaFree(d_err);
+    return ATTN_ERR_CUDA;
+  }
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult qres;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qres) !=
+          cudaSuccess ||
+      qres != cudaDriverEntryPointSuccess || fn == nullptr) {
+    cudaFree(d_err);
+    return ATTN_ERR_CUDA;
+  }
+  s.encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  s.d_err = d_err;
+  s.device = device;
+  s.sm_count = prop.multiProcessorCount;
+  s.inited = true;
+  return ATTN_OK;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int T, int D,
+             int window, int causal, float rope_base, float eps, void* stream) {
+  // ---- argument checks (host only, nothing launched) ----
+  if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || T < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(rope_base) || rope_base < 0.f) return ATTN_ERR_INVALID_ARG;
+  if (std::isnan(eps) || std::isinf(eps)) return ATTN_ERR_INVALID_ARG;
+  const long long n_elem = static_cast<long long>(B) * T * H * D;
+  if (n_elem >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+  const size_t tensor_bytes = static_cast<size_t>(n_elem) * 2;
+  const size_t lse_bytes = static_cast<size_t>(B) * H * T * 4;
+  if (overlaps(out, tensor_bytes, q, tensor_bytes) || overlaps(out, tensor_bytes, k, tensor_bytes) ||
+      overlaps(out, tensor_bytes, v, tensor_bytes))
+    return ATTN_ERR_INVALID_ARG;
+  if (lse && (overlaps(lse, lse_bytes, q, tensor_bytes) || overlaps(lse, lse_bytes, k, tensor_bytes) ||
+              overlaps(lse, lse_bytes, v, tensor_bytes) || overlaps(lse, lse_bytes, out, tensor_bytes)))
+    return ATTN_ERR_INVALID_ARG;
+  if (D != 32 && D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+
+  State& s = state();
+  float2* table = nullptr;
+  int* d_err = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(s.mu);
+    if (!s.inited) return ATTN_ERR_NOT_INITIALIZED;
+    d_err = s.d_err;
+    if (rope_base > 0.f) {
+      RopeTable& t = s.tables[std::make_pair(D, rope_base)];
+      if (t.T < T) {
+        float2* fresh = nullptr;
+        const int want = T;
+        if (with_device(s.device, [&] { return build_table(D, rope_base, want, &fresh); }) != cudaSuccess)
+          return ATTN_ERR_CUDA;
+        if (t.ptr) s.retired.push_back(t.ptr);
+        t.ptr = fresh;
+        t.T = want;
+      }
+      table = t.ptr;
+    }
+  }
+
+  swa::AttnParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.rope = table;
+  p.err = d_err;
+  p.B = B;
+  p.H = H;
+  p.T = T;
+  p.window = window < 0 ? -1 : window;
+  p.causal = causal;
+  p.use_norm = eps >= 0.f ? 1 : 0;
+  p.eps = eps >= 0.f ? eps : 0.f;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+  p.n_qtiles = (T + swa::kTile - 1) / swa::kTile;
+  if (static_cast<long long>(B) * H * p.n_qtiles >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (D) {
+    case 32: e = launch_simple<32>(p, st); break;
+    case 64: e = launch_simple<64>(p, st); break;
+    default: e = launch_simple<128>(p, st); break;
+  }
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+void attn_destroy(void) {
+  State& s = state();
+  std::lock_guard<std::mutex> lock(s.mu);
+  if (!s.inited) return;
+  with_device(s.device, [&]() -> cudaError_t {
+    for (auto& kv : s.tables)
+      if (kv.second.ptr) cudaFree(kv.second.ptr);
+    for (float2* ptr : s.retired) cudaFree(ptr);
+    if (s.d_err) cudaFree(s.d_err);
+    return cudaSuccess;
+  });
+  s.tables.clear();
+  s.retired.clear();
+  s.d_err = nullptr;
+  s.encode_tiled = nullptr;
+  s.inited = false;
+  s.device = -1;
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_NOT_INITIALIZED: return "ATTN_ERR_NOT_INITIALIZED";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT";
+    case ATTN_ERR_NO_DEVICE: return "ATTN_ERR_NO_DEVICE";
+    default: return "ATTN_ERR_UNKNOWN";
+  }
+}
+
+int attn_selftest_wait_timeout(void* stream) {
+  State& s = state();
+  int* d_err = nullptr;
+  int dev = -1;
+  {
+    std::lock_guard<std::mutex> lock(s.mu);
+    if (!s.inited) return ATTN_ERR_NOT_INITIALIZED;
+    d_err = s.d_err;
+    dev = s.device;
+  }
+  cudaError_t e = with_device(dev, [&]() -> cudaError_t {
+    selftest_wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(d_err);
+    return cudaGetLastError();
+  });
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_device_status(void) {
+  State& s = state();
+  std::lock_guard<std::mutex> lock(s.mu);
+  if (!s.inited) return ATTN_ERR_NOT_INITIALIZED;
+  int h = 0;
+  cudaError_t e = with_device(s.device, [&]() -> cudaError_t {
+    cudaError_t r;
+    if ((r = cudaDeviceSynchronize()) != cudaSuccess) return r;
+    if ((r = cudaMemcpy(&h, s.d_err, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess) return r;
+    return cudaMemset(s.d_err, 0, sizeof(int));
+  });
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  return h == 0 ? ATTN_OK : ATTN_ERR_DEVICE_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+"""The five workloads at full size, in the launch configuration the benchmark times.
+
+The oracle checks sampled rows one by one at these sizes (every row for one 12M layer), and
+properties that hold at any size are checked on every output element.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import assert_close, gpu_fwd
+from sliding_window_attention_04_b300 import configs
+from sliding_window_attention_04_b300.inputs import layer_seed, make_qkv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from sliding_window_attention_04_b300 import attn
+
+    attn.attn_init(0)
+    yield attn
+
+
+def sample_rows(B, H, T, window, n, seed):
+    """Random (b, h, i) rows plus the structurally interesting ones: first and last rows,
+    both sides of every 128-row tile edge, and both sides of the window edge."""
+    rng = np.random.default_rng(seed)
+    special = {0, 1, 2, T - 1, T - 2}
+    for e in range(128, T, 128):
+        special |= {e - 1, e}
+    if 0 < window < T:
+        special |= {window - 1, window, window + 1, window + 127, window + 128}
+    special = sorted(i for i in special if 0 <= i < T)
+    rows = [(int(rng.integers(B)), int(rng.integers(H)), i) for i in special]
+    rows += [(int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(T))) for _ in range(n)]
+    return np.array(rows, dtype=np.int32)
+
+
+def check_sampled(q, k, v, layer, rope_base, eps, n, seed, what):
+    B, T, H, D = q.shape
+    out_t, lse_t = gpu_fwd(q, k, v, window=layer.window, causal=layer.causal, rope_base=rope_base, eps=eps,
+                           return_tensors=True)
+    # properties over every element: finite, and each output is a convex combination of v rows
+    assert torch.isfinite(out_t).all() and torch.isfinite(lse_t).all(), what
+    vmax = v.float().abs().amax(dim=1).cuda()  # [B, H, D] max over positions
+    assert (out_t.float().abs() <= vmax[:, None] * (1 + 2 ** -7) + 1e-6).all(), what
+    rows = sample_rows(B, H, T, layer.window, n, seed)
+    ref, lref = oracle.attn_rows(q, k, v, rows, window=layer.window, causal=layer.causal, rope_base=rope_base,
+                                 eps=eps)
+    out = out_t.cpu().to(torch.float64).numpy()
+    lse = lse_t.cpu().to(torch.float64).numpy()
+    got = np.stack([out[b, i, h] for b, h, i in rows])
+    lgot = np.array([lse[b, h, i] for b, h, i in rows])
+    return assert_close(got, ref, lgot, lref, what)
+
+
+@pytest.mark.parametrize("widx", [1, 2, 3])
+def test_andrea_workloads_sampled(widx):
+    w = configs.workloads()[widx]
+    seen = set()
+    for li, layer in enumerate(w.layers):
+        if (layer.window, layer.causal) in seen and li != len(w.layers) - 1:
+            continue  # one S layer and the final L layer carry every distinct launch shape
+        seen.add((layer.window, layer.causal))
+        q, k, v = make_qkv(w.B, w.T, w.H, w.D, seed=layer_seed(w.index, li))
+        check_sampled(q, k, v, layer, w.rope_base, w.eps, 600, 1000 * widx + li, f"{w.name} layer {li}")
+
+
+def test_andrea_12m_layer_full():
+    """One S layer of the ANDREA-12M workload compared on every output element."""
+    w = configs.workloads()[1]
+    q, k, v = make_qkv(w.B, w.T, w.H, w.D, seed=layer_seed(w.index, 0))
+    out, lse = gpu_fwd(q, k, v, window=w.layers[0].window, causal=True, rope_base=w.rope_base, eps=w.eps)
+    ref, lref = oracle.attn_fwd(q, k, v, window=w.layers[0].window, causal=True, rope_base=w.rope_base, eps=w.eps)
+    assert_close(out, ref, lse, lref, "12M layer 0 full")
+
+
+@pytest.mark.parametrize("T", [1024, 2048, 4096, 8192])
+def test_sweep_sampled(T):
+    w = [x for x in configs.sweep_workloads() if x.T == T][0]
+    for li, layer in enumerate(w.layers):
+        q, k, v = make_qkv(w.B, w.T, w.H, w.D, seed=layer_seed(w.index, 10 * li + T // 1024))
+        check_sampled(q, k, v, layer, w.rope_base, w.eps, 300, T + li, f"{w.name} layer {li}")
