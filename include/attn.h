@@ -40,6 +40,7 @@ extern "C" {
 #define ATTN_ERR_CUDA (-4)            /* a CUDA runtime / driver call failed */
 #define ATTN_ERR_DEVICE_TIMEOUT (-5)  /* a kernel gave up on a bounded wait (see attn_device_status) */
 #define ATTN_ERR_NO_DEVICE (-6)       /* no usable sm_103 device */
+#define ATTN_ERR_SCRATCH_LIMIT (-7)   /* attn_fwd_noalloc: T * D / 2 exceeds its fixed cos/sin scratch */
 
 /*
  * attn_init — prepare the library for CUDA device `device`.
@@ -96,6 +97,36 @@ int attn_device_status(void);
  * ATTN_ERR_DEVICE_TIMEOUT. Not part of the computation (the pages have no counterpart); it
  * exists so the failure-reporting path can be tested on real hardware. */
 int attn_selftest_wait_timeout(void* stream);
+
+/* attn_fwd_noalloc — the same forward call as attn_fwd, for callers that must not allocate.
+ *
+ * The pages have no counterpart; this is a deployment convenience. Some callers cannot call
+ * cudaMalloc: serving processes whose device memory is carved up in advance by a framework
+ * allocator or a fixed-size memory pool (a library allocation outside it can fail or break the
+ * budget), and plug-in hosts that forbid a library from allocating device memory behind their
+ * back. attn_fwd allocates its cos/sin table on the first call for a (D, rope_base) pair and
+ * needs attn_init, which allocates the device error word; this entry point needs neither.
+ *
+ * Arguments, layouts, semantics and return codes are those of attn_fwd. Differences:
+ *  - Everything it needs beyond the caller's tensors lives in one file-scope device array of the
+ *    library (4 MiB + 256 bytes), which every GPU that loads the library holds until the process
+ *    exits: the error word and a cos/sin table of at most 524288 (cos, sin) pairs. Requests with
+ *    rope_base > 0 and T * D / 2 > 524288 (for example T > 16384 at D = 64, T > 8192 at D = 128)
+ *    return ATTN_ERR_SCRATCH_LIMIT without launching anything.
+ *  - It runs on the calling thread's current device; `stream` must belong to that device.
+ *    attn_init is not required.
+ *  - The first call on a device does a one-time set-up on the host (checks the device, raises the
+ *    kernels' shared-memory limits, looks up the array's device address); make that first call
+ *    before any stream capture.
+ *  - Each call enqueues, on `stream`, a small kernel that clears the error word and rebuilds the
+ *    table for (T, D, rope_base) in the array (cos / sin evaluated in double on the device,
+ *    stored as fp32), then the attention kernel. All calls share the one array and it keeps the
+ *    last call's contents: calls whose work overlaps on the GPU (other streams, other threads)
+ *    race on it and must be serialised by the caller.
+ *  - A bounded-wait timeout of this path is recorded in that shared error word only; it is not
+ *    reported by attn_device_status. */
+int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int T,
+                     int D, int window, int causal, float rope_base, float eps, void* stream);
 
 #ifdef __cplusplus
 }

@@ -23,9 +23,10 @@ ATTN_ERR_UNSUPPORTED = -3
 ATTN_ERR_CUDA = -4
 ATTN_ERR_DEVICE_TIMEOUT = -5
 ATTN_ERR_NO_DEVICE = -6
+ATTN_ERR_SCRATCH_LIMIT = -7
 
 EXPORTED = ("attn_init", "attn_fwd", "attn_destroy", "attn_status_string", "attn_device_status",
-            "attn_selftest_wait_timeout")
+            "attn_selftest_wait_timeout", "attn_fwd_noalloc")
 
 
 class AttnError(RuntimeError):
@@ -53,6 +54,8 @@ def _load() -> ctypes.CDLL:
     lib.attn_device_status.restype = c_int
     lib.attn_selftest_wait_timeout.argtypes = [c_void_p]
     lib.attn_selftest_wait_timeout.restype = c_int
+    lib.attn_fwd_noalloc.argtypes = list(lib.attn_fwd.argtypes)
+    lib.attn_fwd_noalloc.restype = c_int
     return lib
 
 
@@ -93,6 +96,19 @@ def attn_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, lse_ptr: Opti
                             ctypes.c_void_p(out_ptr), ctypes.c_void_p(lse_ptr or None), int(B), int(H), int(T),
                             int(D), int(window), int(causal), float(rope_base), float(eps),
                             ctypes.c_void_p(stream or None)))
+
+
+def attn_fwd_noalloc_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, lse_ptr: Optional[int], B: int, H: int,
+                         T: int, D: int, window: int, causal: int, rope_base: float, eps: float,
+                         stream: Optional[int]) -> int:
+    """Pass-through of the allocation-free C call (see include/attn.h); returns the status code.
+
+    For callers that must not allocate device memory: the library keeps what it needs in a
+    fixed device array instead, so the only memory involved is the caller's own tensors."""
+    return int(lib.attn_fwd_noalloc(ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+                                    ctypes.c_void_p(out_ptr), ctypes.c_void_p(lse_ptr or None), int(B), int(H),
+                                    int(T), int(D), int(window), int(causal), float(rope_base), float(eps),
+                                    ctypes.c_void_p(stream or None)))
 
 
 def _check_input(name: str, t: torch.Tensor, shape=None):

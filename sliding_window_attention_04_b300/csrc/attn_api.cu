@@ -103,6 +103,84 @@ cudaError_t launch_simple(const swa::AttnParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// ---- allocation-free variant: everything it needs beyond the caller's tensors lives here ----
+// Layout: bytes [0, 256) hold the device error word, then kNoAllocTablePairs (cos, sin) pairs.
+constexpr size_t kNoAllocHeaderBytes = 256;
+constexpr size_t kNoAllocTablePairs = size_t(1) << 19;  // T * D / 2 <= 524288 pairs (4 MiB)
+constexpr size_t kNoAllocBytes = kNoAllocHeaderBytes + kNoAllocTablePairs * sizeof(float2);
+
+// Fills the cos / sin table for (T, D, base) and clears the error word. Runs on the caller's
+// stream right before the attention kernel, so each call starts from a clean state.
+__global__ void noalloc_prepare_kernel(unsigned char* scratch, int T, int D, float base) {
+  float2* table = reinterpret_cast<float2*>(scratch + kNoAllocHeaderBytes);
+  const int half = D / 2;
+  const size_t n = base > 0.f ? static_cast<size_t>(T) * half : 0;
+  for (size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
+       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(idx / half), i = static_cast<int>(idx % half);
+    const double theta = static_cast<double>(t) * pow(static_cast<double>(base), -2.0 * i / D);
+    double sn, cs;
+    sincos(theta, &sn, &cs);
+    table[idx] = make_float2(static_cast<float>(cs), static_cast<float>(sn));
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(scratch) = 0;
+}
+
+struct NoAllocDevice {
+  unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on that device
+};
+
+std::mutex& noalloc_mutex() {
+  static std::mutex m;
+  return m;
+}
+
+std::map<int, NoAllocDevice>& noalloc_devices() {
+  static std::map<int, NoAllocDevice> m;
+  return m;
+}
+
+}  // namespace
+
+// The allocation-free entry point's scratch. In host code this name is only a stand-in for the
+// device array; its device address comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+namespace {
+
+// First use on the current device: check it, raise the kernels' shared-memory limits and look
+// up the device address of the scratch array. Returns ATTN_OK or an error code.
+int noalloc_setup(int* dev_out, unsigned char** scratch_out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(noalloc_mutex());
+  auto it = noalloc_devices().find(dev);
+  if (it == noalloc_devices().end()) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (major != 10 || minor != 3) return ATTN_ERR_NO_DEVICE;
+    if (set_kernel_attrs<32>() != cudaSuccess || set_kernel_attrs<64>() != cudaSuccess ||
+        set_kernel_attrs<128>() != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    unsigned char* ptr = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    NoAllocDevice d;
+    d.scratch = ptr;
+    it = noalloc_devices().emplace(dev, d).first;
+  }
+  *dev_out = dev;
+  *scratch_out = it->second.scratch;
+  return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -250,6 +328,7 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
     case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT";
     case ATTN_ERR_NO_DEVICE: return "ATTN_ERR_NO_DEVICE";
+    case ATTN_ERR_SCRATCH_LIMIT: return "ATTN_ERR_SCRATCH_LIMIT";
     default: return "ATTN_ERR_UNKNOWN";
   }
 }
@@ -284,6 +363,69 @@ int attn_device_status(void) {
   });
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return h == 0 ? ATTN_OK : ATTN_ERR_DEVICE_TIMEOUT;
+}
+
+int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int T,
+                     int D, int window, int causal, float rope_base, float eps, void* stream) {
+  // ---- the same host-side checks as attn_fwd ----
+  if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || T < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(rope_base) || rope_base < 0.f) return ATTN_ERR_INVALID_ARG;
+  if (std::isnan(eps) || std::isinf(eps)) return ATTN_ERR_INVALID_ARG;
+  const long long n_elem = static_cast<long long>(B) * T * H * D;
+  if (n_elem >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+  const size_t tensor_bytes = static_cast<size_t>(n_elem) * 2;
+  const size_t lse_bytes = static_cast<size_t>(B) * H * T * 4;
+  if (overlaps(out, tensor_bytes, q, tensor_bytes) || overlaps(out, tensor_bytes, k, tensor_bytes) ||
+      overlaps(out, tensor_bytes, v, tensor_bytes))
+    return ATTN_ERR_INVALID_ARG;
+  if (lse && (overlaps(lse, lse_bytes, q, tensor_bytes) || overlaps(lse, lse_bytes, k, tensor_bytes) ||
+              overlaps(lse, lse_bytes, v, tensor_bytes) || overlaps(lse, lse_bytes, out, tensor_bytes)))
+    return ATTN_ERR_INVALID_ARG;
+  if (D != 32 && D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  // ---- the fixed-size scratch bounds the cos / sin table ----
+  if (rope_base > 0.f && static_cast<size_t>(T) * (D / 2) > kNoAllocTablePairs) return ATTN_ERR_SCRATCH_LIMIT;
+  const int n_qtiles = (T + swa::kTile - 1) / swa::kTile;
+  if (static_cast<long long>(B) * H * n_qtiles >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+
+  int dev = -1;
+  unsigned char* scratch = nullptr;
+  const int rc = noalloc_setup(&dev, &scratch);
+  if (rc != ATTN_OK) return rc;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t pairs = rope_base > 0.f ? static_cast<size_t>(T) * (D / 2) : 0;
+  const int prep_blocks = static_cast<int>(pairs == 0 ? 1 : (pairs + 255) / 256 < 1184 ? (pairs + 255) / 256 : 1184);
+  noalloc_prepare_kernel<<<prep_blocks, 256, 0, st>>>(scratch, T, D, rope_base);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+
+  swa::AttnParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.rope = rope_base > 0.f ? reinterpret_cast<const float2*>(scratch + kNoAllocHeaderBytes) : nullptr;
+  p.err = reinterpret_cast<int*>(scratch);
+  p.B = B;
+  p.H = H;
+  p.T = T;
+  p.window = window < 0 ? -1 : window;
+  p.causal = causal;
+  p.use_norm = eps >= 0.f ? 1 : 0;
+  p.eps = eps >= 0.f ? eps : 0.f;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+  p.n_qtiles = n_qtiles;
+  cudaError_t e;
+  switch (D) {
+    case 32: e = launch_simple<32>(p, st); break;
+    case 64: e = launch_simple<64>(p, st); break;
+    default: e = launch_simple<128>(p, st); break;
+  }
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // extern "C"

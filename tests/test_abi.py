@@ -47,6 +47,7 @@ def test_status_strings(binding):
     assert binding.status_string(0) == "ATTN_OK"
     assert binding.status_string(-2) == "ATTN_ERR_INVALID_ARG"
     assert binding.status_string(-5) == "ATTN_ERR_DEVICE_TIMEOUT"
+    assert binding.status_string(-7) == "ATTN_ERR_SCRATCH_LIMIT"
     assert binding.status_string(12345) == "ATTN_ERR_UNKNOWN"
 
 
