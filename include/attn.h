@@ -73,9 +73,22 @@ int attn_init(int device);
  * The first call for a new (D, rope_base) pair, or for a T longer than any seen before with
  * that pair, builds the cos/sin table on the device (a cudaMalloc and a synchronous copy);
  * every later call allocates nothing and does not synchronise the host.
+ *
+ * The persistent kernel (D = 32, 64) hands out work through a pair of device counters owned by
+ * the library; each call takes the next of 256 such pairs, and the kernel resets its pair when
+ * it finishes. Calls issued one after another on a stream can therefore be repeated without
+ * limit, and up to 256 calls may run at the same time on different streams.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int T, int D,
              int window, int causal, float rope_base, float eps, void* stream);
+
+/* attn_fwd_kernel — which kernel attn_fwd launches for head dimension D on the initialised
+ * device: 1 = the warp-specialised persistent kernel (TMA-fed K/V ring, tcgen05 MMAs into TMEM,
+ * separate prologue, MMA and softmax warps; D = 32 and 64), 0 = the single-warpgroup kernel
+ * (D = 128, or when the warp-specialised kernel was not compiled to the register count its
+ * run-time register split needs). ATTN_ERR_UNSUPPORTED for other D, ATTN_ERR_NOT_INITIALIZED
+ * before attn_init. Both kernels compute the same function (see attn_fwd). */
+int attn_fwd_kernel(int D);
 
 /* attn_destroy — free the cos/sin tables and the error word; idempotent. The caller must make
  * sure no attn_fwd work is still running. After it, attn_init may be called again. */

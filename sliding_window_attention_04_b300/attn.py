@@ -26,7 +26,7 @@ ATTN_ERR_NO_DEVICE = -6
 ATTN_ERR_SCRATCH_LIMIT = -7
 
 EXPORTED = ("attn_init", "attn_fwd", "attn_destroy", "attn_status_string", "attn_device_status",
-            "attn_selftest_wait_timeout", "attn_fwd_noalloc")
+            "attn_selftest_wait_timeout", "attn_fwd_noalloc", "attn_fwd_kernel")
 
 
 class AttnError(RuntimeError):
@@ -56,6 +56,8 @@ def _load() -> ctypes.CDLL:
     lib.attn_selftest_wait_timeout.restype = c_int
     lib.attn_fwd_noalloc.argtypes = list(lib.attn_fwd.argtypes)
     lib.attn_fwd_noalloc.restype = c_int
+    lib.attn_fwd_kernel.argtypes = [c_int]
+    lib.attn_fwd_kernel.restype = c_int
     return lib
 
 
@@ -79,6 +81,14 @@ def attn_destroy() -> None:
 def attn_device_status() -> int:
     """Synchronise, read and clear the device error word; returns the status code."""
     return int(lib.attn_device_status())
+
+
+def attn_fwd_kernel(D: int) -> str:
+    """Name of the kernel attn_fwd launches for head dimension D ("ws" or "simple")."""
+    rc = int(lib.attn_fwd_kernel(int(D)))
+    if rc < 0:
+        raise AttnError(rc, f"attn_fwd_kernel({D})")
+    return "ws" if rc == 1 else "simple"
 
 
 def attn_selftest_wait_timeout(stream: Optional[torch.cuda.Stream] = None) -> None:

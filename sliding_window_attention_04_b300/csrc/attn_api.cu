@@ -14,6 +14,7 @@
 
 #include "attn.h"
 #include "attn_fwd_simple.cuh"
+#include "attn_fwd_ws.cuh"
 
 namespace {
 
@@ -22,12 +23,22 @@ struct RopeTable {
   int T = 0;  // positions covered
 };
 
+// Ticket counters of the persistent kernel: one (ticket, exits) pair per slot, 128 bytes apart.
+// Each call takes the next slot; the kernel's last CTA resets its pair to zero on exit, so calls
+// that follow each other on a stream reuse slots safely, and up to kSchedSlots calls may be in
+// flight at once on different streams.
+constexpr int kSchedSlots = 256;
+constexpr int kSchedStride = 32;  // ints per slot
+
 struct State {
   std::mutex mu;
   bool inited = false;
   int device = -1;
   int sm_count = 0;
   int* d_err = nullptr;
+  int* d_sched = nullptr;
+  unsigned sched_next = 0;
+  bool ws_ok[2] = {false, false};  // warp-specialised kernel usable for D = 32, 64
   std::map<std::pair<int, float>, RopeTable> tables;  // (D, base) -> table
   std::vector<float2*> retired;                       // outgrown tables, freed at destroy
   PFN_cuTensorMapEncodeTiled_v12000 encode_tiled = nullptr;
@@ -61,6 +72,40 @@ template <int D>
 cudaError_t set_kernel_attrs() {
   return cudaFuncSetAttribute(swa::attn_fwd_simple_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               swa::SimpleCfg<D>::kSmemBytes);
+}
+
+// The warp-specialised kernel re-divides its registers at run time (setmaxnreg): the softmax
+// warpgroups grow to 176 per thread, the others shrink to 104 and 56. That budget adds up to the
+// 65536 registers of the launch only if the kernel was compiled to exactly 128 per thread;
+// with any other count the kernel is not used.
+template <int D>
+cudaError_t set_ws_attrs(bool* usable) {
+  *usable = false;
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, swa::attn_fwd_ws_kernel<D>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != 128) return cudaSuccess;
+  e = cudaFuncSetAttribute(swa::attn_fwd_ws_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           swa::WsCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  *usable = true;
+  return cudaSuccess;
+}
+
+// 4-D view (d, h, t, b) of a [B, T, H, D] bf16 tensor; one box is one 128-row tile of one head,
+// written to shared memory in the tensor core's swizzled layout (128-byte rows: 128-byte swizzle,
+// 64-byte rows: 64-byte swizzle). Rows past T read as zero and are not written by stores.
+CUresult encode_tile_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* map, const void* base, int B,
+                         int H, int T, int D) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                                 static_cast<cuuint64_t>(T) * H * D * 2};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(swa::kTile), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, D == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 // cos / sin of t * base^(-2i/D) for t < T, i < D/2, evaluated in double, stored as fp32 pairs.
@@ -101,6 +146,23 @@ cudaError_t launch_simple(const swa::AttnParams& p, cudaStream_t stream) {
   const int grid = p.B * p.H * p.n_qtiles;
   swa::attn_fwd_simple_kernel<D><<<grid, swa::SimpleCfg<D>::kThreads, swa::SimpleCfg<D>::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int D>
+int launch_ws(const swa::AttnParams& p, PFN_cuTensorMapEncodeTiled_v12000 encode, int sm_count, int* sched,
+              cudaStream_t stream) {
+  swa::WsMaps maps;
+  if (encode_tile_map(encode, &maps.q, p.q, p.B, p.H, p.T, D) != CUDA_SUCCESS ||
+      encode_tile_map(encode, &maps.k, p.k, p.B, p.H, p.T, D) != CUDA_SUCCESS ||
+      encode_tile_map(encode, &maps.v, p.v, p.B, p.H, p.T, D) != CUDA_SUCCESS ||
+      encode_tile_map(encode, &maps.out, p.out, p.B, p.H, p.T, D) != CUDA_SUCCESS)
+    return ATTN_ERR_CUDA;
+  const long long units = static_cast<long long>(p.B) * p.H * ((p.T + 2 * swa::kTile - 1) / (2 * swa::kTile));
+  if (units >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+  const int grid = static_cast<int>(units < sm_count ? units : sm_count);
+  swa::attn_fwd_ws_kernel<D><<<grid, swa::WsCfg<D>::kThreads, swa::WsCfg<D>::kSmemBytes, stream>>>(
+      p, maps, sched, static_cast<int>(units));
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 // ---- allocation-free variant: everything it needs beyond the caller's tensors lives here ----
@@ -199,16 +261,25 @@ int attn_init(int device) {
   if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return ATTN_ERR_CUDA;
   if (prop.major != 10 || prop.minor != 3) return ATTN_ERR_NO_DEVICE;
   int* d_err = nullptr;
+  int* d_sched = nullptr;
+  bool ws_ok[2] = {false, false};
   cudaError_t e = with_device(device, [&]() -> cudaError_t {
     cudaError_t r;
     if ((r = set_kernel_attrs<32>()) != cudaSuccess) return r;
     if ((r = set_kernel_attrs<64>()) != cudaSuccess) return r;
     if ((r = set_kernel_attrs<128>()) != cudaSuccess) return r;
+    if ((r = set_ws_attrs<32>(&ws_ok[0])) != cudaSuccess) return r;
+    if ((r = set_ws_attrs<64>(&ws_ok[1])) != cudaSuccess) return r;
     if ((r = cudaMalloc(&d_err, sizeof(int))) != cudaSuccess) return r;
-    return cudaMemset(d_err, 0, sizeof(int));
+    if ((r = cudaMemset(d_err, 0, sizeof(int))) != cudaSuccess) return r;
+    const size_t sched_bytes = sizeof(int) * kSchedSlots * kSchedStride;
+    if ((r = cudaMalloc(&d_sched, sched_bytes)) != cudaSuccess) return r;
+    if ((r = cudaMemset(d_sched, 0, sched_bytes)) != cudaSuccess) return r;
+    return cudaDeviceSynchronize();
   });
   if (e != cudaSuccess) {
     if (d_err) cudaFree(d_err);
+    if (d_sched) cudaFree(d_sched);
     return ATTN_ERR_CUDA;
   }
   void* fn = nullptr;
@@ -217,10 +288,15 @@ int attn_init(int device) {
           cudaSuccess ||
       qres != cudaDriverEntryPointSuccess || fn == nullptr) {
     cudaFree(d_err);
+    cudaFree(d_sched);
     return ATTN_ERR_CUDA;
   }
   s.encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   s.d_err = d_err;
+  s.d_sched = d_sched;
+  s.sched_next = 0;
+  s.ws_ok[0] = ws_ok[0];
+  s.ws_ok[1] = ws_ok[1];
   s.device = device;
   s.sm_count = prop.multiProcessorCount;
   s.inited = true;
@@ -252,10 +328,21 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
   State& s = state();
   float2* table = nullptr;
   int* d_err = nullptr;
+  int* sched = nullptr;
+  bool use_ws = false;
+  int sm_count = 0;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   {
     std::lock_guard<std::mutex> lock(s.mu);
     if (!s.inited) return ATTN_ERR_NOT_INITIALIZED;
     d_err = s.d_err;
+    use_ws = (D == 32 && s.ws_ok[0]) || (D == 64 && s.ws_ok[1]);
+    if (use_ws) {
+      sched = s.d_sched + static_cast<size_t>(s.sched_next % kSchedSlots) * kSchedStride;
+      ++s.sched_next;
+    }
+    sm_count = s.sm_count;
+    encode = s.encode_tiled;
     if (rope_base > 0.f) {
       RopeTable& t = s.tables[std::make_pair(D, rope_base)];
       if (t.T < T) {
@@ -291,6 +378,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
   if (static_cast<long long>(B) * H * p.n_qtiles >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (use_ws) return D == 32 ? launch_ws<32>(p, encode, sm_count, sched, st) : launch_ws<64>(p, encode, sm_count, sched, st);
   cudaError_t e;
   switch (D) {
     case 32: e = launch_simple<32>(p, st); break;
@@ -298,6 +386,16 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
     default: e = launch_simple<128>(p, st); break;
   }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_fwd_kernel(int D) {
+  State& s = state();
+  std::lock_guard<std::mutex> lock(s.mu);
+  if (!s.inited) return ATTN_ERR_NOT_INITIALIZED;
+  if (D == 32) return s.ws_ok[0] ? 1 : 0;
+  if (D == 64) return s.ws_ok[1] ? 1 : 0;
+  if (D == 128) return 0;
+  return ATTN_ERR_UNSUPPORTED;
 }
 
 void attn_destroy(void) {
@@ -309,8 +407,11 @@ void attn_destroy(void) {
       if (kv.second.ptr) cudaFree(kv.second.ptr);
     for (float2* ptr : s.retired) cudaFree(ptr);
     if (s.d_err) cudaFree(s.d_err);
+    if (s.d_sched) cudaFree(s.d_sched);
     return cudaSuccess;
   });
+  s.d_sched = nullptr;
+  s.ws_ok[0] = s.ws_ok[1] = false;
   s.tables.clear();
   s.retired.clear();
   s.d_err = nullptr;

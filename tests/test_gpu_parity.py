@@ -192,3 +192,34 @@ def test_destroy_and_reinit():
     o2, _ = attn.attn_fwd(q, k, v)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2)
+
+
+def test_fast_kernel_is_used_for_d32_d64():
+    from sliding_window_attention_04_b300 import attn
+
+    assert attn.attn_fwd_kernel(32) == "ws"
+    assert attn.attn_fwd_kernel(64) == "ws"
+    assert attn.attn_fwd_kernel(128) == "simple"
+
+
+def test_many_calls_reuse_ticket_slots():
+    """More calls than the persistent kernel has ticket-counter slots (256), back to back on one
+    stream, then on two streams in turn: every result must be bit-identical to the first."""
+    from sliding_window_attention_04_b300 import attn
+
+    q, k, v = (t.cuda() for t in make_qkv(3, 600, 5, 64, seed=41))
+    ref, lref = attn.attn_fwd(q, k, v, window=200)
+    outs = [attn.attn_fwd(q, k, v, window=200) for _ in range(300)]
+    s2 = torch.cuda.Stream()
+    for i in range(40):
+        s = s2 if i % 2 else torch.cuda.current_stream()
+        s.wait_stream(torch.cuda.current_stream() if i % 2 else s2)
+        with torch.cuda.stream(s):
+            outs.append(attn.attn_fwd(q, k, v, window=200))
+    torch.cuda.synchronize()
+    assert attn.attn_device_status() == attn.ATTN_OK
+    for o, l in outs:
+        assert torch.equal(o, ref) and torch.equal(l, lref)
+    out, lse = ref.cpu().double().numpy(), lref.cpu().double().numpy()
+    r, lr = oracle.attn_fwd(q.cpu(), k.cpu(), v.cpu(), window=200, causal=True)
+    assert_close(out, r, lse, lr, "many calls")
