@@ -211,12 +211,18 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only the first N layers of the workload (profiling captures); 0 = all")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     w = configs.workloads()[WORKLOAD_INDEX]
+    if args.layers > 0:
+        import dataclasses
+
+        w = dataclasses.replace(w, layers=list(w.layers[:args.layers]))
 
     if args.impl == "reference":
         run_reference(args, w, rank)

@@ -24,7 +24,8 @@
  *     CUDA kernel takes it (prec = ORACLE_PREC_F32, the mode used for parity): steps 1-2 are
  *     then evaluated with this fixed sequence of IEEE-754 single-precision operations, each
  *     correctly rounded (fmaf, *, +, sqrtf, /):
- *         ss = 0; for d = 0..D-1: ss = fmaf(x[d], x[d], ss)
+ *         P[m] = 0 for m = 0..7; for d = 0..D-1 in order: P[d % 8] = fmaf(x[d], x[d], P[d % 8])
+ *         ss = ((P[0] + P[2]) + (P[4] + P[6])) + ((P[1] + P[3]) + (P[5] + P[7]))
  *         r  = 1 / sqrtf(ss * (1/D) + eps)                      (r = 1 without the norm)
  *         c  = cos32(theta_i) * r,  s = sin32(theta_i) * r       (c = r, s = 0 without RoPE)
  *         y[i] = fmaf(x1, c, x2 * s),  y[i + D/2] = fmaf(x2, c, -(x1 * s))
@@ -87,8 +88,11 @@ static void prologue_row_f32(const double *x, double *y, int D, int t, double ba
   for (int d = 0; d < D; ++d) xf[d] = (float)x[d]; /* x holds bf16 values: exact */
   float r = 1.0f;
   if (eps >= 0.0) {
-    float ss = 0.0f;
-    for (int d = 0; d < D; ++d) ss = fmaf(xf[d], xf[d], ss);
+    float part[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    for (int d = 0; d < D; ++d) part[d % 8] = fmaf(xf[d], xf[d], part[d % 8]);
+    float even = (part[0] + part[2]) + (part[4] + part[6]);
+    float odd = (part[1] + part[3]) + (part[5] + part[7]);
+    float ss = even + odd;
     float ms = ss * (1.0f / (float)D);
     float den = sqrtf(ms + (float)eps);
     r = 1.0f / den;

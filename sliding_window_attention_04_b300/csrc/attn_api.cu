@@ -19,8 +19,8 @@
 namespace {
 
 struct RopeTable {
-  float2* ptr = nullptr;
-  int T = 0;  // positions covered
+  float4* ptr = nullptr;
+  int T = 0;  // positions covered (the table's row stride)
 };
 
 // Ticket counters of the persistent kernel: one (ticket, exits) pair per slot, 128 bytes apart.
@@ -40,7 +40,7 @@ struct State {
   unsigned sched_next = 0;
   bool ws_ok[2] = {false, false};  // warp-specialised kernel usable for D = 32, 64
   std::map<std::pair<int, float>, RopeTable> tables;  // (D, base) -> table
-  std::vector<float2*> retired;                       // outgrown tables, freed at destroy
+  std::vector<float4*> retired;                       // outgrown tables, freed at destroy
   PFN_cuTensorMapEncodeTiled_v12000 encode_tiled = nullptr;
 };
 
@@ -74,17 +74,16 @@ cudaError_t set_kernel_attrs() {
                               swa::SimpleCfg<D>::kSmemBytes);
 }
 
-// The warp-specialised kernel re-divides its registers at run time (setmaxnreg): the softmax
-// warpgroups grow to 176 per thread, the others shrink to 104 and 56. That budget adds up to the
-// 65536 registers of the launch only if the kernel was compiled to exactly 128 per thread;
-// with any other count the kernel is not used.
+// The warp-specialised kernel re-divides its registers at run time (setmaxnreg); that split adds
+// up to the registers of the launch only if the kernel was compiled to exactly kLaunchRegs per
+// thread. With any other count the kernel is not used.
 template <int D>
 cudaError_t set_ws_attrs(bool* usable) {
   *usable = false;
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, swa::attn_fwd_ws_kernel<D>);
   if (e != cudaSuccess) return e;
-  if (fa.numRegs != 128) return cudaSuccess;
+  if (fa.numRegs != swa::WsCfg<D>::kLaunchRegs) return cudaSuccess;
   e = cudaFuncSetAttribute(swa::attn_fwd_ws_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            swa::WsCfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -108,19 +107,26 @@ CUresult encode_tile_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* 
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-// cos / sin of t * base^(-2i/D) for t < T, i < D/2, evaluated in double, stored as fp32 pairs.
-cudaError_t build_table(int D, float base, int T, float2** out) {
-  std::vector<float2> h(static_cast<size_t>(T) * (D / 2));
+// cos / sin of t * base^(-2i/D) for t < T, i < D/2, evaluated in double and rounded to fp32.
+// Layout [D/4][T] of float4 (cos_2m, sin_2m, cos_2m+1, sin_2m+1): for a fixed pair group the
+// positions are contiguous, so a warp whose threads hold consecutive rows loads whole lines.
+cudaError_t build_table(int D, float base, int T, float4** out) {
+  std::vector<float4> h(static_cast<size_t>(T) * (D / 4));
   for (int t = 0; t < T; ++t)
-    for (int i = 0; i < D / 2; ++i) {
-      const double theta = static_cast<double>(t) * std::pow(static_cast<double>(base), -2.0 * i / D);
-      h[static_cast<size_t>(t) * (D / 2) + i] = make_float2(static_cast<float>(std::cos(theta)),
-                                                            static_cast<float>(std::sin(theta)));
+    for (int m = 0; m < D / 4; ++m) {
+      float cs[4];
+      for (int k = 0; k < 2; ++k) {
+        const int i = 2 * m + k;
+        const double theta = static_cast<double>(t) * std::pow(static_cast<double>(base), -2.0 * i / D);
+        cs[2 * k] = static_cast<float>(std::cos(theta));
+        cs[2 * k + 1] = static_cast<float>(std::sin(theta));
+      }
+      h[static_cast<size_t>(m) * T + t] = make_float4(cs[0], cs[1], cs[2], cs[3]);
     }
-  float2* d = nullptr;
-  cudaError_t e = cudaMalloc(&d, h.size() * sizeof(float2));
+  float4* d = nullptr;
+  cudaError_t e = cudaMalloc(&d, h.size() * sizeof(float4));
   if (e != cudaSuccess) return e;
-  e = cudaMemcpy(d, h.data(), h.size() * sizeof(float2), cudaMemcpyHostToDevice);
+  e = cudaMemcpy(d, h.data(), h.size() * sizeof(float4), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) {
     cudaFree(d);
     return e;
@@ -171,10 +177,11 @@ constexpr size_t kNoAllocHeaderBytes = 256;
 constexpr size_t kNoAllocTablePairs = size_t(1) << 19;  // T * D / 2 <= 524288 pairs (4 MiB)
 constexpr size_t kNoAllocBytes = kNoAllocHeaderBytes + kNoAllocTablePairs * sizeof(float2);
 
-// Fills the cos / sin table for (T, D, base) and clears the error word. Runs on the caller's
-// stream right before the attention kernel, so each call starts from a clean state.
+// Fills the cos / sin table for (T, D, base) in the layout of build_table ([D/4][T] float4) and
+// clears the error word. Runs on the caller's stream right before the attention kernel, so each
+// call starts from a clean state.
 __global__ void noalloc_prepare_kernel(unsigned char* scratch, int T, int D, float base) {
-  float2* table = reinterpret_cast<float2*>(scratch + kNoAllocHeaderBytes);
+  float* table = reinterpret_cast<float*>(scratch + kNoAllocHeaderBytes);
   const int half = D / 2;
   const size_t n = base > 0.f ? static_cast<size_t>(T) * half : 0;
   for (size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
@@ -183,7 +190,9 @@ __global__ void noalloc_prepare_kernel(unsigned char* scratch, int T, int D, flo
     const double theta = static_cast<double>(t) * pow(static_cast<double>(base), -2.0 * i / D);
     double sn, cs;
     sincos(theta, &sn, &cs);
-    table[idx] = make_float2(static_cast<float>(cs), static_cast<float>(sn));
+    float* dst = table + 4 * (static_cast<size_t>(i / 2) * T + t) + 2 * (i % 2);
+    dst[0] = static_cast<float>(cs);
+    dst[1] = static_cast<float>(sn);
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(scratch) = 0;
 }
@@ -326,7 +335,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
   if (D != 32 && D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
 
   State& s = state();
-  float2* table = nullptr;
+  float4* table = nullptr;
+  int table_T = 0;
   int* d_err = nullptr;
   int* sched = nullptr;
   bool use_ws = false;
@@ -346,7 +356,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
     if (rope_base > 0.f) {
       RopeTable& t = s.tables[std::make_pair(D, rope_base)];
       if (t.T < T) {
-        float2* fresh = nullptr;
+        float4* fresh = nullptr;
         const int want = T;
         if (with_device(s.device, [&] { return build_table(D, rope_base, want, &fresh); }) != cudaSuccess)
           return ATTN_ERR_CUDA;
@@ -355,6 +365,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
         t.T = want;
       }
       table = t.ptr;
+      table_T = t.T;
     }
   }
 
@@ -365,6 +376,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.rope = table;
+  p.rope_T = table_T;
   p.err = d_err;
   p.B = B;
   p.H = H;
@@ -405,7 +417,7 @@ void attn_destroy(void) {
   with_device(s.device, [&]() -> cudaError_t {
     for (auto& kv : s.tables)
       if (kv.second.ptr) cudaFree(kv.second.ptr);
-    for (float2* ptr : s.retired) cudaFree(ptr);
+    for (float4* ptr : s.retired) cudaFree(ptr);
     if (s.d_err) cudaFree(s.d_err);
     if (s.d_sched) cudaFree(s.d_sched);
     return cudaSuccess;
@@ -509,7 +521,8 @@ int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, flo
   p.v = static_cast<const __nv_bfloat16*>(v);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
-  p.rope = rope_base > 0.f ? reinterpret_cast<const float2*>(scratch + kNoAllocHeaderBytes) : nullptr;
+  p.rope = rope_base > 0.f ? reinterpret_cast<const float4*>(scratch + kNoAllocHeaderBytes) : nullptr;
+  p.rope_T = T;
   p.err = reinterpret_cast<int*>(scratch);
   p.B = B;
   p.H = H;

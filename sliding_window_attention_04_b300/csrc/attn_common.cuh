@@ -19,7 +19,8 @@ struct AttnParams {
   const __nv_bfloat16* v;  // [B, T, H, D]
   __nv_bfloat16* out;      // [B, T, H, D]
   float* lse;              // [B, H, T] or nullptr
-  const float2* rope;      // [T_table, D/2] (cos, sin) or nullptr (RoPE off)
+  const float4* rope;      // [D/4][rope_T] (cos, sin) of pairs 2i, 2i+1, or nullptr (RoPE off)
+  int rope_T;              // positions the table covers (its row stride), >= T
   int* err;                // device error word
   int B, H, T;
   int window;              // < 0: no window
@@ -70,51 +71,79 @@ __device__ __forceinline__ bool key_visible(int i, int j, int T, int window, int
   return true;
 }
 
-// QK-norm + RoPE for one row held in registers as fp32 x[0..D):
+// QK-norm + RoPE for one row of D bf16 values held as D/2 packed words w (element 2k in the
+// low half of w[k]), transformed in place:
 //   r = 1 / sqrt(mean(x^2) + eps)   (parameter-free RMSNorm; r = 1 when !use_norm)
 //   pair i = (x[i], x[i + D/2]) at position pos, angle pos * base^(-2i/D) from the table:
 //   y[i] = x1 (c r) + x2 (s r),  y[i + D/2] = x2 (c r) - x1 (s r)
 // The result is rounded to bf16 (a quantisation), so the fp32 evaluation is pinned to one fixed
-// sequence of correctly rounded operations: the sum of squares accumulates d = 0..D-1 with
-// fused multiply-adds, r is a rounded square root followed by a rounded division, and every
-// product / fused multiply-add is spelled out with the _rn intrinsics so the compiler cannot
-// re-associate or contract them.
-// The bf16 result is written as D/8 16-byte chunks through `store(chunk, uint4)`.
-template <int D, typename Store>
-__device__ __forceinline__ void qk_row_transform(float (&x)[D], int pos, const float2* rope, int use_norm,
-                                                 float eps, Store store) {
+// sequence of correctly rounded operations:
+//   - sum of squares in 8 partial sums P_m (m = d mod 8), each accumulated over increasing d
+//     with fused multiply-adds starting from 0, combined as
+//     ss = ((P0 + P2) + (P4 + P6)) + ((P1 + P3) + (P5 + P7));
+//   - ms = ss * (1/D); r = 1 / sqrt(ms + eps) as a rounded square root then a rounded division;
+//   - c = cos * r, s = sin * r, y1 = fma(x1, c, x2 * s), y2 = fma(x2, c, x1 * (sin * -r))
+//     (x1 * (sin * -r) is exactly -(x1 * s)).
+// Pairs of lanes go through the packed fp32x2 instructions; each lane is the same IEEE operation
+// as its scalar form, so packing does not change any result.
+template <int D>
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
+  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ uint32_t f2_to_bf16x2(uint64_t v) { return pack_bf16x2(f2_lo(v), f2_hi(v)); }
+
+template <int D>
+__device__ __forceinline__ void qk_row_transform_packed(uint32_t (&w)[D / 2], int pos, const float4* rope, int rope_T,
+                                                        int use_norm, float eps) {
   float r = 1.0f;
   if (use_norm) {
-    float ss = 0.f;
+    uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-    for (int d = 0; d < D; ++d) ss = __fmaf_rn(x[d], x[d], ss);
+    for (int g = 0; g < D / 8; ++g)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t x2 = bf16x2_to_f2<D>(w[4 * g + k]);
+        acc[k] = f2_fma(x2, x2, acc[k]);
+      }
+    const uint64_t e = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+    const float ss = __fadd_rn(f2_lo(e), f2_hi(e));
     const float ms = __fmul_rn(ss, 1.0f / D);
     r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
   }
-  constexpr int H2 = D / 2;
+  constexpr int Q4 = D / 4;  // words per half row
   if (rope != nullptr) {
-    const float2* cs = rope + static_cast<size_t>(pos) * H2;
+    const uint64_t r2 = f2_pack(r, r), nr2 = f2_pack(-r, -r);
+    const float4* cs = rope + pos;
 #pragma unroll
-    for (int i = 0; i < H2; ++i) {
-      const float2 t = __ldg(cs + i);
-      const float c = __fmul_rn(t.x, r), s = __fmul_rn(t.y, r);
-      const float x1 = x[i], x2 = x[i + H2];
-      x[i] = __fmaf_rn(x1, c, __fmul_rn(x2, s));
-      x[i + H2] = __fmaf_rn(x2, c, -__fmul_rn(x1, s));
+    for (int i2 = 0; i2 < Q4; ++i2) {
+      const float4 t = __ldg(cs + static_cast<size_t>(i2) * rope_T);
+      const uint64_t cos2 = f2_pack(t.x, t.z), sin2 = f2_pack(t.y, t.w);
+      const uint64_t c2 = f2_mul(cos2, r2), s2 = f2_mul(sin2, r2), sn2 = f2_mul(sin2, nr2);
+      const uint64_t x1 = bf16x2_to_f2<D>(w[i2]), x2 = bf16x2_to_f2<D>(w[i2 + Q4]);
+      const uint64_t y1 = f2_fma(x1, c2, f2_mul(x2, s2));
+      const uint64_t y2 = f2_fma(x2, c2, f2_mul(x1, sn2));
+      w[i2] = f2_to_bf16x2(y1);
+      w[i2 + Q4] = f2_to_bf16x2(y2);
     }
   } else {
+    const uint64_t r2 = f2_pack(r, r);
 #pragma unroll
-    for (int d = 0; d < D; ++d) x[d] = __fmul_rn(x[d], r);
+    for (int k = 0; k < D / 2; ++k) w[k] = f2_to_bf16x2(f2_mul(bf16x2_to_f2<D>(w[k]), r2));
   }
-#pragma unroll
-  for (int ch = 0; ch < D / 8; ++ch) {
-    uint4 u;
-    u.x = pack_bf16x2(x[ch * 8 + 0], x[ch * 8 + 1]);
-    u.y = pack_bf16x2(x[ch * 8 + 2], x[ch * 8 + 3]);
-    u.z = pack_bf16x2(x[ch * 8 + 4], x[ch * 8 + 5]);
-    u.w = pack_bf16x2(x[ch * 8 + 6], x[ch * 8 + 7]);
-    store(ch, u);
-  }
+}
+
+// One row of D bf16 values as D/2 packed words <-> D/8 16-byte chunks.
+template <int D>
+__device__ __forceinline__ void set_chunk(uint32_t (&w)[D / 2], int ch, uint4 u) {
+  w[4 * ch + 0] = u.x;
+  w[4 * ch + 1] = u.y;
+  w[4 * ch + 2] = u.z;
+  w[4 * ch + 3] = u.w;
+}
+template <int D>
+__device__ __forceinline__ uint4 get_chunk(const uint32_t (&w)[D / 2], int ch) {
+  return make_uint4(w[4 * ch + 0], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
 }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float* f) {

@@ -70,18 +70,13 @@ __global__ void __launch_bounds__(128, 1) attn_fwd_simple_kernel(const AttnParam
   // ---- Q tile: load, normalise, rotate, store swizzled ----
   {
     const int i = q0 + tid;
-    float x[D];
-    if (i < T) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + head_base + static_cast<size_t>(i) * row_stride);
+    uint32_t w[D / 2];
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + head_base + static_cast<size_t>(i) * row_stride);
 #pragma unroll
-      for (int ch = 0; ch < D / 8; ++ch) bf16x8_to_f32(__ldg(src + ch), x + ch * 8);
-    } else {
+    for (int ch = 0; ch < D / 8; ++ch) set_chunk<D>(w, ch, i < T ? __ldg(src + ch) : make_uint4(0, 0, 0, 0));
+    qk_row_transform_packed<D>(w, i < T ? i : 0, p.rope, p.rope_T, p.use_norm, p.eps);
 #pragma unroll
-      for (int d = 0; d < D; ++d) x[d] = 0.f;
-    }
-    qk_row_transform<D>(x, i < T ? i : 0, p.rope, p.use_norm, p.eps, [&](int ch, uint4 u) {
-      *reinterpret_cast<uint4*>(sQ + tile_off<D>(tid, ch)) = u;
-    });
+    for (int ch = 0; ch < D / 8; ++ch) *reinterpret_cast<uint4*>(sQ + tile_off<D>(tid, ch)) = get_chunk<D>(w, ch);
   }
 
   // ---- key-tile range of this query tile ----
@@ -105,18 +100,13 @@ __global__ void __launch_bounds__(128, 1) attn_fwd_simple_kernel(const AttnParam
     // ---- K row (normalise + rotate) and V row into shared memory ----
     {
       const int j = k0 + tid;
-      float x[D];
-      if (j < T) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.k + head_base + static_cast<size_t>(j) * row_stride);
+      uint32_t w[D / 2];
+      const uint4* src = reinterpret_cast<const uint4*>(p.k + head_base + static_cast<size_t>(j) * row_stride);
 #pragma unroll
-        for (int ch = 0; ch < D / 8; ++ch) bf16x8_to_f32(__ldg(src + ch), x + ch * 8);
-      } else {
+      for (int ch = 0; ch < D / 8; ++ch) set_chunk<D>(w, ch, j < T ? __ldg(src + ch) : make_uint4(0, 0, 0, 0));
+      qk_row_transform_packed<D>(w, j < T ? j : 0, p.rope, p.rope_T, p.use_norm, p.eps);
 #pragma unroll
-        for (int d = 0; d < D; ++d) x[d] = 0.f;
-      }
-      qk_row_transform<D>(x, j < T ? j : 0, p.rope, p.use_norm, p.eps, [&](int ch, uint4 u) {
-        *reinterpret_cast<uint4*>(sK + tile_off<D>(tid, ch)) = u;
-      });
+      for (int ch = 0; ch < D / 8; ++ch) *reinterpret_cast<uint4*>(sK + tile_off<D>(tid, ch)) = get_chunk<D>(w, ch);
       const uint4* vsrc = reinterpret_cast<const uint4*>(p.v + head_base + static_cast<size_t>(j) * row_stride);
 #pragma unroll
       for (int ch = 0; ch < D / 8; ++ch) {

@@ -1,30 +1,49 @@
 // Attention forward, warp-specialised persistent version (D = 32 or 64).
 //
-// One CTA per SM (512 threads, 1 CTA/SM: ~200 KB shared memory and all 512 TMEM columns). A work
-// unit is (b, h, 256-row query block) = two 128-row query tiles that share one stream of
-// 128-key K/V tiles. Units are handed out through a global ticket counter in the order
-// (b, h)-major, query block descending, so the four blocks of one head run at about the same time
-// on different SMs (their K/V tiles are shared through L2) and the cheap blocks come last.
+// One CTA per SM (640 threads = five warpgroups, ~200 KB shared memory, all 512 TMEM columns). A
+// work unit is (b, h, 256-row query block) = two 128-row query tiles that share one stream of
+// 128-key K/V tiles. Units are handed out through a global ticket counter in the order (b, h)-major,
+// query block descending, so the blocks of one head run at about the same time on different SMs
+// (their K/V tiles are shared through L2) and the cheap blocks come last.
 //
 // Roles (warp index: role):
-//   0-3   softmax of query tile 0   (thread = query row = TMEM lane)
-//   4-7   softmax of query tile 1
-//   8-11  prologue: QK RMSNorm + RoPE of the Q tiles and of every K tile, in place in shared
-//         memory (TMA writes the raw bf16 rows already in the tensor core's swizzled layout)
-//   12    producer: ticket fetch, TMA loads of Q, K, V (lane 0)
-//   13    MMA issuer (lane 0) and TMEM owner
-//   14-15 idle
+//   0-3    softmax of query tile 0   (thread = query row = TMEM lane)
+//   4-7    softmax of query tile 1
+//   8-15   prologue: QK RMSNorm + RoPE of the Q tiles and of every K tile, two threads per row,
+//          in place in shared memory (TMA writes the raw bf16 rows already in the tensor core's
+//          swizzled layout); the cos/sin entries of a row are loaded before its tile arrives
+//   16     producer: ticket fetch, TMA loads of Q, K, V (lane 0)
+//   17     MMA issuer (lane 0) and TMEM owner
+//   18-19  idle
 //
-// TMEM (512 columns): S_t (128 fp32 columns each), P_t (128 bf16 = 64 columns each, not aliased
-// with S so that S_t of the next key tile can be computed while P_t is still being consumed),
-// O_t (D fp32 columns each).
+// TMEM (512 columns): three rotating 128-column S/P buffers and O_0, O_1 (D columns each). The
+// S jobs (one per query tile and key tile, in stream order) take the buffers round-robin.
+// Every phase-parity barrier has one producer and one consumer that can never be more than one
+// phase apart: S-done and S-seen are per query tile (the next S of a tile is issued only after
+// its softmax has seen the previous one), P-written and buffer-free are per buffer (a buffer is
+// reused only after the P.V that read it). A
+// softmax warpgroup reads S from its buffer and writes P (bf16, 64 columns) into the buffer's upper
+// half once that half has been read, so P needs no space of its own; the P.V MMA reads P from
+// there, and its completion frees the buffer for the S job three places later. With three
+// buffers for two query tiles the S of a tile's next key tile is normally computed while its
+// softmax still works on the current one.
 //
-// Per key tile j the MMA issuer runs one tile ahead on S:  S_0(j+1), S_1(j+1), then
-// O_0 += P_0(j) V(j), O_1 += P_1(j) V(j). The softmax warps read S_t(j), hand the S columns back,
-// compute P_t(j) = exp2(s*scale*log2e - m) with a lazily updated running max m (O and l are
-// rescaled only when the tile max exceeds m by more than kRescaleLog2), and write P_t(j) to TMEM.
-// At the end of a unit they normalise O_t, stage it as bf16 in the (now free) Q tile buffer and
-// store it with one TMA store, and write the per-row log-sum-exp.
+// The MMA issuer is event driven: it polls its barriers and issues whatever is ready, S jobs in
+// stream order and, independently per query tile, the P.V jobs in order, so one tile's softmax
+// never holds up the other tile's MMAs.
+//
+// Softmax of one S tile: three TMEM round trips over the two 64-column halves (half 0 for its
+// max with the reducing TMEM load, half 1 for its max and exponentials, half 0 again for its
+// exponentials). A 32-column block that the mask removes for the whole warp is skipped, and only a
+// block that the mask edge cuts is masked element by element. The running max is updated lazily:
+// O and l are rescaled only when the tile max exceeds the current reference by more than
+// kRescaleLog2. At the end of a unit the softmax warps normalise O_t, stage it as bf16 in the (now
+// free) Q tile buffer, store it with one TMA store, and write the per-row log-sum-exp.
+//
+// Registers: the kernel is compiled to 96 per thread (640 x 96 = 61440); at start the warpgroups
+// re-divide them with setmaxnreg: softmax 128, prologue 80, producer/MMA group 64, i.e.
+// 128 x (128 + 128 + 80 + 80 + 64) = 61440. The host launches the kernel only when the compiled
+// count is exactly kLaunchRegs, so the increase can always be satisfied.
 //
 // Every wait is bounded (kWaitTimeoutNs); a role that gives up records the error, sets a CTA
 // abort flag that makes the other roles leave their loops, and the CTA drains its own TMA loads
@@ -39,48 +58,55 @@ namespace swa {
 template <int D>
 struct WsCfg {
   using G = TileGeom<D>;
-  static constexpr int kThreads = 512;
+  static constexpr int kThreads = 640;
+  static constexpr int kLaunchRegs = 96;  // per thread at launch; the run-time split adds up to it
   static constexpr int kStages = 4;                      // K/V ring depth
+  static constexpr int kSBufs = 3;                       // S/P buffers in TMEM
   static constexpr int kTileBytes = G::kBytes;           // one 128 x D bf16 tile
   static constexpr int kOffQ = 0;                        // [2 slots][2 tiles] Q^ / output staging
   static constexpr int kOffK = kOffQ + 4 * kTileBytes;   // [kStages] K^ (transformed in place)
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   // barrier indices
-  static constexpr int kBarQFull = 0;                    // [2] TMA -> prologue
-  static constexpr int kBarQReady = 2;                   // [2] prologue -> MMA
-  static constexpr int kBarQEmpty = 4;                   // [2] epilogue stores read -> producer
-  static constexpr int kBarUnit = 6;                     // [2] producer -> MMA, softmax (unit id)
-  static constexpr int kBarKFull = 8;                    // [kStages] TMA -> prologue
-  static constexpr int kBarKReady = kBarKFull + kStages; // [kStages] prologue -> MMA
-  static constexpr int kBarVFull = kBarKReady + kStages; // [kStages] TMA -> MMA
-  static constexpr int kBarKVEmpty = kBarVFull + kStages;// [kStages] MMA commit -> producer
-  static constexpr int kBarSFull = kBarKVEmpty + kStages;// [2] MMA commit -> softmax t
-  static constexpr int kBarSFree = kBarSFull + 2;        // [2] softmax t read S -> MMA
-  static constexpr int kBarPFull = kBarSFree + 2;        // [2] softmax t wrote P -> MMA
-  static constexpr int kBarPVDone = kBarPFull + 2;       // [2] MMA commit -> softmax t
-  static constexpr int kBarFinal = kBarPVDone + 2;       // MMA drain at exit
+  static constexpr int kBarQFull = 0;                     // [2] TMA -> prologue
+  static constexpr int kBarQReady = 2;                    // [2] prologue -> MMA
+  static constexpr int kBarQEmpty = 4;                    // [2] epilogue stores read -> producer
+  static constexpr int kBarUnit = 6;                      // [2] producer -> MMA, softmax (unit id)
+  static constexpr int kBarKFull = 8;                     // [kStages] TMA -> prologue
+  static constexpr int kBarKReady = kBarKFull + kStages;  // [kStages] prologue -> MMA
+  static constexpr int kBarVFull = kBarKReady + kStages;  // [kStages] TMA -> MMA
+  static constexpr int kBarKVEmpty = kBarVFull + kStages; // [kStages] MMA commit -> producer
+  static constexpr int kBarSFull = kBarKVEmpty + kStages; // [2] S job of tile t done -> softmax t
+  static constexpr int kBarSSeen = kBarSFull + 2;         // [2] softmax t has seen its S -> MMA
+  static constexpr int kBarBufFree = kBarSSeen + 2;       // [kSBufs] P.V job done -> MMA
+  static constexpr int kBarPFull = kBarBufFree + kSBufs;  // [kSBufs] softmax wrote P into the buffer -> MMA
+  static constexpr int kBarPVDone = kBarPFull + kSBufs;   // [2] P.V job of tile t done -> softmax t
+  static constexpr int kBarFinal = kBarPVDone + 2;        // MMA drain at exit
   static constexpr int kNumBars = kBarFinal + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, unit ids
   static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
   // TMEM columns
   static constexpr uint32_t kTmemCols = 512;
-  static __device__ __forceinline__ uint32_t col_s(int t) { return static_cast<uint32_t>(128 * t); }
-  static __device__ __forceinline__ uint32_t col_p(int t) { return static_cast<uint32_t>(256 + 64 * t); }
-  static __device__ __forceinline__ uint32_t col_o(int t) { return static_cast<uint32_t>(384 + D * t); }
-  static_assert(384 + 2 * D <= 512, "TMEM budget");
+  static __device__ __forceinline__ uint32_t col_buf(int b) { return static_cast<uint32_t>(128 * b); }
+  static __device__ __forceinline__ uint32_t col_o(int t) { return static_cast<uint32_t>(128 * kSBufs + D * t); }
+  static_assert(128 * kSBufs + 2 * D <= 512, "TMEM budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (log2 units): P stays <= 256
 
-// Geometry of one work unit: two 128-row query tiles starting at qs[t] and the key-tile range
-// [kb[t], ke[t]] each needs (empty when kb > ke); [kb_all, ke_all] is their union.
+// Geometry of one work unit: two 128-row query tiles starting at qs0, qs0 + 128 and the
+// key-tile range [kb_t, ke_t] each needs (empty when kb > ke); [kb_all, ke_all] is their union.
 struct UnitGeom {
-  int b, h;
-  int qs[2];
-  int kb[2], ke[2];
+  int b, h, qs0;
+  int kb0, ke0, kb1, ke1;
   int kb_all, ke_all;
+  __device__ __forceinline__ bool has(int t, int j) const {
+    return t == 0 ? (j >= kb0 && j <= ke0) : (j >= kb1 && j <= ke1);
+  }
+  __device__ __forceinline__ int kb(int t) const { return t == 0 ? kb0 : kb1; }
+  __device__ __forceinline__ int ke(int t) const { return t == 0 ? ke0 : ke1; }
+  __device__ __forceinline__ bool valid(int t) const { return kb(t) <= ke(t); }
 };
 
 __device__ __forceinline__ void unit_geom(const AttnParams& p, int n_qb, int unit, UnitGeom& g) {
@@ -88,25 +114,30 @@ __device__ __forceinline__ void unit_geom(const AttnParams& p, int n_qb, int uni
   const int qb = n_qb - 1 - (unit - bh * n_qb);
   g.b = bh / p.H;
   g.h = bh - g.b * p.H;
+  g.qs0 = qb * 2 * kTile;
   const int T = p.T;
+  int kb[2], ke[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    const int qs = qb * 256 + 128 * t;
-    g.qs[t] = qs;
+    const int qs = g.qs0 + kTile * t;
     if (qs < T) {
       const int qe = min(T - 1, qs + kTile - 1);
       const int lo = p.window >= 0 ? max(0, qs - p.window) : 0;
       const int hi = p.causal ? qe : (p.window >= 0 ? min(T - 1, qe + p.window) : T - 1);
-      g.kb[t] = lo / kTile;
-      g.ke[t] = hi / kTile;
+      kb[t] = lo / kTile;
+      ke[t] = hi / kTile;
     } else {
-      g.kb[t] = 1;
-      g.ke[t] = 0;
+      kb[t] = 1;
+      ke[t] = 0;
     }
   }
-  g.kb_all = g.kb[0];
-  g.ke_all = g.kb[1] <= g.ke[1] ? max(g.ke[0], g.ke[1]) : g.ke[0];
-  if (g.kb[1] <= g.ke[1]) g.kb_all = min(g.kb_all, g.kb[1]);
+  g.kb0 = kb[0];
+  g.ke0 = ke[0];
+  g.kb1 = kb[1];
+  g.ke1 = ke[1];
+  const bool two = kb[1] <= ke[1];
+  g.kb_all = two ? min(kb[0], kb[1]) : kb[0];
+  g.ke_all = two ? max(ke[0], ke[1]) : ke[0];
 }
 
 // Does the 128 x 128 score tile (query rows from qs, keys from k0) contain a masked entry?
@@ -120,27 +151,152 @@ __device__ __forceinline__ bool tile_needs_mask(const AttnParams& p, int qs, int
   return false;
 }
 
-// QK-norm + RoPE of row `row` of a swizzled 128-row tile, in place.
+// Half-row QK-norm + RoPE: a row of D values is shared by two threads; half h owns the elements
+// d with d mod 8 in [4h, 4h + 4), i.e. 8 bytes of each 16-byte chunk. RoPE pairs (i, i + D/2) have
+// the same d mod 8, so every pair stays inside one thread; the 8 partial sums of squares split
+// 4 / 4 and are combined with one shuffle in the order qk_row_transform_packed uses.
 template <int D>
-__device__ __forceinline__ void transform_row_inplace(uint8_t* tile, int row, int pos, const AttnParams& p) {
-  float x[D];
+struct RopeHalf {
+  float4 cs[D / 8];  // (cos, sin) of pairs 2 i2, 2 i2 + 1 for this half's i2 values
+  __device__ __forceinline__ void load(const AttnParams& p, int pos, int h) {
+    if (p.rope == nullptr) return;
+    const float4* src = p.rope + pos;
 #pragma unroll
-  for (int ch = 0; ch < D / 8; ++ch)
-    bf16x8_to_f32(*reinterpret_cast<const uint4*>(tile + tile_off<D>(row, ch)), x + ch * 8);
-  qk_row_transform<D>(x, pos, p.rope, p.use_norm, p.eps,
-                      [&](int ch, uint4 u) { *reinterpret_cast<uint4*>(tile + tile_off<D>(row, ch)) = u; });
+    for (int k = 0; k < D / 8; ++k) {
+      const int i2 = 4 * (k >> 1) + 2 * h + (k & 1);  // i2 mod 4 in {2h, 2h + 1}
+      cs[k] = __ldg(src + static_cast<size_t>(i2) * p.rope_T);
+    }
+  }
+};
+
+template <int D>
+__device__ __forceinline__ void transform_half_row_inplace(uint8_t* tile, int row, int h, const RopeHalf<D>& tab,
+                                                           const AttnParams& p) {
+  constexpr int NC = D / 8;  // chunks per row; this thread owns 2 words (4 elements) of each
+  uint32_t w[2 * NC];        // w[2c], w[2c+1]: elements 8c + 4h + {0,1} and {2,3}
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const uint2 u = *reinterpret_cast<const uint2*>(tile + tile_off<D>(row, c) + 8 * h);
+    w[2 * c] = u.x;
+    w[2 * c + 1] = u.y;
+  }
+  float r = 1.0f;
+  if (p.use_norm) {
+    uint64_t acc0 = 0, acc1 = 0;  // (P_{4h}, P_{4h+1}), (P_{4h+2}, P_{4h+3})
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const uint64_t a = bf16x2_to_f2<D>(w[2 * c]), b = bf16x2_to_f2<D>(w[2 * c + 1]);
+      acc0 = f2_fma(a, a, acc0);
+      acc1 = f2_fma(b, b, acc1);
+    }
+    const uint64_t mine = f2_add(acc0, acc1);  // h=0: (P0+P2, P1+P3); h=1: (P4+P6, P5+P7)
+    const uint64_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
+    const uint64_t e = h == 0 ? f2_add(mine, other) : f2_add(other, mine);
+    const float ss = __fadd_rn(f2_lo(e), f2_hi(e));
+    const float ms = __fmul_rn(ss, 1.0f / D);
+    r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, p.eps)));
+  }
+  if (p.rope != nullptr) {
+    const uint64_t r2 = f2_pack(r, r), nr2 = f2_pack(-r, -r);
+    // pair i = 8c + 4h + 2q + e (c < NC/2, q, e in {0,1}) lives in word w[2c + q], element e;
+    // its partner i + D/2 is in word w[2(c + NC/2) + q]. Table entry k = 2c + q.
+#pragma unroll
+    for (int c = 0; c < NC / 2; ++c)
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const float4 t = tab.cs[2 * c + q];
+        const uint64_t cos2 = f2_pack(t.x, t.z), sin2 = f2_pack(t.y, t.w);
+        const uint64_t c2 = f2_mul(cos2, r2), s2 = f2_mul(sin2, r2), sn2 = f2_mul(sin2, nr2);
+        uint32_t& a = w[2 * c + q];
+        uint32_t& b = w[2 * (c + NC / 2) + q];
+        const uint64_t x1 = bf16x2_to_f2<D>(a), x2 = bf16x2_to_f2<D>(b);
+        a = f2_to_bf16x2(f2_fma(x1, c2, f2_mul(x2, s2)));
+        b = f2_to_bf16x2(f2_fma(x2, c2, f2_mul(x1, sn2)));
+      }
+  } else {
+    const uint64_t r2 = f2_pack(r, r);
+#pragma unroll
+    for (int k = 0; k < 2 * NC; ++k) w[k] = f2_to_bf16x2(f2_mul(bf16x2_to_f2<D>(w[k]), r2));
+  }
+#pragma unroll
+  for (int c = 0; c < NC; ++c)
+    *reinterpret_cast<uint2*>(tile + tile_off<D>(row, c) + 8 * h) = make_uint2(w[2 * c], w[2 * c + 1]);
 }
 
 struct WsMaps {
   CUtensorMap q, k, v, out;  // 4-D (D, H, T, B) views, box (D, 1, 128, 1), swizzled
 };
 
+// Visible columns of one 32-column block as a bit mask (bit c set: column c visible), for the
+// block-relative visible range [lo, hi].
+__device__ __forceinline__ uint32_t block_vis(int lo, int hi) {
+  const uint32_t upper = hi >= 31 ? 0xFFFFFFFFu : (hi < 0 ? 0u : (0xFFFFFFFFu >> (31 - hi)));
+  const uint32_t lower = lo <= 0 ? 0xFFFFFFFFu : (lo > 31 ? 0u : (0xFFFFFFFFu << lo));
+  return upper & lower;
+}
+
+// Columns whose bit is clear in `vis` -> -inf (no branches: one select per element).
+__device__ __forceinline__ void mask_block(uint32_t (&s)[32], uint32_t vis) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) s[c] = (vis >> c) & 1u ? s[c] : 0xFF800000u;
+}
+
+// Max of one loaded 32-column block: the hardware-reduced value when no column is masked, else
+// the max of the values after masking (which masks them in place).
+__device__ __forceinline__ float block_max(uint32_t (&s)[32], float red, uint32_t vis) {
+  if (vis == 0u) return -INFINITY;
+  if (vis == 0xFFFFFFFFu) return red;
+  mask_block(s, vis);
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 32; c += 8) {
+    m0 = fmax3(m0, __uint_as_float(s[c + 0]), __uint_as_float(s[c + 1]));
+    m1 = fmax3(m1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+    m2 = fmax3(m2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
+    m3 = fmax3(m3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
+  }
+  return fmax3(m0, m1, fmaxf(m2, m3));
+}
+
+// P = exp2(s * scale - m) of one block (masked columns hold -inf and give 0), accumulated into the
+// row sum (two packed accumulators), packed to bf16 and stored into 16 TMEM columns at tP. A block
+// with no visible column stores zeros.
+__device__ __forceinline__ void exp_store(const uint32_t (&s)[32], bool empty, uint64_t scale2, uint64_t negm2,
+                                          uint32_t tP, uint64_t& sumA, uint64_t& sumB) {
+  uint32_t pk[16];
+  if (empty) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) pk[c] = 0u;
+  } else {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), scale2, negm2);
+      const float p0 = ex2_approx(f2_lo(x2));
+      const float p1 = ex2_approx(f2_hi(x2));
+      const uint64_t pp = f2_pack(p0, p1);
+      if (c & 1) sumB = f2_add(sumB, pp);
+      else sumA = f2_add(sumA, pp);
+      pk[c] = pack_bf16x2(p0, p1);
+    }
+  }
+  __syncwarp();  // the TMEM store is warp-collective; `empty` may differ between rows
+  tmem_st16(tP, pk);
+}
+
+// Shared scratch of the MMA issuer: the P.V jobs of one query tile waiting for their P.
+struct PvJob {
+  uint32_t g;   // global S-job index (its TMEM buffer is g % kSBufs)
+  uint32_t kc;  // K/V stream index of its key tile (ring stage kc % kStages)
+  int first;    // first key tile of the query tile in its unit: O is overwritten
+};
+
 template <int D>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(640, 1)
     attn_fwd_ws_kernel(const AttnParams p, const __grid_constant__ WsMaps maps, int* sched, int n_units) {
   using Cfg = WsCfg<D>;
   constexpr int TB = Cfg::kTileBytes;
   constexpr int S = Cfg::kStages;
+  constexpr int NB = Cfg::kSBufs;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -161,25 +317,28 @@ __global__ void __launch_bounds__(512, 1)
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(Cfg::kBarQFull + i), 1);
-      mbar_init(bar(Cfg::kBarQReady + i), 4);
+      mbar_init(bar(Cfg::kBarQReady + i), 8);
       mbar_init(bar(Cfg::kBarQEmpty + i), 2);
       mbar_init(bar(Cfg::kBarUnit + i), 1);
       mbar_init(bar(Cfg::kBarSFull + i), 1);
-      mbar_init(bar(Cfg::kBarSFree + i), 4);
-      mbar_init(bar(Cfg::kBarPFull + i), 4);
+      mbar_init(bar(Cfg::kBarSSeen + i), 4);
       mbar_init(bar(Cfg::kBarPVDone + i), 1);
     }
     for (int i = 0; i < S; ++i) {
       mbar_init(bar(Cfg::kBarKFull + i), 1);
-      mbar_init(bar(Cfg::kBarKReady + i), 4);
+      mbar_init(bar(Cfg::kBarKReady + i), 8);
       mbar_init(bar(Cfg::kBarVFull + i), 1);
       mbar_init(bar(Cfg::kBarKVEmpty + i), 1);
+    }
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(bar(Cfg::kBarBufFree + i), 1);
+      mbar_init(bar(Cfg::kBarPFull + i), 4);
     }
     mbar_init(bar(Cfg::kBarFinal), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 13) {
+  if (warp == 17) {
     tmem_alloc(tmem_slot, Cfg::kTmemCols);
     tmem_relinquish();
   }
@@ -193,9 +352,13 @@ __global__ void __launch_bounds__(512, 1)
     *abort_flag = 1;
   };
 
-  if (warp >= 12) {
-    regs_dec<56>();
-    if (warp == 12 && lane == 0) {
+  if (warp >= 16) {
+    regs_dec<64>();
+  }
+  if (warp >= 18) {
+    // idle warps: straight to the final barrier
+  } else if (warp == 16) {
+    if (lane == 0) {
       // ---------------- producer: tickets and TMA loads ----------------
       prefetch_tmap(&maps.q);
       prefetch_tmap(&maps.k);
@@ -203,8 +366,9 @@ __global__ void __launch_bounds__(512, 1)
       prefetch_tmap(&maps.out);
       const uint64_t pol_stream = policy_evict_first();
       const uint64_t pol_keep = policy_evict_last();
-      int q_armed[2] = {-1, -1};  // parity of the last armed, not yet drained phase
+      int q_armed[2] = {-1, -1};  // parity of the last armed phase of each barrier (for draining)
       int k_armed[S], v_armed[S];
+#pragma unroll
       for (int i = 0; i < S; ++i) k_armed[i] = v_armed[i] = -1;
       uint32_t kcnt = 0;
       bool ok = true;
@@ -215,7 +379,7 @@ __global__ void __launch_bounds__(512, 1)
           ok = false;
           break;
         }
-        int unit = ok ? atomicAdd(sched, 1) : n_units;
+        int unit = atomicAdd(sched, 1);
         if (unit >= n_units) unit = -1;
         unit_id[slot] = unit;
         mbar_arrive(bar(Cfg::kBarUnit + slot));
@@ -225,12 +389,12 @@ __global__ void __launch_bounds__(512, 1)
         }
         UnitGeom g;
         unit_geom(p, n_qb, unit, g);
-        const bool two = g.kb[1] <= g.ke[1];
+        const bool two = g.valid(1);
         mbar_arrive_expect_tx(bar(Cfg::kBarQFull + slot), (two ? 2 : 1) * TB);
         q_armed[slot] = static_cast<int>(uph);
-        tma_load_4d_hint(q_tile(slot, 0), &maps.q, bar(Cfg::kBarQFull + slot), 0, g.h, g.qs[0], g.b, pol_stream);
+        tma_load_4d_hint(q_tile(slot, 0), &maps.q, bar(Cfg::kBarQFull + slot), 0, g.h, g.qs0, g.b, pol_stream);
         if (two)
-          tma_load_4d_hint(q_tile(slot, 1), &maps.q, bar(Cfg::kBarQFull + slot), 0, g.h, g.qs[1], g.b,
+          tma_load_4d_hint(q_tile(slot, 1), &maps.q, bar(Cfg::kBarQFull + slot), 0, g.h, g.qs0 + kTile, g.b,
                            pol_stream);
         for (int j = g.kb_all; j <= g.ke_all; ++j, ++kcnt) {
           const int st = kcnt % S;
@@ -239,11 +403,12 @@ __global__ void __launch_bounds__(512, 1)
             ok = false;
             break;
           }
+#pragma unroll
+          for (int i = 0; i < S; ++i)
+            if (i == st) k_armed[i] = v_armed[i] = static_cast<int>(ph);
           mbar_arrive_expect_tx(bar(Cfg::kBarKFull + st), TB);
-          k_armed[st] = static_cast<int>(ph);
           tma_load_4d_hint(k_tile(st), &maps.k, bar(Cfg::kBarKFull + st), 0, g.h, j * kTile, g.b, pol_keep);
           mbar_arrive_expect_tx(bar(Cfg::kBarVFull + st), TB);
-          v_armed[st] = static_cast<int>(ph);
           tma_load_4d_hint(v_tile(st), &maps.v, bar(Cfg::kBarVFull + st), 0, g.h, j * kTile, g.b, pol_keep);
         }
         if (!ok) break;
@@ -253,6 +418,7 @@ __global__ void __launch_bounds__(512, 1)
         // Drain: every TMA load this thread issued must land before the CTA exits.
         for (int i = 0; i < 2; ++i)
           if (q_armed[i] >= 0) mbar_wait(bar(Cfg::kBarQFull + i), static_cast<uint32_t>(q_armed[i]));
+#pragma unroll
         for (int i = 0; i < S; ++i) {
           if (k_armed[i] >= 0) mbar_wait(bar(Cfg::kBarKFull + i), static_cast<uint32_t>(k_armed[i]));
           if (v_armed[i] >= 0) mbar_wait(bar(Cfg::kBarVFull + i), static_cast<uint32_t>(v_armed[i]));
@@ -265,82 +431,131 @@ __global__ void __launch_bounds__(512, 1)
         atomicExch(sched, 0);
         atomicExch(sched + 1, 0);
       }
-    } else if (warp == 13 && lane == 0) {
-      // ---------------- MMA issuer ----------------
+    }
+  } else if (warp == 17) {
+    if (lane == 0) {
+      // ---------------- MMA issuer (event driven) ----------------
       using G = TileGeom<D>;
       constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, false);
       constexpr uint32_t idesc_o = make_idesc_bf16(128, D, true);
-      uint32_t kcnt = 0;
-      uint32_t scnt[2] = {0, 0}, pcnt[2] = {0, 0};
       bool ok = true;
-      for (uint32_t ul = 0; ok; ++ul) {
-        const int slot = ul & 1;
-        const uint32_t uph = (ul >> 1) & 1;
-        if (!mbar_wait_or_abort(bar(Cfg::kBarUnit + slot), uph, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const int unit = unit_id[slot];
-        if (unit < 0) break;
-        if (!mbar_wait_or_abort(bar(Cfg::kBarQReady + slot), uph, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        UnitGeom g;
-        unit_geom(p, n_qb, unit, g);
-        const uint32_t qa[2] = {smem_u32(q_tile(slot, 0)), smem_u32(q_tile(slot, 1))};
+      // S side: the next S job (unit s_ul, key tile s_j, query tile s_t), global index gS.
+      UnitGeom sg;
+      uint32_t s_ul = 0, gS = 0, s_kc = 0;
+      int s_j = 0, s_t = 0;
+      int s_state = 0;  // 0: unit not yet known, 1: have a job, 2: no more units
+      // P.V side: per query tile a FIFO of issued S jobs (at most kSBufs in flight in total).
+      PvJob q0[NB], q1[NB];
+      int q0_head = 0, q0_n = 0, q1_head = 0, q1_n = 0;
+      int kv_left[S];  // P.V jobs still to read the V tile of each ring stage
+#pragma unroll
+      for (int i = 0; i < S; ++i) kv_left[i] = 0;
+      uint32_t scnt0 = 0, scnt1 = 0;  // S jobs issued per query tile
+      uint64_t idle_since = 0;
 
-        auto issue_s = [&](int j, uint32_t kc) -> bool {
-          const int st = kc % S;
-          if (!mbar_wait_or_abort(bar(Cfg::kBarKReady + st), (kc / S) & 1, abort_flag)) return false;
-          tc_fence_after();
-          const uint32_t ka = smem_u32(k_tile(st));
-          for (int t = 0; t < 2; ++t) {
-            if (j < g.kb[t] || j > g.ke[t]) continue;
-            if (!mbar_wait_or_abort(bar(Cfg::kBarSFree + t), (scnt[t] & 1) ^ 1, abort_flag)) return false;
+      while (ok) {
+        bool progress = false;
+        // ---- the next S job ----
+        if (s_state == 0) {
+          const int slot = s_ul & 1;
+          const uint32_t uph = (s_ul >> 1) & 1;
+          if (mbar_test(bar(Cfg::kBarUnit + slot), uph)) {
+            const int unit = unit_id[slot];
+            if (unit < 0) {
+              s_state = 2;
+              progress = true;
+            } else if (mbar_test(bar(Cfg::kBarQReady + slot), uph)) {
+              tc_fence_after();
+              unit_geom(p, n_qb, unit, sg);
+              s_j = sg.kb_all;
+              s_t = sg.has(0, s_j) ? 0 : 1;
+              s_state = 1;
+              progress = true;
+            }
+          }
+        }
+        if (s_state == 1) {
+          const int st = s_kc % S;
+          const int b = gS % NB;
+          const uint32_t sc = s_t == 0 ? scnt0 : scnt1;
+          if (mbar_test(bar(Cfg::kBarKReady + st), (s_kc / S) & 1) &&
+              mbar_test(bar(Cfg::kBarBufFree + b), ((gS / NB) & 1) ^ 1) &&
+              mbar_test(bar(Cfg::kBarSSeen + s_t), (sc & 1) ^ 1)) {
             tc_fence_after();
+            const uint32_t qa = smem_u32(q_tile(s_ul & 1, s_t));
+            const uint32_t ka = smem_u32(k_tile(st));
 #pragma unroll
             for (int ks = 0; ks < G::kKSteps; ++ks) {
-              const uint64_t ad = make_sdesc(qa[t] + G::kstep_off(ks), 16, G::kSBO, G::kSwizzle);
+              const uint64_t ad = make_sdesc(qa + G::kstep_off(ks), 16, G::kSBO, G::kSwizzle);
               const uint64_t bd = make_sdesc(ka + G::kstep_off(ks), 16, G::kSBO, G::kSwizzle);
-              umma_ss(tmem + Cfg::col_s(t), ad, bd, idesc_s, ks > 0 ? 1u : 0u);
+              umma_ss(tmem + Cfg::col_buf(b), ad, bd, idesc_s, ks > 0 ? 1u : 0u);
             }
-            umma_commit(bar(Cfg::kBarSFull + t));
-            ++scnt[t];
+            umma_commit(bar(Cfg::kBarSFull + s_t));
+            if (s_t == 0) ++scnt0;
+            else ++scnt1;
+            const PvJob job{gS, s_kc, s_j == sg.kb(s_t) ? 1 : 0};
+            if (s_t == 0) {
+              q0[(q0_head + q0_n) % NB] = job;
+              ++q0_n;
+            } else {
+              q1[(q1_head + q1_n) % NB] = job;
+              ++q1_n;
+            }
+            if (s_t == 0 || !sg.has(0, s_j)) kv_left[st] = (sg.has(0, s_j) ? 1 : 0) + (sg.has(1, s_j) ? 1 : 0);
+            ++gS;
+            // advance the cursor
+            if (s_t == 0 && sg.has(1, s_j)) {
+              s_t = 1;
+            } else if (s_j < sg.ke_all) {
+              ++s_j;
+              ++s_kc;
+              s_t = sg.has(0, s_j) ? 0 : 1;
+            } else {
+              ++s_kc;
+              ++s_ul;
+              s_state = 0;
+            }
+            progress = true;
           }
-          return true;
-        };
-        auto issue_pv = [&](int j, uint32_t kc) -> bool {
-          const int st = kc % S;
-          if (!mbar_wait_or_abort(bar(Cfg::kBarVFull + st), (kc / S) & 1, abort_flag)) return false;
+        }
+        // ---- P.V jobs, independently per query tile ----
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int qn = t == 0 ? q0_n : q1_n;
+          if (qn == 0) continue;
+          const PvJob job = t == 0 ? q0[q0_head] : q1[q1_head];
+          const int st = job.kc % S;
+          if (!mbar_test(bar(Cfg::kBarPFull + job.g % NB), (job.g / NB) & 1) ||
+              !mbar_test(bar(Cfg::kBarVFull + st), (job.kc / S) & 1))
+            continue;
           tc_fence_after();
           const uint32_t va = smem_u32(v_tile(st));
-          for (int t = 0; t < 2; ++t) {
-            if (j < g.kb[t] || j > g.ke[t]) continue;
-            if (!mbar_wait_or_abort(bar(Cfg::kBarPFull + t), pcnt[t] & 1, abort_flag)) return false;
-            tc_fence_after();
+          const uint32_t pa = tmem + Cfg::col_buf(job.g % NB) + 64;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-              const uint64_t bd = make_sdesc(va + ks * 16 * G::kRowBytes, 16, G::kSBO, G::kSwizzle);
-              umma_ts(tmem + Cfg::col_o(t), tmem + Cfg::col_p(t) + ks * 8, bd, idesc_o,
-                      (j > g.kb[t] || ks > 0) ? 1u : 0u);
-            }
-            umma_commit(bar(Cfg::kBarPVDone + t));
-            ++pcnt[t];
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t bd = make_sdesc(va + ks * 16 * G::kRowBytes, 16, G::kSBO, G::kSwizzle);
+            umma_ts(tmem + Cfg::col_o(t), pa + ks * 8, bd, idesc_o, (!job.first || ks > 0) ? 1u : 0u);
           }
-          umma_commit(bar(Cfg::kBarKVEmpty + st));
-          return true;
-        };
-
-        const uint32_t kc0 = kcnt;
-        for (int j = g.kb_all; j <= g.ke_all && ok; ++j) {
-          const uint32_t kc = kc0 + static_cast<uint32_t>(j - g.kb_all);
-          if (!issue_s(j, kc)) ok = false;
-          else if (j > g.kb_all && !issue_pv(j - 1, kc - 1)) ok = false;
+          umma_commit(bar(Cfg::kBarBufFree + job.g % NB));
+          umma_commit(bar(Cfg::kBarPVDone + t));
+          if (--kv_left[st] == 0) umma_commit(bar(Cfg::kBarKVEmpty + st));
+          if (t == 0) {
+            q0_head = (q0_head + 1) % NB;
+            --q0_n;
+          } else {
+            q1_head = (q1_head + 1) % NB;
+            --q1_n;
+          }
+          progress = true;
         }
-        if (ok && !issue_pv(g.ke_all, kc0 + static_cast<uint32_t>(g.ke_all - g.kb_all))) ok = false;
-        kcnt = kc0 + static_cast<uint32_t>(g.ke_all - g.kb_all + 1);
+        if (s_state == 2 && q0_n == 0 && q1_n == 0) break;
+        if (progress) {
+          idle_since = 0;
+        } else {
+          const uint64_t now = globaltimer();
+          if (idle_since == 0) idle_since = now;
+          else if (now - idle_since > kWaitTimeoutNs || *abort_flag) ok = false;
+        }
       }
       if (!ok) fail();
       // Drain: all MMAs this thread issued complete before TMEM is freed.
@@ -348,12 +563,15 @@ __global__ void __launch_bounds__(512, 1)
       mbar_wait(bar(Cfg::kBarFinal), 0);
     }
   } else if (warp >= 8) {
-    regs_dec<104>();
-    // ---------------- prologue: QK-norm + RoPE in place ----------------
-    const int r = tid - 256;  // row of the tile this thread transforms
+    regs_dec<80>();
+    // ---------------- prologue: QK-norm + RoPE in place, two threads per row ----------------
+    const int pr = tid - 256;       // 0..255
+    const int r = pr >> 1;          // row of the tile
+    const int h = pr & 1;           // half of the row
     uint32_t kcnt = 0;
     bool ok = true;
-    for (uint32_t ul = 0;; ++ul) {
+    RopeHalf<D> tab;
+    for (uint32_t ul = 0; ok; ++ul) {
       const int slot = ul & 1;
       const uint32_t uph = (ul >> 1) & 1;
       ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarQFull + slot), uph, abort_flag));
@@ -362,38 +580,46 @@ __global__ void __launch_bounds__(512, 1)
       if (unit < 0) break;
       UnitGeom g;
       unit_geom(p, n_qb, unit, g);
-      for (int t = 0; t < 2; ++t) {
-        if (g.kb[t] > g.ke[t]) continue;
-        const int pos = g.qs[t] + r;
-        transform_row_inplace<D>(q_tile(slot, t), r, pos < p.T ? pos : 0, p);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(Cfg::kBarQReady + slot));
-      for (int j = g.kb_all; j <= g.ke_all; ++j, ++kcnt) {
+      // jobs 0, 1: the two Q tiles; jobs 2..: the K tiles of the unit, in stream order
+      const int n_jobs = 2 + g.ke_all - g.kb_all + 1;
+#pragma unroll 1
+      for (int jb = 0; jb < n_jobs; ++jb) {
+        const bool is_q = jb < 2;
+        if (is_q && !g.valid(jb)) {
+          if (jb == 1 && lane == 0) mbar_arrive(bar(Cfg::kBarQReady + slot));
+          continue;
+        }
         const int st = kcnt % S;
-        ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarKFull + st), (kcnt / S) & 1, abort_flag));
-        if (!ok) break;
-        const int pos = j * kTile + r;
-        transform_row_inplace<D>(k_tile(st), r, pos < p.T ? pos : 0, p);
+        const int pos = is_q ? g.qs0 + kTile * jb + r : (g.kb_all + jb - 2) * kTile + r;
+        uint8_t* tile = is_q ? q_tile(slot, jb) : k_tile(st);
+        tab.load(p, pos < p.T ? pos : 0, h);  // independent of the tile: issued before the wait
+        if (!is_q) {
+          ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarKFull + st), (kcnt / S) & 1, abort_flag));
+          if (!ok) break;
+        }
+        transform_half_row_inplace<D>(tile, r, h, tab, p);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(Cfg::kBarKReady + st));
+        if (is_q) {
+          if (jb == 1 && lane == 0) mbar_arrive(bar(Cfg::kBarQReady + slot));
+        } else {
+          if (lane == 0) mbar_arrive(bar(Cfg::kBarKReady + st));
+          ++kcnt;
+        }
       }
-      if (!ok) break;
     }
     if (!ok && lane == 0) fail();
   } else {
-    regs_inc<176>();
+    regs_inc<128>();
     // ---------------- softmax + epilogue of query tile t ----------------
     const int t = warp >> 2;
     const int r = tid & 127;                                  // row in the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_base + Cfg::col_s(t);
-    const uint32_t tP = tmem + lane_base + Cfg::col_p(t);
     const uint32_t tO = tmem + lane_base + Cfg::col_o(t);
     const float scale = p.scale_log2;
-    uint32_t n = 0;  // P tiles written so far by this warpgroup (all units)
+    const uint64_t scale2 = f2_pack(scale, scale);
+    uint32_t n = 0;   // P tiles written so far by this warpgroup (all units)
+    uint32_t gS = 0;  // global S-job index, counted over both query tiles (as the MMA issuer does)
     bool ok = true;
     for (uint32_t ul = 0; ok; ++ul) {
       const int slot = ul & 1;
@@ -404,112 +630,134 @@ __global__ void __launch_bounds__(512, 1)
       if (unit < 0) break;
       UnitGeom g;
       unit_geom(p, n_qb, unit, g);
-      if (g.kb[t] > g.ke[t]) {  // this query tile lies past T
-        named_bar_sync(1 + t, 128);
-        if (r == 0) mbar_arrive(bar(Cfg::kBarQEmpty + slot));
-        continue;
-      }
-      const int qs = g.qs[t];
+      const int qs = g.qs0 + kTile * t;
       const int i_row = qs + r;
       float m_used = -INFINITY;  // reference max of this row (log2 units)
       float l_run = 0.f;         // sum of exp2(score - m_used)
-      for (int j = g.kb[t]; j <= g.ke[t]; ++j, ++n) {
+      for (int j = g.kb_all; j <= g.ke_all; ++j) {
+        const bool h0 = g.has(0, j), h1 = g.has(1, j);
+        const uint32_t gj = gS + (t == 1 && h0 ? 1u : 0u);
+        gS += (h0 ? 1u : 0u) + (h1 ? 1u : 0u);
+        if (!(t == 0 ? h0 : h1)) continue;
         const int k0 = j * kTile;
+        const int b = gj % NB;
+        const uint32_t tS = tmem + lane_base + Cfg::col_buf(b);
+        // visible columns of this row in this tile: lo <= c <= hi
+        int lo = 0, hi = kTile - 1;
+        if (tile_needs_mask(p, qs, k0)) {
+          lo = p.window >= 0 ? i_row - p.window - k0 : -1;
+          hi = p.causal ? i_row - k0 : (p.window >= 0 ? i_row + p.window - k0 : kTile);
+          hi = min(hi, p.T - 1 - k0);
+        }
+        // S of this tile's n-th job: the MMA issues the next one only after every warp has seen
+        // this one, so the barrier is never more than one phase ahead of this wait.
         ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarSFull + t), n & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
-        uint32_t s[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, s + 32 * c);
-        tmem_ld_wait();
-        reg_fence<128>(s);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(Cfg::kBarSFree + t));
-
-        if (tile_needs_mask(p, qs, k0)) {
-          // visible columns of this row: lo <= c <= hi
-          int lo = p.window >= 0 ? i_row - p.window - k0 : -1;
-          int hi = p.causal ? i_row - k0 : (p.window >= 0 ? i_row + p.window - k0 : kTile);
-          hi = min(hi, p.T - 1 - k0);
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c < lo || c > hi) s[c] = __float_as_uint(-INFINITY);
-        }
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 128; c += 8) {
-          mx0 = fmax3(mx0, __uint_as_float(s[c + 0]), __uint_as_float(s[c + 1]));
-          mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
-          mx2 = fmax3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
-          mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
-        }
-        const float m_tile = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * scale;
-        const bool grow = m_tile > m_used + kRescaleLog2 || (m_used == -INFINITY && m_tile > -INFINITY);
-        const float m_new = grow ? m_tile : m_used;
-        const float alpha = grow ? ex2_approx(m_used - m_new) : 1.0f;  // 0 when m_used = -inf
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const uint64_t scale2 = f2_pack(scale, scale);
-        const uint64_t negm2 = f2_pack(-m_use, -m_use);
-        uint64_t sum2 = 0;  // two fp32 zeros
-        uint32_t pk[64];
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), scale2, negm2);
-          const float p0 = ex2_approx(f2_lo(x2));
-          const float p1 = ex2_approx(f2_hi(x2));
-          const uint64_t pp = f2_pack(p0, p1);
-          sum2 = f2_add(sum2, pp);
-          pk[c] = pack_bf16x2(p0, p1);
-        }
-        const float rowsum = f2_lo(sum2) + f2_hi(sum2);
-
-        // P_t(j-1) must have been consumed (and O_t updated) before P and O are touched again.
+        if (lane == 0) mbar_arrive(bar(Cfg::kBarSSeen + t));
+        // This tile's previous P.V must have completed before any P of this job is written to
+        // TMEM (and before O is rescaled). The P tiles live in different buffers, but measured
+        // results show corrupted outputs when these TMEM stores overlap the tile's P.V in flight.
         if (n > 0) {
           ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarPVDone + t), (n - 1) & 1, abort_flag));
           if (!ok) break;
           tc_fence_after();
         }
-        if (j > g.kb[t] && __any_sync(0xffffffffu, alpha != 1.0f)) {
-          uint32_t o[D];
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + 32 * c, o + 32 * c);
+
+        // Three TMEM round trips over the two 64-column halves of S: it = 0 reads half 0 for its
+        // max, it = 1 reads half 1 for its max and exponentials, it = 2 reads half 0 again for its
+        // exponentials. P of blocks 2, 3 goes to columns 96..127 (S block 3, read at it = 1) and
+        // P of blocks 0, 1 to columns 64..95 (S block 2, read at it = 1).
+        float mx = -INFINITY;
+        float alpha = 1.0f, m_new = m_used;
+        uint64_t negm2 = 0;
+        uint64_t sumA = 0, sumB = 0;  // pairs of fp32 zeros
+        bool grow = false;
+#pragma unroll 1
+        for (int it = 0; it < 3; ++it) {
+          const int hb = it == 1 ? 2 : 0;  // first block of the half
+          const uint32_t va = block_vis(lo - 32 * hb, hi - 32 * hb);
+          const uint32_t vc = block_vis(lo - 32 * hb - 32, hi - 32 * hb - 32);
+          uint32_t a[32], c[32];
+          float ra = -INFINITY, rc = -INFINITY;
+          __syncwarp();  // warp-collective TMEM loads after per-row branches
+          tmem_ld32_max(tS + 32 * hb, a, ra);
+          tmem_ld32_max(tS + 32 * hb + 32, c, rc);
           tmem_ld_wait();
-          reg_fence<D>(o);
+          reg_fence<32>(a);
+          reg_fence<32>(c);
+          asm volatile("" : "+f"(ra), "+f"(rc));
+          if (it < 2) {
+            mx = fmax3(mx, block_max(a, ra, va), block_max(c, rc, vc));
+          } else {
+            if (va != 0xFFFFFFFFu) mask_block(a, va);
+            if (vc != 0xFFFFFFFFu) mask_block(c, vc);
+          }
+          if (it == 1) {
+            const float m_tile = mx * scale;
+            grow = m_tile > m_used + kRescaleLog2 || (m_used == -INFINITY && m_tile > -INFINITY);
+            m_new = grow ? m_tile : m_used;
+            alpha = grow ? ex2_approx(m_used - m_new) : 1.0f;  // 0 when m_used = -inf
+            const float m_use = m_new == -INFINITY ? 0.f : m_new;
+            negm2 = f2_pack(-m_use, -m_use);
+          }
+          if (it >= 1) {
+            const uint32_t pcol = it == 1 ? 96u : 64u;
+            exp_store(a, va == 0u, scale2, negm2, tS + pcol, sumA, sumB);
+            exp_store(c, vc == 0u, scale2, negm2, tS + pcol + 16, sumA, sumB);
+          }
+        }
+        const uint64_t sum2 = f2_add(sumA, sumB);
+        const float rowsum = f2_lo(sum2) + f2_hi(sum2);
+        // O rescale (rare): this tile's previous P.V has finished (waited above) and the next one is
+        // issued only after this step's P is announced.
+        if (j > g.kb(t) && __any_sync(0xffffffffu, alpha != 1.0f)) {
+          uint32_t o[32];
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            tmem_ld32(tO + 32 * cc, o);
+            tmem_ld_wait();
+            reg_fence<32>(o);
 #pragma unroll
-          for (int c = 0; c < D; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) tmem_st32(tO + 32 * c, o + 32 * c);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + 32 * cc, o);
+          }
         }
         l_run = l_run * alpha + rowsum;
         m_used = m_new;
-        tmem_st32(tP, pk);
-        tmem_st32(tP + 32, pk + 32);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(Cfg::kBarPFull + t));
+        if (lane == 0) mbar_arrive(bar(Cfg::kBarPFull + b));
+        ++n;
       }
       if (!ok) break;
+      if (!g.valid(t)) {  // this query tile lies past T
+        named_bar_sync(1 + t, 128);
+        if (r == 0) mbar_arrive(bar(Cfg::kBarQEmpty + slot));
+        continue;
+      }
       // ---- epilogue: O / l -> bf16 staged in this tile's Q buffer, one TMA store; LSE ----
       ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarPVDone + t), (n - 1) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      uint32_t o[D];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + 32 * c, o + 32 * c);
-      tmem_ld_wait();
-      reg_fence<D>(o);
       const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
       uint8_t* stage = q_tile(slot, t);
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * c, o);
+        tmem_ld_wait();
+        reg_fence<32>(o);
 #pragma unroll
-      for (int ch = 0; ch < D / 8; ++ch) {
-        uint4 u;
-        u.x = pack_bf16x2(__uint_as_float(o[ch * 8 + 0]) * inv_l, __uint_as_float(o[ch * 8 + 1]) * inv_l);
-        u.y = pack_bf16x2(__uint_as_float(o[ch * 8 + 2]) * inv_l, __uint_as_float(o[ch * 8 + 3]) * inv_l);
-        u.z = pack_bf16x2(__uint_as_float(o[ch * 8 + 4]) * inv_l, __uint_as_float(o[ch * 8 + 5]) * inv_l);
-        u.w = pack_bf16x2(__uint_as_float(o[ch * 8 + 6]) * inv_l, __uint_as_float(o[ch * 8 + 7]) * inv_l);
-        *reinterpret_cast<uint4*>(stage + tile_off<D>(r, ch)) = u;
+        for (int q = 0; q < 4; ++q) {
+          uint4 u;
+          u.x = pack_bf16x2(__uint_as_float(o[q * 8 + 0]) * inv_l, __uint_as_float(o[q * 8 + 1]) * inv_l);
+          u.y = pack_bf16x2(__uint_as_float(o[q * 8 + 2]) * inv_l, __uint_as_float(o[q * 8 + 3]) * inv_l);
+          u.z = pack_bf16x2(__uint_as_float(o[q * 8 + 4]) * inv_l, __uint_as_float(o[q * 8 + 5]) * inv_l);
+          u.w = pack_bf16x2(__uint_as_float(o[q * 8 + 6]) * inv_l, __uint_as_float(o[q * 8 + 7]) * inv_l);
+          *reinterpret_cast<uint4*>(stage + tile_off<D>(r, 4 * c + q)) = u;
+        }
       }
       if (p.lse != nullptr && i_row < p.T) {
         const float m_fin = m_used == -INFINITY ? 0.f : m_used;
@@ -530,7 +778,7 @@ __global__ void __launch_bounds__(512, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 13) {
+  if (warp == 17) {
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::kTmemCols);
   }
