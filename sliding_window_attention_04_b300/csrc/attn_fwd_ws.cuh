@@ -13,24 +13,25 @@
 //          in place in shared memory (TMA writes the raw bf16 rows already in the tensor core's
 //          swizzled layout); the cos/sin entries of a row are loaded before its tile arrives
 //   16     producer: ticket fetch, TMA loads of Q, K, V (lane 0)
-//   17     MMA issuer (lane 0) and TMEM owner
-//   18-19  idle
+//   17     S issuer (lane 0): S = Q^ K^^T jobs in stream order; TMEM owner
+//   18, 19 P.V issuers of query tiles 0 and 1 (lane 0): O_t += P V in order
 //
 // TMEM (512 columns): three rotating 128-column S/P buffers and O_0, O_1 (D columns each). The
 // S jobs (one per query tile and key tile, in stream order) take the buffers round-robin.
 // Every phase-parity barrier has one producer and one consumer that can never be more than one
-// phase apart: S-done and S-seen are per query tile (the next S of a tile is issued only after
-// its softmax has seen the previous one), P-written and buffer-free are per buffer (a buffer is
-// reused only after the P.V that read it). A
+// phase apart: S-done, S-seen, P-written and P.V-done are per query tile (the next S of a tile is
+// issued only after its softmax has seen the previous one; the next P of a tile is written only
+// after its previous P.V has completed), buffer-free is per buffer and waited only by the S
+// issuer, which issues the buffer's next S only after the P.V that read it. A
 // softmax warpgroup reads S from its buffer and writes P (bf16, 64 columns) into the buffer's upper
 // half once that half has been read, so P needs no space of its own; the P.V MMA reads P from
 // there, and its completion frees the buffer for the S job three places later. With three
 // buffers for two query tiles the S of a tile's next key tile is normally computed while its
 // softmax still works on the current one.
 //
-// The MMA issuer is event driven: it polls its barriers and issues whatever is ready, S jobs in
-// stream order and, independently per query tile, the P.V jobs in order, so one tile's softmax
-// never holds up the other tile's MMAs.
+// Three single-thread MMA issuers each run a plain in-order loop of blocking waits: the S issuer
+// (S jobs in stream order) and one P.V issuer per query tile, which wakes as soon as its tile's P
+// is written, so one tile's softmax never holds up the other tile's MMAs.
 //
 // Softmax of one S tile: three TMEM round trips over the two 64-column halves (half 0 for its
 // max with the reducing TMEM load, half 1 for its max and exponentials, half 0 again for its
@@ -73,16 +74,17 @@ struct WsCfg {
   static constexpr int kBarQEmpty = 4;                    // [2] epilogue stores read -> producer
   static constexpr int kBarUnit = 6;                      // [2] producer -> MMA, softmax (unit id)
   static constexpr int kBarKFull = 8;                     // [kStages] TMA -> prologue
-  static constexpr int kBarKReady = kBarKFull + kStages;  // [kStages] prologue -> MMA
-  static constexpr int kBarVFull = kBarKReady + kStages;  // [kStages] TMA -> MMA
-  static constexpr int kBarKVEmpty = kBarVFull + kStages; // [kStages] MMA commit -> producer
-  static constexpr int kBarSFull = kBarKVEmpty + kStages; // [2] S job of tile t done -> softmax t
-  static constexpr int kBarSSeen = kBarSFull + 2;         // [2] softmax t has seen its S -> MMA
-  static constexpr int kBarBufFree = kBarSSeen + 2;       // [kSBufs] P.V job done -> MMA
-  static constexpr int kBarPFull = kBarBufFree + kSBufs;  // [kSBufs] softmax wrote P into the buffer -> MMA
-  static constexpr int kBarPVDone = kBarPFull + kSBufs;   // [2] P.V job of tile t done -> softmax t
-  static constexpr int kBarFinal = kBarPVDone + 2;        // MMA drain at exit
-  static constexpr int kNumBars = kBarFinal + 1;
+  static constexpr int kBarKReady = kBarKFull + kStages;  // [kStages] prologue -> S issuer
+  static constexpr int kBarVFull = kBarKReady + kStages;  // [kStages] TMA -> P.V issuers
+  static constexpr int kBarKFree = kBarVFull + kStages;   // [kStages] S jobs of the step done -> producer
+  static constexpr int kBarVFree = kBarKFree + kStages;   // [kStages] both P.V issuers done with V -> producer
+  static constexpr int kBarSFull = kBarVFree + kStages;   // [2] S job of tile t done -> softmax t
+  static constexpr int kBarSSeen = kBarSFull + 2;         // [2] softmax t has seen its S -> S issuer
+  static constexpr int kBarBufFree = kBarSSeen + 2;       // [kSBufs] P.V job done -> S issuer
+  static constexpr int kBarPFull = kBarBufFree + kSBufs;  // [2] softmax t wrote P -> P.V issuer t
+  static constexpr int kBarPVDone = kBarPFull + 2;        // [2] P.V job of tile t done -> softmax t
+  static constexpr int kBarFinal = kBarPVDone + 2;        // [3] MMA drain at exit (S issuer, P.V issuers)
+  static constexpr int kNumBars = kBarFinal + 3;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, unit ids
   static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
   // TMEM columns
@@ -283,13 +285,6 @@ __device__ __forceinline__ void exp_store(const uint32_t (&s)[32], bool empty, u
   tmem_st16(tP, pk);
 }
 
-// Shared scratch of the MMA issuer: the P.V jobs of one query tile waiting for their P.
-struct PvJob {
-  uint32_t g;   // global S-job index (its TMEM buffer is g % kSBufs)
-  uint32_t kc;  // K/V stream index of its key tile (ring stage kc % kStages)
-  int first;    // first key tile of the query tile in its unit: O is overwritten
-};
-
 template <int D>
 __global__ void __launch_bounds__(640, 1)
     attn_fwd_ws_kernel(const AttnParams p, const __grid_constant__ WsMaps maps, int* sched, int n_units) {
@@ -322,19 +317,20 @@ __global__ void __launch_bounds__(640, 1)
       mbar_init(bar(Cfg::kBarUnit + i), 1);
       mbar_init(bar(Cfg::kBarSFull + i), 1);
       mbar_init(bar(Cfg::kBarSSeen + i), 4);
+      mbar_init(bar(Cfg::kBarPFull + i), 4);
       mbar_init(bar(Cfg::kBarPVDone + i), 1);
     }
     for (int i = 0; i < S; ++i) {
       mbar_init(bar(Cfg::kBarKFull + i), 1);
       mbar_init(bar(Cfg::kBarKReady + i), 8);
       mbar_init(bar(Cfg::kBarVFull + i), 1);
-      mbar_init(bar(Cfg::kBarKVEmpty + i), 1);
+      mbar_init(bar(Cfg::kBarKFree + i), 1);
+      mbar_init(bar(Cfg::kBarVFree + i), 2);
     }
     for (int i = 0; i < NB; ++i) {
       mbar_init(bar(Cfg::kBarBufFree + i), 1);
-      mbar_init(bar(Cfg::kBarPFull + i), 4);
     }
-    mbar_init(bar(Cfg::kBarFinal), 1);
+    for (int i = 0; i < 3; ++i) mbar_init(bar(Cfg::kBarFinal + i), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -355,9 +351,7 @@ __global__ void __launch_bounds__(640, 1)
   if (warp >= 16) {
     regs_dec<64>();
   }
-  if (warp >= 18) {
-    // idle warps: straight to the final barrier
-  } else if (warp == 16) {
+  if (warp == 16) {
     if (lane == 0) {
       // ---------------- producer: tickets and TMA loads ----------------
       prefetch_tmap(&maps.q);
@@ -399,7 +393,8 @@ __global__ void __launch_bounds__(640, 1)
         for (int j = g.kb_all; j <= g.ke_all; ++j, ++kcnt) {
           const int st = kcnt % S;
           const uint32_t ph = (kcnt / S) & 1;
-          if (!mbar_wait_or_abort(bar(Cfg::kBarKVEmpty + st), ph ^ 1, abort_flag)) {
+          if (!mbar_wait_or_abort(bar(Cfg::kBarKFree + st), ph ^ 1, abort_flag) ||
+              !mbar_wait_or_abort(bar(Cfg::kBarVFree + st), ph ^ 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -434,133 +429,103 @@ __global__ void __launch_bounds__(640, 1)
     }
   } else if (warp == 17) {
     if (lane == 0) {
-      // ---------------- MMA issuer (event driven) ----------------
+      // ---------------- S issuer: S = Q^ K^^T jobs in stream order ----------------
       using G = TileGeom<D>;
       constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, false);
-      constexpr uint32_t idesc_o = make_idesc_bf16(128, D, true);
       bool ok = true;
-      // S side: the next S job (unit s_ul, key tile s_j, query tile s_t), global index gS.
-      UnitGeom sg;
-      uint32_t s_ul = 0, gS = 0, s_kc = 0;
-      int s_j = 0, s_t = 0;
-      int s_state = 0;  // 0: unit not yet known, 1: have a job, 2: no more units
-      // P.V side: per query tile a FIFO of issued S jobs (at most kSBufs in flight in total).
-      PvJob q0[NB], q1[NB];
-      int q0_head = 0, q0_n = 0, q1_head = 0, q1_n = 0;
-      int kv_left[S];  // P.V jobs still to read the V tile of each ring stage
-#pragma unroll
-      for (int i = 0; i < S; ++i) kv_left[i] = 0;
-      uint32_t scnt0 = 0, scnt1 = 0;  // S jobs issued per query tile
-      uint64_t idle_since = 0;
-
-      while (ok) {
-        bool progress = false;
-        // ---- the next S job ----
-        if (s_state == 0) {
-          const int slot = s_ul & 1;
-          const uint32_t uph = (s_ul >> 1) & 1;
-          if (mbar_test(bar(Cfg::kBarUnit + slot), uph)) {
-            const int unit = unit_id[slot];
-            if (unit < 0) {
-              s_state = 2;
-              progress = true;
-            } else if (mbar_test(bar(Cfg::kBarQReady + slot), uph)) {
-              tc_fence_after();
-              unit_geom(p, n_qb, unit, sg);
-              s_j = sg.kb_all;
-              s_t = sg.has(0, s_j) ? 0 : 1;
-              s_state = 1;
-              progress = true;
+      uint32_t gS = 0, kc = 0, scnt0 = 0, scnt1 = 0;
+      for (uint32_t ul = 0; ok; ++ul) {
+        const int slot = ul & 1;
+        const uint32_t uph = (ul >> 1) & 1;
+        if (!mbar_wait_or_abort(bar(Cfg::kBarUnit + slot), uph, abort_flag)) { ok = false; break; }
+        const int unit = unit_id[slot];
+        if (unit < 0) break;
+        if (!mbar_wait_or_abort(bar(Cfg::kBarQReady + slot), uph, abort_flag)) { ok = false; break; }
+        UnitGeom g;
+        unit_geom(p, n_qb, unit, g);
+        for (int j = g.kb_all; j <= g.ke_all && ok; ++j, ++kc) {
+          const int st = kc % S;
+          if (!mbar_wait_or_abort(bar(Cfg::kBarKReady + st), (kc / S) & 1, abort_flag)) { ok = false; break; }
+          const uint32_t ka = smem_u32(k_tile(st));
+#pragma unroll 1
+          for (int t = 0; t < 2; ++t) {
+            if (!g.has(t, j)) continue;
+            const int b = gS % NB;
+            uint32_t& sc = t == 0 ? scnt0 : scnt1;
+            if (!mbar_wait_or_abort(bar(Cfg::kBarBufFree + b), ((gS / NB) & 1) ^ 1, abort_flag) ||
+                !mbar_wait_or_abort(bar(Cfg::kBarSSeen + t), (sc & 1) ^ 1, abort_flag)) {
+              ok = false;
+              break;
             }
-          }
-        }
-        if (s_state == 1) {
-          const int st = s_kc % S;
-          const int b = gS % NB;
-          const uint32_t sc = s_t == 0 ? scnt0 : scnt1;
-          if (mbar_test(bar(Cfg::kBarKReady + st), (s_kc / S) & 1) &&
-              mbar_test(bar(Cfg::kBarBufFree + b), ((gS / NB) & 1) ^ 1) &&
-              mbar_test(bar(Cfg::kBarSSeen + s_t), (sc & 1) ^ 1)) {
             tc_fence_after();
-            const uint32_t qa = smem_u32(q_tile(s_ul & 1, s_t));
-            const uint32_t ka = smem_u32(k_tile(st));
+            const uint32_t qa = smem_u32(q_tile(slot, t));
 #pragma unroll
             for (int ks = 0; ks < G::kKSteps; ++ks) {
               const uint64_t ad = make_sdesc(qa + G::kstep_off(ks), 16, G::kSBO, G::kSwizzle);
               const uint64_t bd = make_sdesc(ka + G::kstep_off(ks), 16, G::kSBO, G::kSwizzle);
               umma_ss(tmem + Cfg::col_buf(b), ad, bd, idesc_s, ks > 0 ? 1u : 0u);
             }
-            umma_commit(bar(Cfg::kBarSFull + s_t));
-            if (s_t == 0) ++scnt0;
-            else ++scnt1;
-            const PvJob job{gS, s_kc, s_j == sg.kb(s_t) ? 1 : 0};
-            if (s_t == 0) {
-              q0[(q0_head + q0_n) % NB] = job;
-              ++q0_n;
-            } else {
-              q1[(q1_head + q1_n) % NB] = job;
-              ++q1_n;
-            }
-            if (s_t == 0 || !sg.has(0, s_j)) kv_left[st] = (sg.has(0, s_j) ? 1 : 0) + (sg.has(1, s_j) ? 1 : 0);
+            umma_commit(bar(Cfg::kBarSFull + t));
+            ++sc;
             ++gS;
-            // advance the cursor
-            if (s_t == 0 && sg.has(1, s_j)) {
-              s_t = 1;
-            } else if (s_j < sg.ke_all) {
-              ++s_j;
-              ++s_kc;
-              s_t = sg.has(0, s_j) ? 0 : 1;
-            } else {
-              ++s_kc;
-              ++s_ul;
-              s_state = 0;
-            }
-            progress = true;
           }
-        }
-        // ---- P.V jobs, independently per query tile ----
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int qn = t == 0 ? q0_n : q1_n;
-          if (qn == 0) continue;
-          const PvJob job = t == 0 ? q0[q0_head] : q1[q1_head];
-          const int st = job.kc % S;
-          if (!mbar_test(bar(Cfg::kBarPFull + job.g % NB), (job.g / NB) & 1) ||
-              !mbar_test(bar(Cfg::kBarVFull + st), (job.kc / S) & 1))
-            continue;
-          tc_fence_after();
-          const uint32_t va = smem_u32(v_tile(st));
-          const uint32_t pa = tmem + Cfg::col_buf(job.g % NB) + 64;
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t bd = make_sdesc(va + ks * 16 * G::kRowBytes, 16, G::kSBO, G::kSwizzle);
-            umma_ts(tmem + Cfg::col_o(t), pa + ks * 8, bd, idesc_o, (!job.first || ks > 0) ? 1u : 0u);
-          }
-          umma_commit(bar(Cfg::kBarBufFree + job.g % NB));
-          umma_commit(bar(Cfg::kBarPVDone + t));
-          if (--kv_left[st] == 0) umma_commit(bar(Cfg::kBarKVEmpty + st));
-          if (t == 0) {
-            q0_head = (q0_head + 1) % NB;
-            --q0_n;
-          } else {
-            q1_head = (q1_head + 1) % NB;
-            --q1_n;
-          }
-          progress = true;
-        }
-        if (s_state == 2 && q0_n == 0 && q1_n == 0) break;
-        if (progress) {
-          idle_since = 0;
-        } else {
-          const uint64_t now = globaltimer();
-          if (idle_since == 0) idle_since = now;
-          else if (now - idle_since > kWaitTimeoutNs || *abort_flag) ok = false;
+          if (ok) umma_commit(bar(Cfg::kBarKFree + st));  // K^ of this stage no longer read
         }
       }
       if (!ok) fail();
-      // Drain: all MMAs this thread issued complete before TMEM is freed.
-      umma_commit(bar(Cfg::kBarFinal));
-      mbar_wait(bar(Cfg::kBarFinal), 0);
+      umma_commit(bar(Cfg::kBarFinal + 0));
+      mbar_wait(bar(Cfg::kBarFinal + 0), 0);
+    }
+  } else if (warp == 18 || warp == 19) {
+    if (lane == 0) {
+      // ---------------- P.V issuer of query tile t: O_t += P V, in order ----------------
+      using G = TileGeom<D>;
+      constexpr uint32_t idesc_o = make_idesc_bf16(128, D, true);
+      const int t = warp - 18;
+      bool ok = true;
+      uint32_t gS = 0, kc = 0, pcnt = 0;
+      for (uint32_t ul = 0; ok; ++ul) {
+        const int slot = ul & 1;
+        const uint32_t uph = (ul >> 1) & 1;
+        if (!mbar_wait_or_abort(bar(Cfg::kBarUnit + slot), uph, abort_flag)) { ok = false; break; }
+        const int unit = unit_id[slot];
+        if (unit < 0) break;
+        UnitGeom g;
+        unit_geom(p, n_qb, unit, g);
+        for (int j = g.kb_all; j <= g.ke_all; ++j, ++kc) {
+          const bool h0 = g.has(0, j), h1 = g.has(1, j);
+          const uint32_t gj = gS + (t == 1 && h0 ? 1u : 0u);
+          gS += (h0 ? 1u : 0u) + (h1 ? 1u : 0u);
+          const int st = kc % S;
+          // Every step's V phase is observed (and released) by both issuers, active or not, so the
+          // stage's barriers never run two phases ahead of either of them.
+          if (!mbar_wait_or_abort(bar(Cfg::kBarVFull + st), (kc / S) & 1, abort_flag)) { ok = false; break; }
+          if (!(t == 0 ? h0 : h1)) {
+            mbar_arrive(bar(Cfg::kBarVFree + st));
+            continue;
+          }
+          const int b = gj % NB;
+          // P of this tile's next job: the softmax writes the one after only once this P.V is done,
+          // so the per-tile barrier is never more than one phase ahead of this wait.
+          if (!mbar_wait_or_abort(bar(Cfg::kBarPFull + t), pcnt & 1, abort_flag)) { ok = false; break; }
+          ++pcnt;
+          tc_fence_after();
+          const uint32_t va = smem_u32(v_tile(st));
+          const uint32_t pa = tmem + Cfg::col_buf(b) + 64;
+          const bool first = j == g.kb(t);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t bd = make_sdesc(va + ks * 16 * G::kRowBytes, 16, G::kSBO, G::kSwizzle);
+            umma_ts(tmem + Cfg::col_o(t), pa + ks * 8, bd, idesc_o, (!first || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(bar(Cfg::kBarBufFree + b));
+          umma_commit(bar(Cfg::kBarPVDone + t));
+          umma_commit(bar(Cfg::kBarVFree + st));
+        }
+      }
+      if (!ok) fail();
+      umma_commit(bar(Cfg::kBarFinal + 1 + t));
+      mbar_wait(bar(Cfg::kBarFinal + 1 + t), 0);
     }
   } else if (warp >= 8) {
     regs_dec<80>();
@@ -728,7 +693,7 @@ __global__ void __launch_bounds__(640, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(Cfg::kBarPFull + b));
+        if (lane == 0) mbar_arrive(bar(Cfg::kBarPFull + t));
         ++n;
       }
       if (!ok) break;
