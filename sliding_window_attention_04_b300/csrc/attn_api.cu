@@ -108,7 +108,7 @@ CUresult encode_tile_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* 
 }
 
 // cos / sin of t * base^(-2i/D) for t < T, i < D/2, evaluated in double and rounded to fp32.
-// Layout [D/4][T] of float4 (cos_2m, sin_2m, cos_2m+1, sin_2m+1): for a fixed pair group the
+// Layout [D/4][T] of float4 (cos_2m, cos_2m+1, sin_2m, sin_2m+1): for a fixed pair group the
 // positions are contiguous, so a warp whose threads hold consecutive rows loads whole lines.
 cudaError_t build_table(int D, float base, int T, float4** out) {
   std::vector<float4> h(static_cast<size_t>(T) * (D / 4));
@@ -121,7 +121,7 @@ cudaError_t build_table(int D, float base, int T, float4** out) {
         cs[2 * k] = static_cast<float>(std::cos(theta));
         cs[2 * k + 1] = static_cast<float>(std::sin(theta));
       }
-      h[static_cast<size_t>(m) * T + t] = make_float4(cs[0], cs[1], cs[2], cs[3]);
+      h[static_cast<size_t>(m) * T + t] = make_float4(cs[0], cs[2], cs[1], cs[3]);
     }
   float4* d = nullptr;
   cudaError_t e = cudaMalloc(&d, h.size() * sizeof(float4));
@@ -190,9 +190,9 @@ __global__ void noalloc_prepare_kernel(unsigned char* scratch, int T, int D, flo
     const double theta = static_cast<double>(t) * pow(static_cast<double>(base), -2.0 * i / D);
     double sn, cs;
     sincos(theta, &sn, &cs);
-    float* dst = table + 4 * (static_cast<size_t>(i / 2) * T + t) + 2 * (i % 2);
+    float* dst = table + 4 * (static_cast<size_t>(i / 2) * T + t) + (i % 2);
     dst[0] = static_cast<float>(cs);
-    dst[1] = static_cast<float>(sn);
+    dst[2] = static_cast<float>(sn);
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(scratch) = 0;
 }

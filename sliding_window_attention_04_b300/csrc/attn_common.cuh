@@ -19,7 +19,7 @@ struct AttnParams {
   const __nv_bfloat16* v;  // [B, T, H, D]
   __nv_bfloat16* out;      // [B, T, H, D]
   float* lse;              // [B, H, T] or nullptr
-  const float4* rope;      // [D/4][rope_T] (cos, sin) of pairs 2i, 2i+1, or nullptr (RoPE off)
+  const float4* rope;      // [D/4][rope_T] (cos_2i, cos_2i+1, sin_2i, sin_2i+1), or nullptr (RoPE off)
   int rope_T;              // positions the table covers (its row stride), >= T
   int* err;                // device error word
   int B, H, T;
@@ -118,7 +118,7 @@ __device__ __forceinline__ void qk_row_transform_packed(uint32_t (&w)[D / 2], in
 #pragma unroll
     for (int i2 = 0; i2 < Q4; ++i2) {
       const float4 t = __ldg(cs + static_cast<size_t>(i2) * rope_T);
-      const uint64_t cos2 = f2_pack(t.x, t.z), sin2 = f2_pack(t.y, t.w);
+      const uint64_t cos2 = f2_pack(t.x, t.y), sin2 = f2_pack(t.z, t.w);
       const uint64_t c2 = f2_mul(cos2, r2), s2 = f2_mul(sin2, r2), sn2 = f2_mul(sin2, nr2);
       const uint64_t x1 = bf16x2_to_f2<D>(w[i2]), x2 = bf16x2_to_f2<D>(w[i2 + Q4]);
       const uint64_t y1 = f2_fma(x1, c2, f2_mul(x2, s2));

@@ -159,7 +159,7 @@ __device__ __forceinline__ bool tile_needs_mask(const AttnParams& p, int qs, int
 // 4 / 4 and are combined with one shuffle in the order qk_row_transform_packed uses.
 template <int D>
 struct RopeHalf {
-  float4 cs[D / 8];  // (cos, sin) of pairs 2 i2, 2 i2 + 1 for this half's i2 values
+  float4 cs[D / 8];  // (cos, cos, sin, sin) of pairs 2 i2, 2 i2 + 1 for this half's i2 values
   __device__ __forceinline__ void load(const AttnParams& p, int pos, int h) {
     if (p.rope == nullptr) return;
     const float4* src = p.rope + pos;
@@ -207,7 +207,7 @@ __device__ __forceinline__ void transform_half_row_inplace(uint8_t* tile, int ro
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         const float4 t = tab.cs[2 * c + q];
-        const uint64_t cos2 = f2_pack(t.x, t.z), sin2 = f2_pack(t.y, t.w);
+        const uint64_t cos2 = f2_pack(t.x, t.y), sin2 = f2_pack(t.z, t.w);
         const uint64_t c2 = f2_mul(cos2, r2), s2 = f2_mul(sin2, r2), sn2 = f2_mul(sin2, nr2);
         uint32_t& a = w[2 * c + q];
         uint32_t& b = w[2 * (c + NC / 2) + q];
