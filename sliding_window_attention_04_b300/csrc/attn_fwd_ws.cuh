@@ -609,7 +609,8 @@ __global__ void __launch_bounds__(640, 1)
         const uint32_t tS = tmem + lane_base + Cfg::col_buf(b);
         // visible columns of this row in this tile: lo <= c <= hi
         int lo = 0, hi = kTile - 1;
-        if (tile_needs_mask(p, qs, k0)) {
+        const bool masked = tile_needs_mask(p, qs, k0);  // same for the whole warpgroup
+        if (masked) {
           lo = p.window >= 0 ? i_row - p.window - k0 : -1;
           hi = p.causal ? i_row - k0 : (p.window >= 0 ? i_row + p.window - k0 : kTile);
           hi = min(hi, p.T - 1 - k0);
@@ -641,8 +642,8 @@ __global__ void __launch_bounds__(640, 1)
 #pragma unroll 1
         for (int it = 0; it < 3; ++it) {
           const int hb = it == 1 ? 2 : 0;  // first block of the half
-          const uint32_t va = block_vis(lo - 32 * hb, hi - 32 * hb);
-          const uint32_t vc = block_vis(lo - 32 * hb - 32, hi - 32 * hb - 32);
+          const uint32_t va = masked ? block_vis(lo - 32 * hb, hi - 32 * hb) : 0xFFFFFFFFu;
+          const uint32_t vc = masked ? block_vis(lo - 32 * hb - 32, hi - 32 * hb - 32) : 0xFFFFFFFFu;
           uint32_t a[32], c[32];
           float ra = -INFINITY, rc = -INFINITY;
           __syncwarp();  // warp-collective TMEM loads after per-row branches
