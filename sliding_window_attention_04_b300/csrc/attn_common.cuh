@@ -109,7 +109,7 @@ __device__ __forceinline__ void qk_row_transform_packed(uint32_t (&w)[D / 2], in
     const uint64_t e = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
     const float ss = __fadd_rn(f2_lo(e), f2_hi(e));
     const float ms = __fmul_rn(ss, 1.0f / D);
-    r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+    r = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
   }
   constexpr int Q4 = D / 4;  // words per half row
   if (rope != nullptr) {

@@ -11,18 +11,23 @@
 //   4-7    softmax of query tile 1
 //   8-15   prologue: QK RMSNorm + RoPE of the Q tiles and of every K tile, two threads per row,
 //          in place in shared memory (TMA writes the raw bf16 rows already in the tensor core's
-//          swizzled layout); the cos/sin entries of a row are loaded before its tile arrives
+//          swizzled layout); a row is widened to fp32 once and its cos/sin entries are loaded
+//          while its sum of squares is formed
 //   16     producer: ticket fetch, TMA loads of Q, K, V (lane 0)
 //   17     S issuer (lane 0): S = Q^ K^^T jobs in stream order; TMEM owner
 //   18, 19 P.V issuers of query tiles 0 and 1 (lane 0): O_t += P V in order
 //
 // TMEM (512 columns): three rotating 128-column S/P buffers and O_0, O_1 (D columns each). The
 // S jobs (one per query tile and key tile, in stream order) take the buffers round-robin.
-// Every phase-parity barrier has one producer and one consumer that can never be more than one
-// phase apart: S-done, S-seen, P-written and P.V-done are per query tile (the next S of a tile is
-// issued only after its softmax has seen the previous one; the next P of a tile is written only
-// after its previous P.V has completed), buffer-free is per buffer and waited only by the S
-// issuer, which issues the buffer's next S only after the P.V that read it. A
+// Every wait on a phase-parity barrier is exact: the waiter is never two phases away from the
+// barrier. S-done and S-seen are per query tile (the next S of a tile is issued only after its
+// softmax has seen the previous one). P-written and P.V-done have two slots per tile, used by the
+// tile's even and odd jobs, and S job n of a tile is issued only after the tile's P.V job n - 2 has
+// completed; so P of job n + 2 cannot be written before P.V job n is issued, and a softmax that
+// waits for P.V job n - 1 (O rescale, epilogue) knows that job n - 3 has completed. Buffer-free is
+// per buffer and waited only by the S issuer, which issues the buffer's next S only after the P.V
+// that read it. A softmax writes the P of its next job while the previous P.V may still run (the
+// two sit in different buffers); only the O rescale and the epilogue wait for that P.V. A
 // softmax warpgroup reads S from its buffer and writes P (bf16, 64 columns) into the buffer's upper
 // half once that half has been read, so P needs no space of its own; the P.V MMA reads P from
 // there, and its completion frees the buffer for the S job three places later. With three
@@ -33,10 +38,10 @@
 // (S jobs in stream order) and one P.V issuer per query tile, which wakes as soon as its tile's P
 // is written, so one tile's softmax never holds up the other tile's MMAs.
 //
-// Softmax of one S tile: three TMEM round trips over the two 64-column halves (half 0 for its
-// max with the reducing TMEM load, half 1 for its max and exponentials, half 0 again for its
-// exponentials). A 32-column block that the mask removes for the whole warp is skipped, and only a
-// block that the mask edge cuts is masked element by element. The running max is updated lazily:
+// Softmax of one S tile (softmax_tile): the row max over the four 32-column blocks (reducing TMEM
+// loads), then the exponentials block by block. A row's block that the mask removes entirely
+// gets zero P without exponentials, and only a block that the mask edge cuts is masked element
+// by element; tiles without any masked entry skip the mask tests. The running max is updated lazily:
 // O and l are rescaled only when the tile max exceeds the current reference by more than
 // kRescaleLog2. At the end of a unit the softmax warps normalise O_t, stage it as bf16 in the (now
 // free) Q tile buffer, store it with one TMA store, and write the per-row log-sum-exp.
@@ -71,7 +76,7 @@ struct WsCfg {
   // barrier indices
   static constexpr int kBarQFull = 0;                     // [2] TMA -> prologue
   static constexpr int kBarQReady = 2;                    // [2] prologue -> MMA
-  static constexpr int kBarQEmpty = 4;                    // [2] epilogue stores read -> producer
+  static constexpr int kBarQEmpty = 4;                    // [2] slot free (epilogues, P.V issuers) -> producer
   static constexpr int kBarUnit = 6;                      // [2] producer -> MMA, softmax (unit id)
   static constexpr int kBarKFull = 8;                     // [kStages] TMA -> prologue
   static constexpr int kBarKReady = kBarKFull + kStages;  // [kStages] prologue -> S issuer
@@ -81,12 +86,12 @@ struct WsCfg {
   static constexpr int kBarSFull = kBarVFree + kStages;   // [2] S job of tile t done -> softmax t
   static constexpr int kBarSSeen = kBarSFull + 2;         // [2] softmax t has seen its S -> S issuer
   static constexpr int kBarBufFree = kBarSSeen + 2;       // [kSBufs] P.V job done -> S issuer
-  static constexpr int kBarPFull = kBarBufFree + kSBufs;  // [2] softmax t wrote P -> P.V issuer t
-  static constexpr int kBarPVDone = kBarPFull + 2;        // [2] P.V job of tile t done -> softmax t
-  static constexpr int kBarFinal = kBarPVDone + 2;        // [3] MMA drain at exit (S issuer, P.V issuers)
+  static constexpr int kBarPFull = kBarBufFree + kSBufs;  // [2 tiles][2] softmax t wrote P of job n -> P.V issuer t
+  static constexpr int kBarPVDone = kBarPFull + 4;        // [2 tiles][2] P.V job n of tile t done -> softmax, S issuer
+  static constexpr int kBarFinal = kBarPVDone + 4;        // [3] MMA drain at exit (S issuer, P.V issuers)
   static constexpr int kNumBars = kBarFinal + 3;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, unit ids
-  static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, unit ids, unit geometry
+  static constexpr int kSmemBytes = kOffMisc + 128 + 1024;  // + alignment slack
   // TMEM columns
   static constexpr uint32_t kTmemCols = 512;
   static __device__ __forceinline__ uint32_t col_buf(int b) { return static_cast<uint32_t>(128 * b); }
@@ -172,57 +177,60 @@ struct RopeHalf {
 };
 
 template <int D>
-__device__ __forceinline__ void transform_half_row_inplace(uint8_t* tile, int row, int h, const RopeHalf<D>& tab,
+__device__ __forceinline__ void transform_half_row_inplace(uint8_t* tile, int row, int h, int pos, RopeHalf<D>& tab,
                                                            const AttnParams& p) {
   constexpr int NC = D / 8;  // chunks per row; this thread owns 2 words (4 elements) of each
-  uint32_t w[2 * NC];        // w[2c], w[2c+1]: elements 8c + 4h + {0,1} and {2,3}
+  uint64_t x[2 * NC];        // x[2c], x[2c+1]: elements 8c + 4h + {0,1} and {2,3} as fp32 pairs
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
     const uint2 u = *reinterpret_cast<const uint2*>(tile + tile_off<D>(row, c) + 8 * h);
-    w[2 * c] = u.x;
-    w[2 * c + 1] = u.y;
+    x[2 * c] = bf16x2_to_f2<D>(u.x);
+    x[2 * c + 1] = bf16x2_to_f2<D>(u.y);
   }
   float r = 1.0f;
   if (p.use_norm) {
     uint64_t acc0 = 0, acc1 = 0;  // (P_{4h}, P_{4h+1}), (P_{4h+2}, P_{4h+3})
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-      const uint64_t a = bf16x2_to_f2<D>(w[2 * c]), b = bf16x2_to_f2<D>(w[2 * c + 1]);
-      acc0 = f2_fma(a, a, acc0);
-      acc1 = f2_fma(b, b, acc1);
+      acc0 = f2_fma(x[2 * c], x[2 * c], acc0);
+      acc1 = f2_fma(x[2 * c + 1], x[2 * c + 1], acc1);
     }
     const uint64_t mine = f2_add(acc0, acc1);  // h=0: (P0+P2, P1+P3); h=1: (P4+P6, P5+P7)
     const uint64_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
     const uint64_t e = h == 0 ? f2_add(mine, other) : f2_add(other, mine);
     const float ss = __fadd_rn(f2_lo(e), f2_hi(e));
     const float ms = __fmul_rn(ss, 1.0f / D);
-    r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, p.eps)));
+    r = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, p.eps)));  // = 1 / sqrt(.), both correctly rounded
   }
   if (p.rope != nullptr) {
+    // Loaded here rather than before the tile arrives: keeping both the fp32 row and the table
+    // live across the wait does not fit the prologue's register share.
+    tab.load(p, pos, h);
     const uint64_t r2 = f2_pack(r, r), nr2 = f2_pack(-r, -r);
-    // pair i = 8c + 4h + 2q + e (c < NC/2, q, e in {0,1}) lives in word w[2c + q], element e;
-    // its partner i + D/2 is in word w[2(c + NC/2) + q]. Table entry k = 2c + q.
+    // pair i = 8c + 4h + 2q + e (c < NC/2, q, e in {0,1}) is element e of x[2c + q]; its partner
+    // i + D/2 is element e of x[2(c + NC/2) + q]. Table entry k = 2c + q.
 #pragma unroll
-    for (int c = 0; c < NC / 2; ++c)
+    for (int c = 0; c < NC / 2; ++c) {
+      uint32_t wa[2], wb[2];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         const float4 t = tab.cs[2 * c + q];
         const uint64_t cos2 = f2_pack(t.x, t.y), sin2 = f2_pack(t.z, t.w);
         const uint64_t c2 = f2_mul(cos2, r2), s2 = f2_mul(sin2, r2), sn2 = f2_mul(sin2, nr2);
-        uint32_t& a = w[2 * c + q];
-        uint32_t& b = w[2 * (c + NC / 2) + q];
-        const uint64_t x1 = bf16x2_to_f2<D>(a), x2 = bf16x2_to_f2<D>(b);
-        a = f2_to_bf16x2(f2_fma(x1, c2, f2_mul(x2, s2)));
-        b = f2_to_bf16x2(f2_fma(x2, c2, f2_mul(x1, sn2)));
+        const uint64_t x1 = x[2 * c + q], x2 = x[2 * (c + NC / 2) + q];
+        wa[q] = f2_to_bf16x2(f2_fma(x1, c2, f2_mul(x2, s2)));
+        wb[q] = f2_to_bf16x2(f2_fma(x2, c2, f2_mul(x1, sn2)));
       }
+      *reinterpret_cast<uint2*>(tile + tile_off<D>(row, c) + 8 * h) = make_uint2(wa[0], wa[1]);
+      *reinterpret_cast<uint2*>(tile + tile_off<D>(row, c + NC / 2) + 8 * h) = make_uint2(wb[0], wb[1]);
+    }
   } else {
     const uint64_t r2 = f2_pack(r, r);
 #pragma unroll
-    for (int k = 0; k < 2 * NC; ++k) w[k] = f2_to_bf16x2(f2_mul(bf16x2_to_f2<D>(w[k]), r2));
+    for (int c = 0; c < NC; ++c)
+      *reinterpret_cast<uint2*>(tile + tile_off<D>(row, c) + 8 * h) =
+          make_uint2(f2_to_bf16x2(f2_mul(x[2 * c], r2)), f2_to_bf16x2(f2_mul(x[2 * c + 1], r2)));
   }
-#pragma unroll
-  for (int c = 0; c < NC; ++c)
-    *reinterpret_cast<uint2*>(tile + tile_off<D>(row, c) + 8 * h) = make_uint2(w[2 * c], w[2 * c + 1]);
 }
 
 struct WsMaps {
@@ -285,6 +293,59 @@ __device__ __forceinline__ void exp_store(const uint32_t (&s)[32], bool empty, u
   tmem_st16(tP, pk);
 }
 
+// Softmax of one S tile held in TMEM at tS for this thread's row (lane): the row sees columns
+// lo..hi when `masked` (an unmasked tile: all 128). Writes P (bf16) over the upper half of the
+// buffer, returns the row sum of P and sets the new reference max m_new and the factor alpha that
+// rescales the previous O and l. `masked` is uniform over the warpgroup; the unmasked tiles skip
+// the per-block mask tests at run time.
+//
+// Two passes over the four 32-column blocks of S: the row max, two blocks per TMEM round trip with
+// the reducing load; then the exponentials one block per round trip, in the order 3, 2, 0, 1 so
+// that S blocks 3 and 2 are read before P (16 columns per block, at column 64 + 16 b) covers them.
+// The kernel is limited by instruction fetch more than by instruction count: this form keeps one
+// copy of the exponential code and measured faster than handling two blocks per trip, which
+// needs two copies; likewise one copy serves masked and unmasked tiles.
+__device__ __forceinline__ float softmax_tile(bool masked, uint32_t tS, int lo, int hi, float scale, uint64_t scale2,
+                                              float m_used, float& m_new, float& alpha) {
+  float mx = -INFINITY;
+#pragma unroll 1
+  for (int hb = 0; hb < 4; hb += 2) {
+    const uint32_t va = masked ? block_vis(lo - 32 * hb, hi - 32 * hb) : 0xFFFFFFFFu;
+    const uint32_t vc = masked ? block_vis(lo - 32 * hb - 32, hi - 32 * hb - 32) : 0xFFFFFFFFu;
+    uint32_t a[32], c[32];
+    float ra = -INFINITY, rc = -INFINITY;
+    __syncwarp();  // warp-collective TMEM loads after per-row branches
+    tmem_ld32_max(tS + 32 * hb, a, ra);
+    tmem_ld32_max(tS + 32 * hb + 32, c, rc);
+    tmem_ld_wait();
+    reg_fence<32>(a);
+    reg_fence<32>(c);
+    asm volatile("" : "+f"(ra), "+f"(rc));
+    mx = fmax3(mx, block_max(a, ra, va), block_max(c, rc, vc));
+  }
+  const float m_tile = mx * scale;
+  const bool grow = m_tile > m_used + kRescaleLog2 || (m_used == -INFINITY && m_tile > -INFINITY);
+  m_new = grow ? m_tile : m_used;
+  alpha = grow ? ex2_approx(m_used - m_new) : 1.0f;  // 0 when m_used = -inf
+  const float m_use = m_new == -INFINITY ? 0.f : m_new;
+  const uint64_t negm2 = f2_pack(-m_use, -m_use);
+  uint64_t sumA = 0, sumB = 0;  // pairs of fp32 zeros
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i) {
+    const int bk = i < 2 ? 3 - i : i - 2;
+    const uint32_t v = masked ? block_vis(lo - 32 * bk, hi - 32 * bk) : 0xFFFFFFFFu;
+    uint32_t a[32];
+    __syncwarp();
+    tmem_ld32(tS + 32 * bk, a);
+    tmem_ld_wait();
+    reg_fence<32>(a);
+    if (v != 0xFFFFFFFFu) mask_block(a, v);
+    exp_store(a, v == 0u, scale2, negm2, tS + 64 + 16 * bk, sumA, sumB);
+  }
+  const uint64_t sum2 = f2_add(sumA, sumB);
+  return f2_lo(sum2) + f2_hi(sum2);
+}
+
 template <int D>
 __global__ void __launch_bounds__(640, 1)
     attn_fwd_ws_kernel(const AttnParams p, const __grid_constant__ WsMaps maps, int* sched, int n_units) {
@@ -299,6 +360,8 @@ __global__ void __launch_bounds__(640, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
   volatile int* unit_id = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);  // [2]
+  // [2] geometry of the unit in each slot, written by the producer with the unit id
+  UnitGeom* unit_geo = reinterpret_cast<UnitGeom*>(smem + Cfg::kOffMisc + 16);
   auto bar = [&](int i) { return bars + i; };
   auto q_tile = [&](int slot, int t) { return smem + Cfg::kOffQ + (2 * slot + t) * TB; };
   auto k_tile = [&](int st) { return smem + Cfg::kOffK + st * TB; };
@@ -313,10 +376,12 @@ __global__ void __launch_bounds__(640, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(Cfg::kBarQFull + i), 1);
       mbar_init(bar(Cfg::kBarQReady + i), 8);
-      mbar_init(bar(Cfg::kBarQEmpty + i), 2);
+      mbar_init(bar(Cfg::kBarQEmpty + i), 4);
       mbar_init(bar(Cfg::kBarUnit + i), 1);
       mbar_init(bar(Cfg::kBarSFull + i), 1);
       mbar_init(bar(Cfg::kBarSSeen + i), 4);
+    }
+    for (int i = 0; i < 4; ++i) {
       mbar_init(bar(Cfg::kBarPFull + i), 4);
       mbar_init(bar(Cfg::kBarPVDone + i), 1);
     }
@@ -375,14 +440,17 @@ __global__ void __launch_bounds__(640, 1)
         }
         int unit = atomicAdd(sched, 1);
         if (unit >= n_units) unit = -1;
+        UnitGeom g;
+        if (unit >= 0) {
+          unit_geom(p, n_qb, unit, g);
+          unit_geo[slot] = g;  // read by the other roles after the unit barrier
+        }
         unit_id[slot] = unit;
         mbar_arrive(bar(Cfg::kBarUnit + slot));
         if (unit < 0) {
           mbar_arrive(bar(Cfg::kBarQFull + slot));
           break;
         }
-        UnitGeom g;
-        unit_geom(p, n_qb, unit, g);
         const bool two = g.valid(1);
         mbar_arrive_expect_tx(bar(Cfg::kBarQFull + slot), (two ? 2 : 1) * TB);
         q_armed[slot] = static_cast<int>(uph);
@@ -441,8 +509,7 @@ __global__ void __launch_bounds__(640, 1)
         const int unit = unit_id[slot];
         if (unit < 0) break;
         if (!mbar_wait_or_abort(bar(Cfg::kBarQReady + slot), uph, abort_flag)) { ok = false; break; }
-        UnitGeom g;
-        unit_geom(p, n_qb, unit, g);
+        const UnitGeom g = unit_geo[slot];
         for (int j = g.kb_all; j <= g.ke_all && ok; ++j, ++kc) {
           const int st = kc % S;
           if (!mbar_wait_or_abort(bar(Cfg::kBarKReady + st), (kc / S) & 1, abort_flag)) { ok = false; break; }
@@ -452,8 +519,13 @@ __global__ void __launch_bounds__(640, 1)
             if (!g.has(t, j)) continue;
             const int b = gS % NB;
             uint32_t& sc = t == 0 ? scnt0 : scnt1;
+            // S job n of tile t waits for the tile's P.V job n - 2: when its softmax then waits for
+            // P.V job n - 1 (O rescale, epilogue), job n - 3 is known to be complete and job n + 1
+            // cannot be, so that two-slot parity wait is exact.
             if (!mbar_wait_or_abort(bar(Cfg::kBarBufFree + b), ((gS / NB) & 1) ^ 1, abort_flag) ||
-                !mbar_wait_or_abort(bar(Cfg::kBarSSeen + t), (sc & 1) ^ 1, abort_flag)) {
+                !mbar_wait_or_abort(bar(Cfg::kBarSSeen + t), (sc & 1) ^ 1, abort_flag) ||
+                (sc >= 2 && !mbar_wait_or_abort(bar(Cfg::kBarPVDone + 2 * t + (sc & 1)), ((sc - 2) >> 1) & 1,
+                                                abort_flag))) {
               ok = false;
               break;
             }
@@ -490,8 +562,11 @@ __global__ void __launch_bounds__(640, 1)
         if (!mbar_wait_or_abort(bar(Cfg::kBarUnit + slot), uph, abort_flag)) { ok = false; break; }
         const int unit = unit_id[slot];
         if (unit < 0) break;
-        UnitGeom g;
-        unit_geom(p, n_qb, unit, g);
+        const UnitGeom g = unit_geo[slot];
+        // The slot's unit id and geometry have been read: the producer may reuse the slot once the
+        // epilogues are done too. (An issuer whose query tile lies past T has no P.V job in the
+        // unit, so without this arrival the epilogues alone would not order its read.)
+        mbar_arrive(bar(Cfg::kBarQEmpty + slot));
         for (int j = g.kb_all; j <= g.ke_all; ++j, ++kc) {
           const bool h0 = g.has(0, j), h1 = g.has(1, j);
           const uint32_t gj = gS + (t == 1 && h0 ? 1u : 0u);
@@ -505,10 +580,13 @@ __global__ void __launch_bounds__(640, 1)
             continue;
           }
           const int b = gj % NB;
-          // P of this tile's next job: the softmax writes the one after only once this P.V is done,
-          // so the per-tile barrier is never more than one phase ahead of this wait.
-          if (!mbar_wait_or_abort(bar(Cfg::kBarPFull + t), pcnt & 1, abort_flag)) { ok = false; break; }
-          ++pcnt;
+          // P of this tile's job k, on slot k & 1: P of job k + 2 needs S job k + 2, which waits for
+          // this P.V, so the slot is never two phases ahead of this wait.
+          const uint32_t k = pcnt++;
+          if (!mbar_wait_or_abort(bar(Cfg::kBarPFull + 2 * t + (k & 1)), (k >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t va = smem_u32(v_tile(st));
           const uint32_t pa = tmem + Cfg::col_buf(b) + 64;
@@ -519,7 +597,7 @@ __global__ void __launch_bounds__(640, 1)
             umma_ts(tmem + Cfg::col_o(t), pa + ks * 8, bd, idesc_o, (!first || ks > 0) ? 1u : 0u);
           }
           umma_commit(bar(Cfg::kBarBufFree + b));
-          umma_commit(bar(Cfg::kBarPVDone + t));
+          umma_commit(bar(Cfg::kBarPVDone + 2 * t + (k & 1)));
           umma_commit(bar(Cfg::kBarVFree + st));
         }
       }
@@ -543,8 +621,7 @@ __global__ void __launch_bounds__(640, 1)
       if (!ok) break;
       const int unit = unit_id[slot];
       if (unit < 0) break;
-      UnitGeom g;
-      unit_geom(p, n_qb, unit, g);
+      const UnitGeom g = unit_geo[slot];
       // jobs 0, 1: the two Q tiles; jobs 2..: the K tiles of the unit, in stream order
       const int n_jobs = 2 + g.ke_all - g.kb_all + 1;
 #pragma unroll 1
@@ -557,12 +634,11 @@ __global__ void __launch_bounds__(640, 1)
         const int st = kcnt % S;
         const int pos = is_q ? g.qs0 + kTile * jb + r : (g.kb_all + jb - 2) * kTile + r;
         uint8_t* tile = is_q ? q_tile(slot, jb) : k_tile(st);
-        tab.load(p, pos < p.T ? pos : 0, h);  // independent of the tile: issued before the wait
         if (!is_q) {
           ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarKFull + st), (kcnt / S) & 1, abort_flag));
           if (!ok) break;
         }
-        transform_half_row_inplace<D>(tile, r, h, tab, p);
+        transform_half_row_inplace<D>(tile, r, h, pos < p.T ? pos : 0, tab, p);
         fence_proxy_async_smem();
         __syncwarp();
         if (is_q) {
@@ -593,8 +669,7 @@ __global__ void __launch_bounds__(640, 1)
       if (!ok) break;
       const int unit = unit_id[slot];
       if (unit < 0) break;
-      UnitGeom g;
-      unit_geom(p, n_qb, unit, g);
+      const UnitGeom g = unit_geo[slot];
       const int qs = g.qs0 + kTile * t;
       const int i_row = qs + r;
       float m_used = -INFINITY;  // reference max of this row (log2 units)
@@ -621,63 +696,16 @@ __global__ void __launch_bounds__(640, 1)
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) mbar_arrive(bar(Cfg::kBarSSeen + t));
-        // This tile's previous P.V must have completed before any P of this job is written to
-        // TMEM (and before O is rescaled). The P tiles live in different buffers, but measured
-        // results show corrupted outputs when these TMEM stores overlap the tile's P.V in flight.
-        if (n > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarPVDone + t), (n - 1) & 1, abort_flag));
+
+        float m_new, alpha;
+        const float rowsum = softmax_tile(masked, tS, lo, hi, scale, scale2, m_used, m_new, alpha);
+        // O rescale (rare): after the tile's previous P.V job (n - 1) has completed; the next one is
+        // issued only after this job's P is announced.
+        if (j > g.kb(t) && __any_sync(0xffffffffu, alpha != 1.0f)) {
+          ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarPVDone + 2 * t + ((n - 1) & 1)),
+                                                          ((n - 1) >> 1) & 1, abort_flag));
           if (!ok) break;
           tc_fence_after();
-        }
-
-        // Three TMEM round trips over the two 64-column halves of S: it = 0 reads half 0 for its
-        // max, it = 1 reads half 1 for its max and exponentials, it = 2 reads half 0 again for its
-        // exponentials. P of blocks 2, 3 goes to columns 96..127 (S block 3, read at it = 1) and
-        // P of blocks 0, 1 to columns 64..95 (S block 2, read at it = 1).
-        float mx = -INFINITY;
-        float alpha = 1.0f, m_new = m_used;
-        uint64_t negm2 = 0;
-        uint64_t sumA = 0, sumB = 0;  // pairs of fp32 zeros
-        bool grow = false;
-#pragma unroll 1
-        for (int it = 0; it < 3; ++it) {
-          const int hb = it == 1 ? 2 : 0;  // first block of the half
-          const uint32_t va = masked ? block_vis(lo - 32 * hb, hi - 32 * hb) : 0xFFFFFFFFu;
-          const uint32_t vc = masked ? block_vis(lo - 32 * hb - 32, hi - 32 * hb - 32) : 0xFFFFFFFFu;
-          uint32_t a[32], c[32];
-          float ra = -INFINITY, rc = -INFINITY;
-          __syncwarp();  // warp-collective TMEM loads after per-row branches
-          tmem_ld32_max(tS + 32 * hb, a, ra);
-          tmem_ld32_max(tS + 32 * hb + 32, c, rc);
-          tmem_ld_wait();
-          reg_fence<32>(a);
-          reg_fence<32>(c);
-          asm volatile("" : "+f"(ra), "+f"(rc));
-          if (it < 2) {
-            mx = fmax3(mx, block_max(a, ra, va), block_max(c, rc, vc));
-          } else {
-            if (va != 0xFFFFFFFFu) mask_block(a, va);
-            if (vc != 0xFFFFFFFFu) mask_block(c, vc);
-          }
-          if (it == 1) {
-            const float m_tile = mx * scale;
-            grow = m_tile > m_used + kRescaleLog2 || (m_used == -INFINITY && m_tile > -INFINITY);
-            m_new = grow ? m_tile : m_used;
-            alpha = grow ? ex2_approx(m_used - m_new) : 1.0f;  // 0 when m_used = -inf
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            negm2 = f2_pack(-m_use, -m_use);
-          }
-          if (it >= 1) {
-            const uint32_t pcol = it == 1 ? 96u : 64u;
-            exp_store(a, va == 0u, scale2, negm2, tS + pcol, sumA, sumB);
-            exp_store(c, vc == 0u, scale2, negm2, tS + pcol + 16, sumA, sumB);
-          }
-        }
-        const uint64_t sum2 = f2_add(sumA, sumB);
-        const float rowsum = f2_lo(sum2) + f2_hi(sum2);
-        // O rescale (rare): this tile's previous P.V has finished (waited above) and the next one is
-        // issued only after this step's P is announced.
-        if (j > g.kb(t) && __any_sync(0xffffffffu, alpha != 1.0f)) {
           uint32_t o[32];
 #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
@@ -694,7 +722,7 @@ __global__ void __launch_bounds__(640, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(Cfg::kBarPFull + t));
+        if (lane == 0) mbar_arrive(bar(Cfg::kBarPFull + 2 * t + (n & 1)));
         ++n;
       }
       if (!ok) break;
@@ -704,10 +732,11 @@ __global__ void __launch_bounds__(640, 1)
         continue;
       }
       // ---- epilogue: O / l -> bf16 staged in this tile's Q buffer, one TMA store; LSE ----
-      ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarPVDone + t), (n - 1) & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarPVDone + 2 * t + ((n - 1) & 1)),
+                                                      ((n - 1) >> 1) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
+      const float inv_l = l_run > 0.f ? __frcp_rn(l_run) : 0.f;  // = 1 / l_run, correctly rounded
       uint8_t* stage = q_tile(slot, t);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
