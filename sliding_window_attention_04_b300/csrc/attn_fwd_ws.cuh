@@ -425,11 +425,8 @@ __global__ void __launch_bounds__(640, 1)
       prefetch_tmap(&maps.out);
       const uint64_t pol_stream = policy_evict_first();
       const uint64_t pol_keep = policy_evict_last();
-      int q_armed[2] = {-1, -1};  // parity of the last armed phase of each barrier (for draining)
-      int k_armed[S], v_armed[S];
-#pragma unroll
-      for (int i = 0; i < S; ++i) k_armed[i] = v_armed[i] = -1;
-      uint32_t kcnt = 0;
+      int q_armed[2] = {-1, -1};  // parity of the last armed phase of each Q barrier (for draining)
+      uint32_t kcnt = 0;          // K/V stage loads issued
       bool ok = true;
       for (uint32_t ul = 0;; ++ul) {
         const int slot = ul & 1;
@@ -466,9 +463,6 @@ __global__ void __launch_bounds__(640, 1)
             ok = false;
             break;
           }
-#pragma unroll
-          for (int i = 0; i < S; ++i)
-            if (i == st) k_armed[i] = v_armed[i] = static_cast<int>(ph);
           mbar_arrive_expect_tx(bar(Cfg::kBarKFull + st), TB);
           tma_load_4d_hint(k_tile(st), &maps.k, bar(Cfg::kBarKFull + st), 0, g.h, j * kTile, g.b, pol_keep);
           mbar_arrive_expect_tx(bar(Cfg::kBarVFull + st), TB);
@@ -478,13 +472,22 @@ __global__ void __launch_bounds__(640, 1)
       }
       if (!ok) {
         fail();
-        // Drain: every TMA load this thread issued must land before the CTA exits.
-        for (int i = 0; i < 2; ++i)
-          if (q_armed[i] >= 0) mbar_wait(bar(Cfg::kBarQFull + i), static_cast<uint32_t>(q_armed[i]));
-#pragma unroll
-        for (int i = 0; i < S; ++i) {
-          if (k_armed[i] >= 0) mbar_wait(bar(Cfg::kBarKFull + i), static_cast<uint32_t>(k_armed[i]));
-          if (v_armed[i] >= 0) mbar_wait(bar(Cfg::kBarVFull + i), static_cast<uint32_t>(v_armed[i]));
+        // Drain: every TMA load this thread issued must land before the CTA exits. Only the last
+        // S K/V loads can still be in flight (each earlier one was consumed before its stage was
+        // reloaded); load n went to stage n % S, phase n / S.
+        const uint32_t first = kcnt > static_cast<uint32_t>(S) ? kcnt - S : 0u;
+#pragma unroll 1
+        for (uint32_t m = 2 * first; m < 2 * kcnt + 2; ++m) {
+          int b, par;
+          if (m >= 2 * kcnt) {
+            b = Cfg::kBarQFull + static_cast<int>(m - 2 * kcnt);
+            par = q_armed[m - 2 * kcnt];
+          } else {
+            const uint32_t n = m >> 1;
+            b = ((m & 1) ? Cfg::kBarVFull : Cfg::kBarKFull) + static_cast<int>(n % S);
+            par = static_cast<int>((n / S) & 1);
+          }
+          if (par >= 0) mbar_wait(bar(b), static_cast<uint32_t>(par));
         }
       }
       // The last CTA to leave resets the ticket counters for the next launch on this slot.

@@ -76,14 +76,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait that also gives up early once another role of the CTA has set `abort`.
+__device__ __forceinline__ uint32_t globaltimer_lo() {
+  uint32_t t;
+  asm volatile("mov.u32 %0, %%globaltimer_lo;" : "=r"(t));
+  return t;
+}
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, const volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (true) {
+  const uint32_t t0 = globaltimer_lo();
+  do {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer() - t0 > kWaitTimeoutNs) return false;
-  }
+  } while ((*abort == 0) & (globaltimer_lo() - t0 < static_cast<uint32_t>(kWaitTimeoutNs)));
+  return false;
 }
 
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy
