@@ -82,6 +82,20 @@ int attn_init(int device);
 int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int T, int D,
              int window, int causal, float rope_base, float eps, void* stream);
 
+/* attn_fwd_gqa — attn_fwd with grouped K/V heads (habr "Autoresearch" deep dive, train.py
+ * listing: GPTConfig.n_kv_head and CausalSelfAttention, where k and v are projected to
+ * n_kv_head <= n_head heads, n_head % n_kv_head == 0, and passed to the attention call as
+ * they are). Query head h attends with K/V head h / (H / H_kv), the convention of that call.
+ *
+ *  k, v      [in]  bf16 [B, T, H_kv, D], 16-byte aligned; out must not overlap them.
+ *  H_kv            1 <= H_kv <= H and H % H_kv == 0 (else ATTN_ERR_INVALID_ARG).
+ *  everything else as attn_fwd (q, out [B, T, H, D]; lse [B, H, T]). H_kv = H is exactly
+ *  attn_fwd. The norm and rotation of each K row are applied once per query tile that reads
+ *  it, as for attn_fwd.
+ */
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int H_kv,
+                 int T, int D, int window, int causal, float rope_base, float eps, void* stream);
+
 /* attn_fwd_kernel — which kernel attn_fwd launches for head dimension D on the initialised
  * device: 1 = the warp-specialised persistent kernel (TMA-fed K/V ring, tcgen05 MMAs into TMEM,
  * separate prologue, MMA and softmax warps; D = 32 and 64), 0 = the single-warpgroup kernel

@@ -6,7 +6,9 @@ code with the CUDA path (see attn_oracle.c for the step-by-step definition and t
 of the pages each step follows).
 
 Every function takes q, k, v as bf16 tensors (CPU torch.bfloat16) or uint16 numpy arrays of
-bf16 bit patterns, in [B, T, H, D] layout, and returns float64 numpy arrays.
+bf16 bit patterns: q in [B, T, H, D] layout, k and v in [B, T, Hkv, D] with H a multiple of Hkv
+(grouped K/V heads: query head h uses K/V head h // (H // Hkv); Hkv = H is multi-head attention),
+and returns float64 numpy arrays.
 
 `qk_precision` selects how the QK-norm + RoPE prologue is evaluated before q^ and k^ are
 rounded to bf16: "f32" (default, used for parity) takes that quantisation decision with the same
@@ -38,10 +40,11 @@ def _load():
         f64p = ctypes.POINTER(ctypes.c_double)
         i32p = ctypes.POINTER(ctypes.c_int32)
         ci, cd, cl = ctypes.c_int, ctypes.c_double, ctypes.c_long
-        lib.oracle_attn_fwd.argtypes = [u16p, u16p, u16p, f64p, f64p, ci, ci, ci, ci, ci, ci, cd, cd, ci, ci, ci]
-        lib.oracle_attn_rows.argtypes = [u16p, u16p, u16p, i32p, cl, f64p, f64p, ci, ci, ci, ci, ci, ci,
+        lib.oracle_attn_fwd.argtypes = [u16p, u16p, u16p, f64p, f64p, ci, ci, ci, ci, ci, ci, ci, cd, cd, ci, ci, ci]
+        lib.oracle_attn_rows.argtypes = [u16p, u16p, u16p, i32p, cl, f64p, f64p, ci, ci, ci, ci, ci, ci, ci,
                                          cd, cd, ci, ci, ci]
-        lib.oracle_attn_probs.argtypes = [u16p, u16p, u16p, ci, ci, f64p, ci, ci, ci, ci, ci, ci, cd, cd, ci, ci]
+        lib.oracle_attn_probs.argtypes = [u16p, u16p, u16p, ci, ci, f64p, ci, ci, ci, ci, ci, ci, ci, cd, cd, ci,
+                                          ci]
         lib.oracle_qk_prologue.argtypes = [u16p, f64p, ci, ci, ci, ci, cd, cd, ci, ci, ci]
         lib.oracle_round_bf16.argtypes = [cd]
         lib.oracle_round_bf16.restype = cd
@@ -104,16 +107,24 @@ def qk_prologue(x, rope_base: float = 10000.0, eps: float = 1e-6, round_qk: bool
     return y
 
 
+def _kv_heads(qb, kb, vb) -> int:
+    B, T, H, D = qb.shape
+    Hkv = kb.shape[2]
+    assert kb.shape == (B, T, Hkv, D) and vb.shape == kb.shape, "k, v must be [B, T, Hkv, D]"
+    assert 1 <= Hkv <= H and H % Hkv == 0, "H must be a multiple of Hkv"
+    return Hkv
+
+
 def attn_fwd(q, k, v, window: int = -1, causal: bool = True, rope_base: float = 10000.0,
              eps: float = 1e-6, round_qk: bool = True, nthreads: int = 0, qk_precision: str = "f32"):
     """Full forward. Returns (out float64 [B, T, H, D], lse float64 [B, H, T], natural log)."""
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     B, T, H, D = qb.shape
-    assert kb.shape == qb.shape and vb.shape == qb.shape
+    Hkv = _kv_heads(qb, kb, vb)
     out = np.empty((B, T, H, D), dtype=np.float64)
     lse = np.empty((B, H, T), dtype=np.float64)
     _check(_load().oracle_attn_fwd(_p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
-                                   _p(out, ctypes.c_double), _p(lse, ctypes.c_double), B, H, T, D,
+                                   _p(out, ctypes.c_double), _p(lse, ctypes.c_double), B, H, Hkv, T, D,
                                    int(window), int(bool(causal)), float(rope_base), float(eps),
                                    int(round_qk), _prec(qk_precision), int(nthreads)))
     return out, lse
@@ -125,13 +136,14 @@ def attn_rows(q, k, v, rows, window: int = -1, causal: bool = True, rope_base: f
     Returns (out float64 [n, D], lse float64 [n])."""
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     B, T, H, D = qb.shape
+    Hkv = _kv_heads(qb, kb, vb)
     r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
     n = r.shape[0]
     out = np.empty((n, D), dtype=np.float64)
     lse = np.empty((n,), dtype=np.float64)
     _check(_load().oracle_attn_rows(_p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
                                     _p(r, ctypes.c_int32), n, _p(out, ctypes.c_double), _p(lse, ctypes.c_double),
-                                    B, H, T, D, int(window), int(bool(causal)), float(rope_base), float(eps),
+                                    B, H, Hkv, T, D, int(window), int(bool(causal)), float(rope_base), float(eps),
                                     int(round_qk), _prec(qk_precision), int(nthreads)))
     return out, lse
 
@@ -141,9 +153,10 @@ def attn_probs(q, k, v, b: int, h: int, window: int = -1, causal: bool = True, r
     """The attention weight matrix p [T, T] (queries x keys) of head (b, h)."""
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     B, T, H, D = qb.shape
+    Hkv = _kv_heads(qb, kb, vb)
     p = np.empty((T, T), dtype=np.float64)
     _check(_load().oracle_attn_probs(_p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
-                                     int(b), int(h), _p(p, ctypes.c_double), B, H, T, D, int(window),
+                                     int(b), int(h), _p(p, ctypes.c_double), B, H, Hkv, T, D, int(window),
                                      int(bool(causal)), float(rope_base), float(eps), int(round_qk),
                                      _prec(qk_precision)))
     return p

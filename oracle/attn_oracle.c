@@ -37,6 +37,11 @@
  *     tokens 0..t; habr listing, flash_attn_func(..., causal=True, window_size=(W, 0))):
  *     J(i) = { j in [0, T) : (causal => j <= i),
  *                            (window >= 0 => j >= i - window and (not causal => j <= i + window)) }.
+ *  4b. Grouped K/V heads (habr "Autoresearch" deep dive, train.py listing, GPTConfig.n_kv_head and
+ *     CausalSelfAttention: k and v carry n_kv_head <= n_head heads with n_head % n_kv_head == 0 and
+ *     go to the attention call as they are): query head h attends with K/V head
+ *     h / (n_head / n_kv_head), the convention of the FlashAttention call the listing makes.
+ *     n_kv_head = n_head is plain multi-head attention.
  *  5. softmax(Q K^T / sqrt(d_k)) V ("geometry_of_andrea", "O que a Atenção Calcula" and
  *     "Escalonamento por sqrt(d_k)"): s_ij = q_i . k_j / sqrt(D) for j in J(i); m = max s;
  *     Z = sum exp(s - m); p_ij = exp(s_ij - m) / Z; out_i = sum p_ij v_j; lse_i = m + ln Z.
@@ -168,6 +173,9 @@ static int check_dims(int B, int H, int T, int D, double base) {
   return 1;
 }
 
+/* K/V head count: 1 <= Hkv <= H and H a multiple of Hkv (step 4b). */
+static int check_kv_heads(int H, int Hkv) { return Hkv >= 1 && Hkv <= H && H % Hkv == 0; }
+
 /* Index of element (b, t, h, d) in a [B, T, H, D] tensor. */
 static size_t idx4(int b, int t, int h, int d, int T, int H, int D) {
   return (((size_t)b * T + t) * H + h) * D + d;
@@ -188,11 +196,12 @@ int oracle_qk_prologue(const uint16_t *x, double *y, int B, int T, int H, int D,
   return ORACLE_OK;
 }
 
-/* Step 4-5 for query row i of head (b, h), given prologue outputs qh, kh (doubles, [B,T,H,D]).
+/* Step 4-5 for query row i of head (b, h), given prologue outputs qh ([B,T,H,D] doubles) and kh
+ * ([B,T,Hkv,D] doubles) and v ([B,T,Hkv,D] bf16); the row uses K/V head hk (step 4b).
  * Writes out[0..D) and *lse; if p is non-NULL also writes the T weights p[0..T). */
-static void attend_row(const double *qh, const double *kh, const uint16_t *v, int b, int h, int i,
-                       int T, int H, int D, int window, int causal, double *out, double *lse,
-                       double *p) {
+static void attend_row(const double *qh, const double *kh, const uint16_t *v, int b, int h, int hk,
+                       int i, int T, int H, int Hkv, int D, int window, int causal, double *out,
+                       double *lse, double *p) {
   double *s = (double *)malloc(sizeof(double) * (size_t)T);
   const double scale = 1.0 / sqrt((double)D);
   const double *qi = qh + idx4(b, i, h, 0, T, H, D);
@@ -202,7 +211,7 @@ static void attend_row(const double *qh, const double *kh, const uint16_t *v, in
       s[j] = -INFINITY;
       continue;
     }
-    const double *kj = kh + idx4(b, j, h, 0, T, H, D);
+    const double *kj = kh + idx4(b, j, hk, 0, T, Hkv, D);
     double dot = 0.0;
     for (int d = 0; d < D; ++d) dot += qi[d] * kj[d];
     s[j] = dot * scale;
@@ -222,20 +231,21 @@ static void attend_row(const double *qh, const double *kh, const uint16_t *v, in
     double pj = (s[j] == -INFINITY) ? 0.0 : exp(s[j] - m) / Z;
     if (p) p[j] = pj;
     if (pj == 0.0) continue;
-    for (int d = 0; d < D; ++d) out[d] += pj * bf16_to_double(v[idx4(b, j, h, d, T, H, D)]);
+    for (int d = 0; d < D; ++d) out[d] += pj * bf16_to_double(v[idx4(b, j, hk, d, T, Hkv, D)]);
   }
   *lse = m + log(Z);
   free(s);
 }
 
-/* Full forward: out is [B, T, H, D] doubles, lse is [B, H, T] doubles (either may be NULL). */
+/* Full forward: q is [B, T, H, D], k and v are [B, T, Hkv, D] (bf16 bits); out is [B, T, H, D]
+ * doubles, lse is [B, H, T] doubles (either may be NULL). */
 int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, double *out,
-                    double *lse, int B, int H, int T, int D, int window, int causal,
+                    double *lse, int B, int H, int Hkv, int T, int D, int window, int causal,
                     double rope_base, double eps, int round_qk, int prec, int nthreads) {
-  if (!q || !k || !v || !check_dims(B, H, T, D, rope_base)) return ORACLE_EINVAL;
+  if (!q || !k || !v || !check_dims(B, H, T, D, rope_base) || !check_kv_heads(H, Hkv)) return ORACLE_EINVAL;
   size_t n = (size_t)B * T * H * D;
   double *qh = (double *)malloc(sizeof(double) * n);
-  double *kh = (double *)malloc(sizeof(double) * n);
+  double *kh = (double *)malloc(sizeof(double) * ((size_t)B * T * Hkv * D));
   if (!qh || !kh) {
     free(qh);
     free(kh);
@@ -243,7 +253,7 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, dou
   }
   int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
   oracle_qk_prologue(q, qh, B, T, H, D, rope_base, eps, round_qk, prec, nt);
-  oracle_qk_prologue(k, kh, B, T, H, D, rope_base, eps, round_qk, prec, nt);
+  oracle_qk_prologue(k, kh, B, T, Hkv, D, rope_base, eps, round_qk, prec, nt);
   long rows = (long)B * H * T;
 #pragma omp parallel for schedule(dynamic, 16) num_threads(nt)
   for (long r = 0; r < rows; ++r) {
@@ -251,7 +261,7 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, dou
     int h = (int)((r / T) % H);
     int b = (int)(r / ((long)T * H));
     double o[1024], l;
-    attend_row(qh, kh, v, b, h, i, T, H, D, window, causal, o, &l, NULL);
+    attend_row(qh, kh, v, b, h, h / (H / Hkv), i, T, H, Hkv, D, window, causal, o, &l, NULL);
     if (out)
       for (int d = 0; d < D; ++d) out[idx4(b, i, h, d, T, H, D)] = o[d];
     if (lse) lse[((size_t)b * H + h) * T + i] = l;
@@ -264,10 +274,11 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, dou
 /* Selected rows only: rows is n triples (b, h, i); out is [n, D], lse is [n].
  * The prologue is evaluated for the query row and for every allowed key of it. */
 int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *rows,
-                     long n, double *out, double *lse, int B, int H, int T, int D, int window,
-                     int causal, double rope_base, double eps, int round_qk, int prec,
+                     long n, double *out, double *lse, int B, int H, int Hkv, int T, int D,
+                     int window, int causal, double rope_base, double eps, int round_qk, int prec,
                      int nthreads) {
-  if (!q || !k || !v || !rows || n < 0 || !check_dims(B, H, T, D, rope_base)) return ORACLE_EINVAL;
+  if (!q || !k || !v || !rows || n < 0 || !check_dims(B, H, T, D, rope_base) || !check_kv_heads(H, Hkv))
+    return ORACLE_EINVAL;
   for (long r = 0; r < n; ++r) {
     const int32_t *t3 = rows + 3 * r;
     if (t3[0] < 0 || t3[0] >= B || t3[1] < 0 || t3[1] >= H || t3[2] < 0 || t3[2] >= T)
@@ -277,6 +288,7 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, co
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
   for (long r = 0; r < n; ++r) {
     int b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
+    int hk = h / (H / Hkv);
     /* a private [1, T, 1, D] copy of the prologue for this head's needed rows */
     double *qh = (double *)calloc((size_t)T * D, sizeof(double));
     double *kh = (double *)calloc((size_t)T * D, sizeof(double));
@@ -285,15 +297,15 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, co
     prologue_row(xr, qh + (size_t)i * D, D, i, rope_base, eps, round_qk, prec);
     for (int j = 0; j < T; ++j) {
       if (!key_allowed(i, j, T, window, causal)) continue;
-      for (int d = 0; d < D; ++d) xr[d] = bf16_to_double(k[idx4(b, j, h, d, T, H, D)]);
+      for (int d = 0; d < D; ++d) xr[d] = bf16_to_double(k[idx4(b, j, hk, d, T, Hkv, D)]);
       prologue_row(xr, kh + (size_t)j * D, D, j, rope_base, eps, round_qk, prec);
     }
     /* attend_row indexes a [B, T, H, D] tensor; view the private copy as B = H = 1 and
        gather v into the same [1, T, 1, D] view. */
     uint16_t *vv = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)T * D);
     for (int j = 0; j < T; ++j)
-      for (int d = 0; d < D; ++d) vv[(size_t)j * D + d] = v[idx4(b, j, h, d, T, H, D)];
-    attend_row(qh, kh, vv, 0, 0, i, T, 1, D, window, causal, out + r * D, lse + r, NULL);
+      for (int d = 0; d < D; ++d) vv[(size_t)j * D + d] = v[idx4(b, j, hk, d, T, Hkv, D)];
+    attend_row(qh, kh, vv, 0, 0, 0, i, T, 1, 1, D, window, causal, out + r * D, lse + r, NULL);
     free(vv);
     free(qh);
     free(kh);
@@ -303,24 +315,24 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, co
 
 /* The full weight matrix p[T][T] of head (b, h) (rows: queries, columns: keys). */
 int oracle_attn_probs(const uint16_t *q, const uint16_t *k, const uint16_t *v, int b, int h,
-                      double *p, int B, int H, int T, int D, int window, int causal,
+                      double *p, int B, int H, int Hkv, int T, int D, int window, int causal,
                       double rope_base, double eps, int round_qk, int prec) {
-  if (!q || !k || !v || !p || !check_dims(B, H, T, D, rope_base) || b < 0 || b >= B || h < 0 ||
-      h >= H)
+  if (!q || !k || !v || !p || !check_dims(B, H, T, D, rope_base) || !check_kv_heads(H, Hkv) || b < 0 ||
+      b >= B || h < 0 || h >= H)
     return ORACLE_EINVAL;
   size_t n = (size_t)B * T * H * D;
   double *qh = (double *)malloc(sizeof(double) * n);
-  double *kh = (double *)malloc(sizeof(double) * n);
+  double *kh = (double *)malloc(sizeof(double) * ((size_t)B * T * Hkv * D));
   if (!qh || !kh) {
     free(qh);
     free(kh);
     return ORACLE_ENOMEM;
   }
   oracle_qk_prologue(q, qh, B, T, H, D, rope_base, eps, round_qk, prec, 1);
-  oracle_qk_prologue(k, kh, B, T, H, D, rope_base, eps, round_qk, prec, 1);
+  oracle_qk_prologue(k, kh, B, T, Hkv, D, rope_base, eps, round_qk, prec, 1);
   double o[1024], l;
   for (int i = 0; i < T; ++i)
-    attend_row(qh, kh, v, b, h, i, T, H, D, window, causal, o, &l, p + (size_t)i * T);
+    attend_row(qh, kh, v, b, h, h / (H / Hkv), i, T, H, Hkv, D, window, causal, o, &l, p + (size_t)i * T);
   free(qh);
   free(kh);
   return ORACLE_OK;

@@ -26,7 +26,7 @@ ATTN_ERR_NO_DEVICE = -6
 ATTN_ERR_SCRATCH_LIMIT = -7
 
 EXPORTED = ("attn_init", "attn_fwd", "attn_destroy", "attn_status_string", "attn_device_status",
-            "attn_selftest_wait_timeout", "attn_fwd_noalloc", "attn_fwd_kernel")
+            "attn_selftest_wait_timeout", "attn_fwd_noalloc", "attn_fwd_kernel", "attn_fwd_gqa")
 
 
 class AttnError(RuntimeError):
@@ -46,6 +46,9 @@ def _load() -> ctypes.CDLL:
     lib.attn_fwd.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                              c_int, c_int, c_float, c_float, c_void_p]
     lib.attn_fwd.restype = c_int
+    lib.attn_fwd_gqa.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                                 c_int, c_int, c_int, c_float, c_float, c_void_p]
+    lib.attn_fwd_gqa.restype = c_int
     lib.attn_destroy.argtypes = []
     lib.attn_destroy.restype = None
     lib.attn_status_string.argtypes = [c_int]
@@ -108,6 +111,16 @@ def attn_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, lse_ptr: Opti
                             ctypes.c_void_p(stream or None)))
 
 
+def attn_fwd_gqa_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, lse_ptr: Optional[int], B: int, H: int,
+                     H_kv: int, T: int, D: int, window: int, causal: int, rope_base: float, eps: float,
+                     stream: Optional[int]) -> int:
+    """Pass-through of the grouped-K/V-head C call (k, v have H_kv heads); returns the status code."""
+    return int(lib.attn_fwd_gqa(ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+                                ctypes.c_void_p(out_ptr), ctypes.c_void_p(lse_ptr or None), int(B), int(H),
+                                int(H_kv), int(T), int(D), int(window), int(causal), float(rope_base), float(eps),
+                                ctypes.c_void_p(stream or None)))
+
+
 def attn_fwd_noalloc_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, lse_ptr: Optional[int], B: int, H: int,
                          T: int, D: int, window: int, causal: int, rope_base: float, eps: float,
                          stream: Optional[int]) -> int:
@@ -138,7 +151,9 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: int = -1
              rope_base: float = 10000.0, eps: float = 1e-6, out: Optional[torch.Tensor] = None,
              lse: Optional[torch.Tensor] = None, return_lse: bool = True,
              stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """Attention forward on [B, T, H, D] bf16 CUDA tensors. Returns (out, lse [B, H, T] fp32 or None).
+    """Attention forward on bf16 CUDA tensors: q [B, T, H, D]; k, v [B, T, H_kv, D] with H a multiple
+    of H_kv (grouped K/V heads, query head h reads K/V head h // (H // H_kv); H_kv = H is
+    multi-head attention). Returns (out [B, T, H, D], lse [B, H, T] fp32 or None).
 
     The call is asynchronous on `stream` (default: the current stream of q's device).
     """
@@ -146,8 +161,13 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: int = -1
     if q.dim() != 4:
         raise ValueError("q must be [B, T, H, D]")
     B, T, H, D = q.shape
-    _check_input("k", k, q.shape)
-    _check_input("v", v, q.shape)
+    _check_input("k", k)
+    if k.dim() != 4 or k.shape[0] != B or k.shape[1] != T or k.shape[3] != D:
+        raise ValueError(f"k has shape {tuple(k.shape)}, expected [B, T, H_kv, D] = [{B}, {T}, H_kv, {D}]")
+    H_kv = k.shape[2]
+    if H_kv < 1 or H % H_kv != 0:
+        raise ValueError(f"H = {H} is not a multiple of H_kv = {H_kv}")
+    _check_input("v", v, k.shape)
     if out is None:
         out = torch.empty_like(q)
     else:
@@ -158,9 +178,19 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: int = -1
         if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, T):
             raise ValueError("lse must be a contiguous float32 [B, H, T] tensor")
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
-    rc = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                      lse.data_ptr() if lse is not None else None, B, H, T, D, int(window), int(bool(causal)),
-                      float(rope_base), float(eps), s.cuda_stream)
+    lse_ptr = lse.data_ptr() if lse is not None else None
+    if H_kv == H:
+        rc = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, H, T, D,
+                          int(window), int(bool(causal)), float(rope_base), float(eps), s.cuda_stream)
+    else:
+        rc = attn_fwd_gqa_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, H, H_kv, T, D,
+                              int(window), int(bool(causal)), float(rope_base), float(eps), s.cuda_stream)
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_fwd")
+        raise AttnError(rc, "attn_fwd" if H_kv == H else "attn_fwd_gqa")
     return out, lse
+
+
+def attn_fwd_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, **kwargs):
+    """attn_fwd with grouped K/V heads (k, v: [B, T, H_kv, D]); the same call as attn_fwd, which
+    accepts both shapes."""
+    return attn_fwd(q, k, v, **kwargs)

@@ -159,8 +159,8 @@ int launch_ws(const swa::AttnParams& p, PFN_cuTensorMapEncodeTiled_v12000 encode
               cudaStream_t stream) {
   swa::WsMaps maps;
   if (encode_tile_map(encode, &maps.q, p.q, p.B, p.H, p.T, D) != CUDA_SUCCESS ||
-      encode_tile_map(encode, &maps.k, p.k, p.B, p.H, p.T, D) != CUDA_SUCCESS ||
-      encode_tile_map(encode, &maps.v, p.v, p.B, p.H, p.T, D) != CUDA_SUCCESS ||
+      encode_tile_map(encode, &maps.k, p.k, p.B, p.Hkv, p.T, D) != CUDA_SUCCESS ||
+      encode_tile_map(encode, &maps.v, p.v, p.B, p.Hkv, p.T, D) != CUDA_SUCCESS ||
       encode_tile_map(encode, &maps.out, p.out, p.B, p.H, p.T, D) != CUDA_SUCCESS)
     return ATTN_ERR_CUDA;
   const long long units = static_cast<long long>(p.B) * p.H * ((p.T + 2 * swa::kTile - 1) / (2 * swa::kTile));
@@ -312,25 +312,28 @@ int attn_init(int device) {
   return ATTN_OK;
 }
 
-int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int T, int D,
-             int window, int causal, float rope_base, float eps, void* stream) {
+// attn_fwd and attn_fwd_gqa: q, out [B, T, H, D]; k, v [B, T, Hkv, D]; lse [B, H, T].
+static int fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int Hkv, int T,
+             int D, int window, int causal, float rope_base, float eps, void* stream) {
   // ---- argument checks (host only, nothing launched) ----
   if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || T < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
+  if (Hkv < 1 || Hkv > H || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(rope_base) || rope_base < 0.f) return ATTN_ERR_INVALID_ARG;
   if (std::isnan(eps) || std::isinf(eps)) return ATTN_ERR_INVALID_ARG;
   const long long n_elem = static_cast<long long>(B) * T * H * D;
   if (n_elem >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
   const size_t tensor_bytes = static_cast<size_t>(n_elem) * 2;
+  const size_t kv_bytes = tensor_bytes / static_cast<size_t>(H / Hkv);
   const size_t lse_bytes = static_cast<size_t>(B) * H * T * 4;
-  if (overlaps(out, tensor_bytes, q, tensor_bytes) || overlaps(out, tensor_bytes, k, tensor_bytes) ||
-      overlaps(out, tensor_bytes, v, tensor_bytes))
+  if (overlaps(out, tensor_bytes, q, tensor_bytes) || overlaps(out, tensor_bytes, k, kv_bytes) ||
+      overlaps(out, tensor_bytes, v, kv_bytes))
     return ATTN_ERR_INVALID_ARG;
-  if (lse && (overlaps(lse, lse_bytes, q, tensor_bytes) || overlaps(lse, lse_bytes, k, tensor_bytes) ||
-              overlaps(lse, lse_bytes, v, tensor_bytes) || overlaps(lse, lse_bytes, out, tensor_bytes)))
+  if (lse && (overlaps(lse, lse_bytes, q, tensor_bytes) || overlaps(lse, lse_bytes, k, kv_bytes) ||
+              overlaps(lse, lse_bytes, v, kv_bytes) || overlaps(lse, lse_bytes, out, tensor_bytes)))
     return ATTN_ERR_INVALID_ARG;
   if (D != 32 && D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
 
@@ -380,6 +383,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
   p.err = d_err;
   p.B = B;
   p.H = H;
+  p.Hkv = Hkv;
+  p.kv_group = H / Hkv;
   p.T = T;
   p.window = window < 0 ? -1 : window;
   p.causal = causal;
@@ -398,6 +403,16 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
     default: e = launch_simple<128>(p, st); break;
   }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int T, int D,
+             int window, int causal, float rope_base, float eps, void* stream) {
+  return fwd_impl(q, k, v, out, lse, B, H, H, T, D, window, causal, rope_base, eps, stream);
+}
+
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int H_kv,
+                 int T, int D, int window, int causal, float rope_base, float eps, void* stream) {
+  return fwd_impl(q, k, v, out, lse, B, H, H_kv, T, D, window, causal, rope_base, eps, stream);
 }
 
 int attn_fwd_kernel(int D) {
@@ -526,6 +541,8 @@ int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, flo
   p.err = reinterpret_cast<int*>(scratch);
   p.B = B;
   p.H = H;
+  p.Hkv = H;
+  p.kv_group = 1;
   p.T = T;
   p.window = window < 0 ? -1 : window;
   p.causal = causal;

@@ -15,14 +15,16 @@ constexpr int kDevErrTimeout = 1;
 
 struct AttnParams {
   const __nv_bfloat16* q;  // [B, T, H, D]
-  const __nv_bfloat16* k;  // [B, T, H, D]
-  const __nv_bfloat16* v;  // [B, T, H, D]
+  const __nv_bfloat16* k;  // [B, T, Hkv, D]
+  const __nv_bfloat16* v;  // [B, T, Hkv, D]
   __nv_bfloat16* out;      // [B, T, H, D]
   float* lse;              // [B, H, T] or nullptr
   const float4* rope;      // [D/4][rope_T] (cos_2i, cos_2i+1, sin_2i, sin_2i+1), or nullptr (RoPE off)
   int rope_T;              // positions the table covers (its row stride), >= T
   int* err;                // device error word
   int B, H, T;
+  int Hkv;                 // K/V heads; query head h uses K/V head h / kv_group
+  int kv_group;            // H / Hkv (1: multi-head attention)
   int window;              // < 0: no window
   int causal;
   int use_norm;

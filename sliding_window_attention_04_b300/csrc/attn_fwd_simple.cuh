@@ -51,6 +51,9 @@ __global__ void __launch_bounds__(128, 1) attn_fwd_simple_kernel(const AttnParam
   const int q0 = qt * kTile;
   const size_t row_stride = static_cast<size_t>(p.H) * D;  // elements between consecutive t
   const size_t head_base = static_cast<size_t>(b) * T * row_stride + static_cast<size_t>(h) * D;
+  // K/V rows: Hkv heads per position; this query head reads K/V head h / kv_group
+  const size_t kv_stride = static_cast<size_t>(p.Hkv) * D;
+  const size_t kv_base = static_cast<size_t>(b) * T * kv_stride + static_cast<size_t>(h / p.kv_group) * D;
 
   if (tid == 0) {
     mbar_init(bar, 1);
@@ -101,13 +104,13 @@ __global__ void __launch_bounds__(128, 1) attn_fwd_simple_kernel(const AttnParam
     {
       const int j = k0 + tid;
       uint32_t w[D / 2];
-      const uint4* src = reinterpret_cast<const uint4*>(p.k + head_base + static_cast<size_t>(j) * row_stride);
+      const uint4* src = reinterpret_cast<const uint4*>(p.k + kv_base + static_cast<size_t>(j) * kv_stride);
 #pragma unroll
       for (int ch = 0; ch < D / 8; ++ch) set_chunk<D>(w, ch, j < T ? __ldg(src + ch) : make_uint4(0, 0, 0, 0));
       qk_row_transform_packed<D>(w, j < T ? j : 0, p.rope, p.rope_T, p.use_norm, p.eps);
 #pragma unroll
       for (int ch = 0; ch < D / 8; ++ch) *reinterpret_cast<uint4*>(sK + tile_off<D>(tid, ch)) = get_chunk<D>(w, ch);
-      const uint4* vsrc = reinterpret_cast<const uint4*>(p.v + head_base + static_cast<size_t>(j) * row_stride);
+      const uint4* vsrc = reinterpret_cast<const uint4*>(p.v + kv_base + static_cast<size_t>(j) * kv_stride);
 #pragma unroll
       for (int ch = 0; ch < D / 8; ++ch) {
         const uint4 u = j < T ? __ldg(vsrc + ch) : make_uint4(0, 0, 0, 0);

@@ -105,7 +105,7 @@ constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (log2 units): P 
 // Geometry of one work unit: two 128-row query tiles starting at qs0, qs0 + 128 and the
 // key-tile range [kb_t, ke_t] each needs (empty when kb > ke); [kb_all, ke_all] is their union.
 struct UnitGeom {
-  int b, h, qs0;
+  int b, h, hk, qs0;  // hk: the K/V head of query head h
   int kb0, ke0, kb1, ke1;
   int kb_all, ke_all;
   __device__ __forceinline__ bool has(int t, int j) const {
@@ -121,6 +121,7 @@ __device__ __forceinline__ void unit_geom(const AttnParams& p, int n_qb, int uni
   const int qb = n_qb - 1 - (unit - bh * n_qb);
   g.b = bh / p.H;
   g.h = bh - g.b * p.H;
+  g.hk = g.h / p.kv_group;
   g.qs0 = qb * 2 * kTile;
   const int T = p.T;
   int kb[2], ke[2];
@@ -464,9 +465,9 @@ __global__ void __launch_bounds__(640, 1)
             break;
           }
           mbar_arrive_expect_tx(bar(Cfg::kBarKFull + st), TB);
-          tma_load_4d_hint(k_tile(st), &maps.k, bar(Cfg::kBarKFull + st), 0, g.h, j * kTile, g.b, pol_keep);
+          tma_load_4d_hint(k_tile(st), &maps.k, bar(Cfg::kBarKFull + st), 0, g.hk, j * kTile, g.b, pol_keep);
           mbar_arrive_expect_tx(bar(Cfg::kBarVFull + st), TB);
-          tma_load_4d_hint(v_tile(st), &maps.v, bar(Cfg::kBarVFull + st), 0, g.h, j * kTile, g.b, pol_keep);
+          tma_load_4d_hint(v_tile(st), &maps.v, bar(Cfg::kBarVFull + st), 0, g.hk, j * kTile, g.b, pol_keep);
         }
         if (!ok) break;
       }

@@ -86,6 +86,28 @@ def test_host_validation_codes(binding):
     assert binding.attn_device_status() == E.ATTN_ERR_NOT_INITIALIZED
 
 
+def call_gqa(b, **kw):
+    a = dict(q=FAKE, k=FAKE + (1 << 24), v=FAKE + (2 << 24), out=FAKE + (3 << 24), lse=FAKE + (4 << 24), B=1, H=4,
+             H_kv=2, T=64, D=64, window=-1, causal=1, rope_base=10000.0, eps=1e-6, stream=None)
+    a.update(kw)
+    return b.attn_fwd_gqa_raw(a["q"], a["k"], a["v"], a["out"], a["lse"], a["B"], a["H"], a["H_kv"], a["T"], a["D"],
+                              a["window"], a["causal"], a["rope_base"], a["eps"], a["stream"])
+
+
+def test_gqa_host_validation_codes(binding):
+    E = binding
+    for bad in (0, -1, 3, 8):  # not a divisor of H = 4, or more K/V heads than query heads
+        assert call_gqa(binding, H_kv=bad) == E.ATTN_ERR_INVALID_ARG, bad
+    assert call_gqa(binding, k=FAKE + 8) == E.ATTN_ERR_INVALID_ARG  # misaligned
+    # out [1, 64, 4, 64] bf16 = 32 KB; k [1, 64, 2, 64] = 16 KB: out placed 8 KB into k overlaps it
+    assert call_gqa(binding, out=FAKE + (1 << 24) + 8192) == E.ATTN_ERR_INVALID_ARG
+    # ... and right after the end of k does not
+    assert call_gqa(binding, out=FAKE + (1 << 24) + 16384) == E.ATTN_ERR_NOT_INITIALIZED
+    assert call_gqa(binding) == E.ATTN_ERR_NOT_INITIALIZED
+    assert call_gqa(binding, H_kv=4) == E.ATTN_ERR_NOT_INITIALIZED
+    assert call_gqa(binding, H_kv=1, D=128) == E.ATTN_ERR_NOT_INITIALIZED
+
+
 def test_init_without_device(binding):
     import torch
 

@@ -223,3 +223,24 @@ def test_many_calls_reuse_ticket_slots():
     out, lse = ref.cpu().double().numpy(), lref.cpu().double().numpy()
     r, lr = oracle.attn_fwd(q.cpu(), k.cpu(), v.cpu(), window=200, causal=True)
     assert_close(out, r, lse, lr, "many calls")
+
+
+@pytest.mark.parametrize("D,H,Hkv,T,window", [(64, 4, 2, 513, 127), (64, 6, 1, 300, -1), (32, 4, 2, 300, 100),
+                                             (128, 4, 2, 256, 64), (64, 8, 2, 1024, 512)])
+def test_gqa_parity(D, H, Hkv, T, window):
+    """Grouped K/V heads (k, v with Hkv heads; query head h reads K/V head h // (H // Hkv))."""
+    q, _, _ = make_qkv(2, T, H, D, seed=31 * T + H)
+    _, k, v = make_qkv(2, T, Hkv, D, seed=37 * T + Hkv)
+    check(q, k, v, window, True, what=f"gqa D={D} H={H} Hkv={Hkv} T={T} w={window}")
+
+
+@pytest.mark.parametrize("D", [32, 64, 128])
+def test_gqa_bitwise_equals_repeated_heads(D):
+    """The grouped call computes exactly what the multi-head call computes on repeated K/V heads."""
+    H, Hkv, T = 6, 2, 400
+    q, _, _ = make_qkv(1, T, H, D, seed=4242)
+    _, k, v = make_qkv(1, T, Hkv, D, seed=4343)
+    out, lse = gpu_fwd(q, k, v, window=150, causal=True, return_tensors=True)
+    ref, lref = gpu_fwd(q, k.repeat_interleave(H // Hkv, dim=2), v.repeat_interleave(H // Hkv, dim=2), window=150,
+                        causal=True, return_tensors=True)
+    assert torch.equal(out, ref) and torch.equal(lse, lref)

@@ -318,6 +318,54 @@ def test_rows_match_full():
 
 
 # ---------------------------------------------------------------------------------------------
+# Grouped K/V heads (habr "Autoresearch" deep dive, train.py listing: GPTConfig.n_kv_head and
+# CausalSelfAttention, k and v with n_kv_head heads passed to the attention call): query head h
+# reads K/V head h // (H // Hkv).
+
+
+@pytest.mark.parametrize("H,Hkv,D,window,causal", [(4, 2, 32, 5, True), (4, 1, 64, -1, True),
+                                                   (6, 3, 32, 3, False), (6, 2, 16, 11, True)])
+def test_gqa_equals_mha_on_repeated_kv_heads(H, Hkv, D, window, causal):
+    """Pinned to a library construction of the same attention: multi-head attention on K/V heads
+    repeated with torch.repeat_interleave (head h of the result is head h // g of k). The two must
+    agree bit for bit, for the full forward and for selected rows."""
+    g = H // Hkv
+    q, _, _ = make_qkv(2, 37, H, D, seed=900 + H)
+    _, k, v = make_qkv(2, 37, Hkv, D, seed=901 + Hkv)
+    out, lse = oracle.attn_fwd(q, k, v, window=window, causal=causal)
+    ref, lref = oracle.attn_fwd(q, k.repeat_interleave(g, dim=2), v.repeat_interleave(g, dim=2),
+                                window=window, causal=causal)
+    assert np.array_equal(out, ref) and np.array_equal(lse, lref)
+    rows = [(b, h, i) for b in (0, 1) for h in range(H) for i in (0, 6, 36)]
+    ro, rl = oracle.attn_rows(q, k, v, rows, window=window, causal=causal)
+    for n, (b, h, i) in enumerate(rows):
+        assert np.array_equal(ro[n], out[b, i, h]) and rl[n] == lse[b, h, i]
+
+
+def test_gqa_brute_force():
+    """Brute force (pure Python) on K/V heads expanded by list indexing, T <= 6."""
+    H, Hkv, D = 4, 2, 8
+    for T in (1, 3, 6):
+        q, _, _ = make_qkv(1, T, H, D, seed=910 + T)
+        _, k, v = make_qkv(1, T, Hkv, D, seed=920 + T)
+        qn, kn, vn = (f64(t).tolist() for t in (q, k, v))
+        ke = [[[kn[b][t][h // (H // Hkv)] for h in range(H)] for t in range(T)] for b in range(1)]
+        ve = [[[vn[b][t][h // (H // Hkv)] for h in range(H)] for t in range(T)] for b in range(1)]
+        for window, causal in ((-1, True), (1, True), (2, False)):
+            out, lse = oracle.attn_fwd(q, k, v, window=window, causal=causal, qk_precision="f64")
+            bo, bl = brute.forward(qn, ke, ve, window, causal, 10000.0, 1e-6)
+            np.testing.assert_allclose(out, np.array(bo), rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse, np.array(bl), rtol=0, atol=1e-12)
+
+
+def test_gqa_rejects_non_divisor_heads():
+    q, _, _ = make_qkv(1, 8, 4, 8, seed=1)
+    _, k, v = make_qkv(1, 8, 3, 8, seed=2)
+    with pytest.raises(AssertionError):
+        oracle.attn_fwd(q, k, v)
+
+
+# ---------------------------------------------------------------------------------------------
 # The single-precision prologue (the precision in which q^, k^ are quantised to bf16) computes
 # the same function as the double one, up to its rounding.
 
