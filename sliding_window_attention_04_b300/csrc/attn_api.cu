@@ -163,11 +163,13 @@ int launch_ws(const swa::AttnParams& p, PFN_cuTensorMapEncodeTiled_v12000 encode
       encode_tile_map(encode, &maps.v, p.v, p.B, p.Hkv, p.T, D) != CUDA_SUCCESS ||
       encode_tile_map(encode, &maps.out, p.out, p.B, p.H, p.T, D) != CUDA_SUCCESS)
     return ATTN_ERR_CUDA;
-  const long long units = static_cast<long long>(p.B) * p.H * ((p.T + 2 * swa::kTile - 1) / (2 * swa::kTile));
-  if (units >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
-  const int grid = static_cast<int>(units < sm_count ? units : sm_count);
+  // work is handed out in chunks of two 256-row query blocks of one head (see the kernel)
+  const long long n_qb = (p.T + 2 * swa::kTile - 1) / (2 * swa::kTile);
+  const long long chunks = static_cast<long long>(p.B) * p.H * ((n_qb + 1) / 2);
+  if (chunks >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+  const int grid = static_cast<int>(chunks < sm_count ? chunks : sm_count);
   swa::attn_fwd_ws_kernel<D><<<grid, swa::WsCfg<D>::kThreads, swa::WsCfg<D>::kSmemBytes, stream>>>(
-      p, maps, sched, static_cast<int>(units));
+      p, maps, sched, static_cast<int>(chunks));
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

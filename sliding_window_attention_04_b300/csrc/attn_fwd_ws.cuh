@@ -108,6 +108,10 @@ struct UnitGeom {
   int b, h, hk, qs0;  // hk: the K/V head of query head h
   int kb0, ke0, kb1, ke1;
   int kb_all, ke_all;
+  // Key steps run from ke_all down to kb_all. The first r_in of them reuse K^ / V tiles the
+  // previous unit left in the ring; the last r_out are left there for the next unit.
+  int r_in, r_out;
+  __device__ __forceinline__ int n_steps() const { return ke_all - kb_all + 1; }
   __device__ __forceinline__ bool has(int t, int j) const {
     return t == 0 ? (j >= kb0 && j <= ke0) : (j >= kb1 && j <= ke1);
   }
@@ -116,9 +120,8 @@ struct UnitGeom {
   __device__ __forceinline__ bool valid(int t) const { return kb(t) <= ke(t); }
 };
 
-__device__ __forceinline__ void unit_geom(const AttnParams& p, int n_qb, int unit, UnitGeom& g) {
-  const int bh = unit / n_qb;
-  const int qb = n_qb - 1 - (unit - bh * n_qb);
+__device__ __forceinline__ void unit_geom(const AttnParams& p, int bh, int qb, UnitGeom& g) {
+  g.r_in = g.r_out = 0;
   g.b = bh / p.H;
   g.h = bh - g.b * p.H;
   g.hk = g.h / p.kv_group;
@@ -146,6 +149,17 @@ __device__ __forceinline__ void unit_geom(const AttnParams& p, int n_qb, int uni
   const bool two = kb[1] <= ke[1];
   g.kb_all = two ? min(kb[0], kb[1]) : kb[0];
   g.ke_all = two ? max(ke[0], ke[1]) : ke[0];
+}
+
+// Key tiles that unit `a` (query block qb of a head) and the next unit `nb` of the same CTA (block
+// qb - 1 of the same head) can share through the ring: with both streaming key tiles downwards, the
+// last R tiles `a` loads are the first R that `nb` needs, in the same (first-in, first-out) order,
+// where R = nb.ke_all - a.kb_all + 1. They stay resident when R is at most the ring depth.
+template <int S>
+__device__ __forceinline__ int shared_steps(const UnitGeom& a, const UnitGeom& nb) {
+  if (a.b != nb.b || a.h != nb.h || nb.qs0 + 2 * kTile != a.qs0) return 0;
+  const int R = nb.ke_all - a.kb_all + 1;
+  return (R >= 1 && R <= S && R <= a.n_steps() && R <= nb.n_steps()) ? R : 0;
 }
 
 // Does the 128 x 128 score tile (query rows from qs, keys from k0) contain a masked entry?
@@ -349,7 +363,7 @@ __device__ __forceinline__ float softmax_tile(bool masked, uint32_t tS, int lo, 
 
 template <int D>
 __global__ void __launch_bounds__(640, 1)
-    attn_fwd_ws_kernel(const AttnParams p, const __grid_constant__ WsMaps maps, int* sched, int n_units) {
+    attn_fwd_ws_kernel(const AttnParams p, const __grid_constant__ WsMaps maps, int* sched, int n_chunks) {
   using Cfg = WsCfg<D>;
   constexpr int TB = Cfg::kTileBytes;
   constexpr int S = Cfg::kStages;
@@ -429,6 +443,13 @@ __global__ void __launch_bounds__(640, 1)
       int q_armed[2] = {-1, -1};  // parity of the last armed phase of each Q barrier (for draining)
       uint32_t kcnt = 0;          // K/V stage loads issued
       bool ok = true;
+      // A ticket is a chunk: query blocks qb and qb - 1 of one head, heaviest chunks of every head
+      // first. The two units of a chunk run back to back on this CTA and share the key tiles both
+      // need through the ring (shared_steps).
+      const int n_bh = p.B * p.H;
+      int c_bh = 0, c_qb = -1, c_left = 0;  // the current chunk: head, next query block, units left
+      UnitGeom g;
+      g.r_out = 0;
       for (uint32_t ul = 0;; ++ul) {
         const int slot = ul & 1;
         const uint32_t uph = (ul >> 1) & 1;
@@ -436,11 +457,28 @@ __global__ void __launch_bounds__(640, 1)
           ok = false;
           break;
         }
-        int unit = atomicAdd(sched, 1);
-        if (unit >= n_units) unit = -1;
-        UnitGeom g;
-        if (unit >= 0) {
-          unit_geom(p, n_qb, unit, g);
+        int unit = -1;
+        if (c_left == 0) {
+          const int c = atomicAdd(sched, 1);
+          if (c < n_chunks) {
+            const int rank = c / n_bh;
+            c_bh = c - rank * n_bh;
+            c_qb = n_qb - 1 - 2 * rank;
+            c_left = c_qb >= 1 ? 2 : 1;
+          }
+        }
+        if (c_left > 0) {
+          const int r_in = g.r_out;  // the previous unit (same chunk) left that many steps
+          unit_geom(p, c_bh, c_qb, g);
+          unit = c_bh * n_qb + c_qb;
+          g.r_in = c_left == 1 ? r_in : 0;
+          if (c_left == 2) {
+            UnitGeom nb;
+            unit_geom(p, c_bh, c_qb - 1, nb);
+            g.r_out = shared_steps<S>(g, nb);
+          }
+          --c_left;
+          --c_qb;
           unit_geo[slot] = g;  // read by the other roles after the unit barrier
         }
         unit_id[slot] = unit;
@@ -456,7 +494,9 @@ __global__ void __launch_bounds__(640, 1)
         if (two)
           tma_load_4d_hint(q_tile(slot, 1), &maps.q, bar(Cfg::kBarQFull + slot), 0, g.h, g.qs0 + kTile, g.b,
                            pol_stream);
-        for (int j = g.kb_all; j <= g.ke_all; ++j, ++kcnt) {
+        // key steps from ke_all down; the first r_in are already resident (no load)
+        for (int i = g.r_in; i < g.n_steps(); ++i, ++kcnt) {
+          const int j = g.ke_all - i;
           const int st = kcnt % S;
           const uint32_t ph = (kcnt / S) & 1;
           if (!mbar_wait_or_abort(bar(Cfg::kBarKFree + st), ph ^ 1, abort_flag) ||
@@ -514,9 +554,14 @@ __global__ void __launch_bounds__(640, 1)
         if (unit < 0) break;
         if (!mbar_wait_or_abort(bar(Cfg::kBarQReady + slot), uph, abort_flag)) { ok = false; break; }
         const UnitGeom g = unit_geo[slot];
-        for (int j = g.kb_all; j <= g.ke_all && ok; ++j, ++kc) {
-          const int st = kc % S;
-          if (!mbar_wait_or_abort(bar(Cfg::kBarKReady + st), (kc / S) & 1, abort_flag)) { ok = false; break; }
+        const int n_st = g.n_steps();
+        for (int i = 0; i < n_st && ok; ++i) {
+          const int j = g.ke_all - i;
+          // ring position of step i: a resident step sits where the previous unit loaded it (its
+          // K^-ready phase is complete and the stage is not reloaded before this unit frees it)
+          const uint32_t pos = i < g.r_in ? kc - g.r_in + i : kc++;
+          const int st = pos % S;
+          if (!mbar_wait_or_abort(bar(Cfg::kBarKReady + st), (pos / S) & 1, abort_flag)) { ok = false; break; }
           const uint32_t ka = smem_u32(k_tile(st));
 #pragma unroll 1
           for (int t = 0; t < 2; ++t) {
@@ -545,7 +590,8 @@ __global__ void __launch_bounds__(640, 1)
             ++sc;
             ++gS;
           }
-          if (ok) umma_commit(bar(Cfg::kBarKFree + st));  // K^ of this stage no longer read
+          // K^ of this stage no longer read (unless the next unit reuses it)
+          if (ok && i < n_st - g.r_out) umma_commit(bar(Cfg::kBarKFree + st));
         }
       }
       if (!ok) fail();
@@ -571,16 +617,20 @@ __global__ void __launch_bounds__(640, 1)
         // epilogues are done too. (An issuer whose query tile lies past T has no P.V job in the
         // unit, so without this arrival the epilogues alone would not order its read.)
         mbar_arrive(bar(Cfg::kBarQEmpty + slot));
-        for (int j = g.kb_all; j <= g.ke_all; ++j, ++kc) {
+        const int n_st = g.n_steps();
+        for (int i = 0; i < n_st; ++i) {
+          const int j = g.ke_all - i;
           const bool h0 = g.has(0, j), h1 = g.has(1, j);
           const uint32_t gj = gS + (t == 1 && h0 ? 1u : 0u);
           gS += (h0 ? 1u : 0u) + (h1 ? 1u : 0u);
-          const int st = kc % S;
-          // Every step's V phase is observed (and released) by both issuers, active or not, so the
-          // stage's barriers never run two phases ahead of either of them.
-          if (!mbar_wait_or_abort(bar(Cfg::kBarVFull + st), (kc / S) & 1, abort_flag)) { ok = false; break; }
+          const uint32_t pos = i < g.r_in ? kc - g.r_in + i : kc++;  // ring position (see the S issuer)
+          const int st = pos % S;
+          const bool release = i < n_st - g.r_out;  // not kept for the next unit
+          // Every load's V phase is observed (and released, at its last use) by both issuers, active
+          // or not, so the stage's barriers never run two phases ahead of either of them.
+          if (!mbar_wait_or_abort(bar(Cfg::kBarVFull + st), (pos / S) & 1, abort_flag)) { ok = false; break; }
           if (!(t == 0 ? h0 : h1)) {
-            mbar_arrive(bar(Cfg::kBarVFree + st));
+            if (release) mbar_arrive(bar(Cfg::kBarVFree + st));
             continue;
           }
           const int b = gj % NB;
@@ -594,7 +644,7 @@ __global__ void __launch_bounds__(640, 1)
           tc_fence_after();
           const uint32_t va = smem_u32(v_tile(st));
           const uint32_t pa = tmem + Cfg::col_buf(b) + 64;
-          const bool first = j == g.kb(t);
+          const bool first = j == g.ke(t);  // the unit's first P.V of this tile starts O_t
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint64_t bd = make_sdesc(va + ks * 16 * G::kRowBytes, 16, G::kSBO, G::kSwizzle);
@@ -602,7 +652,7 @@ __global__ void __launch_bounds__(640, 1)
           }
           umma_commit(bar(Cfg::kBarBufFree + b));
           umma_commit(bar(Cfg::kBarPVDone + 2 * t + (k & 1)));
-          umma_commit(bar(Cfg::kBarVFree + st));
+          if (release) umma_commit(bar(Cfg::kBarVFree + st));
         }
       }
       if (!ok) fail();
@@ -626,8 +676,9 @@ __global__ void __launch_bounds__(640, 1)
       const int unit = unit_id[slot];
       if (unit < 0) break;
       const UnitGeom g = unit_geo[slot];
-      // jobs 0, 1: the two Q tiles; jobs 2..: the K tiles of the unit, in stream order
-      const int n_jobs = 2 + g.ke_all - g.kb_all + 1;
+      // jobs 0, 1: the two Q tiles; then the K tiles the producer loads (not the resident ones),
+      // from key step r_in on: step i holds key tile ke_all - i
+      const int n_jobs = 2 + g.n_steps() - g.r_in;
 #pragma unroll 1
       for (int jb = 0; jb < n_jobs; ++jb) {
         const bool is_q = jb < 2;
@@ -636,7 +687,7 @@ __global__ void __launch_bounds__(640, 1)
           continue;
         }
         const int st = kcnt % S;
-        const int pos = is_q ? g.qs0 + kTile * jb + r : (g.kb_all + jb - 2) * kTile + r;
+        const int pos = is_q ? g.qs0 + kTile * jb + r : (g.ke_all - (g.r_in + jb - 2)) * kTile + r;
         uint8_t* tile = is_q ? q_tile(slot, jb) : k_tile(st);
         if (!is_q) {
           ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarKFull + st), (kcnt / S) & 1, abort_flag));
@@ -678,7 +729,7 @@ __global__ void __launch_bounds__(640, 1)
       const int i_row = qs + r;
       float m_used = -INFINITY;  // reference max of this row (log2 units)
       float l_run = 0.f;         // sum of exp2(score - m_used)
-      for (int j = g.kb_all; j <= g.ke_all; ++j) {
+      for (int j = g.ke_all; j >= g.kb_all; --j) {  // key steps downwards, as the MMA issuers
         const bool h0 = g.has(0, j), h1 = g.has(1, j);
         const uint32_t gj = gS + (t == 1 && h0 ? 1u : 0u);
         gS += (h0 ? 1u : 0u) + (h1 ? 1u : 0u);
@@ -705,7 +756,7 @@ __global__ void __launch_bounds__(640, 1)
         const float rowsum = softmax_tile(masked, tS, lo, hi, scale, scale2, m_used, m_new, alpha);
         // O rescale (rare): after the tile's previous P.V job (n - 1) has completed; the next one is
         // issued only after this job's P is announced.
-        if (j > g.kb(t) && __any_sync(0xffffffffu, alpha != 1.0f)) {
+        if (j < g.ke(t) && __any_sync(0xffffffffu, alpha != 1.0f)) {  // not the unit's first job
           ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarPVDone + 2 * t + ((n - 1) & 1)),
                                                           ((n - 1) >> 1) & 1, abort_flag));
           if (!ok) break;
