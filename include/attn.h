@@ -98,9 +98,9 @@ int attn_fwd_gqa(const void* q, const void* k, const void* v, void* out, float* 
 
 /* attn_fwd_kernel — which kernel attn_fwd launches for head dimension D on the initialised
  * device: 1 = the warp-specialised persistent kernel (TMA-fed K/V ring, tcgen05 MMAs into TMEM,
- * separate prologue, MMA and softmax warps; D = 32 and 64), 0 = the single-warpgroup kernel
- * (D = 128, or when the warp-specialised kernel was not compiled to the register count its
- * run-time register split needs). ATTN_ERR_UNSUPPORTED for other D, ATTN_ERR_NOT_INITIALIZED
+ * separate prologue, MMA and softmax warps; D = 32, 64 and 128), 0 = the single-warpgroup kernel
+ * (only when the warp-specialised kernel was not compiled to the register count its run-time
+ * register split needs). ATTN_ERR_UNSUPPORTED for other D, ATTN_ERR_NOT_INITIALIZED
  * before attn_init. Both kernels compute the same function (see attn_fwd). */
 int attn_fwd_kernel(int D);
 

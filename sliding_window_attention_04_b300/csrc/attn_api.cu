@@ -38,7 +38,7 @@ struct State {
   int* d_err = nullptr;
   int* d_sched = nullptr;
   unsigned sched_next = 0;
-  bool ws_ok[2] = {false, false};  // warp-specialised kernel usable for D = 32, 64
+  bool ws_ok[3] = {false, false, false};  // warp-specialised kernel usable for D = 32, 64, 128
   std::map<std::pair<int, float>, RopeTable> tables;  // (D, base) -> table
   std::vector<float4*> retired;                       // outgrown tables, freed at destroy
   PFN_cuTensorMapEncodeTiled_v12000 encode_tiled = nullptr;
@@ -100,10 +100,11 @@ CUresult encode_tile_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* 
                               static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
                                  static_cast<cuuint64_t>(T) * H * D * 2};
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(swa::kTile), 1};
+  // D = 128 rows are 256 bytes: a box covers 64 columns (the 128-byte swizzle span), two per tile
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(D > 64 ? 64 : D), 1, static_cast<cuuint32_t>(swa::kTile), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, D == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
@@ -273,7 +274,7 @@ int attn_init(int device) {
   if (prop.major != 10 || prop.minor != 3) return ATTN_ERR_NO_DEVICE;
   int* d_err = nullptr;
   int* d_sched = nullptr;
-  bool ws_ok[2] = {false, false};
+  bool ws_ok[3] = {false, false, false};
   cudaError_t e = with_device(device, [&]() -> cudaError_t {
     cudaError_t r;
     if ((r = set_kernel_attrs<32>()) != cudaSuccess) return r;
@@ -281,6 +282,7 @@ int attn_init(int device) {
     if ((r = set_kernel_attrs<128>()) != cudaSuccess) return r;
     if ((r = set_ws_attrs<32>(&ws_ok[0])) != cudaSuccess) return r;
     if ((r = set_ws_attrs<64>(&ws_ok[1])) != cudaSuccess) return r;
+    if ((r = set_ws_attrs<128>(&ws_ok[2])) != cudaSuccess) return r;
     if ((r = cudaMalloc(&d_err, sizeof(int))) != cudaSuccess) return r;
     if ((r = cudaMemset(d_err, 0, sizeof(int))) != cudaSuccess) return r;
     const size_t sched_bytes = sizeof(int) * kSchedSlots * kSchedStride;
@@ -308,6 +310,7 @@ int attn_init(int device) {
   s.sched_next = 0;
   s.ws_ok[0] = ws_ok[0];
   s.ws_ok[1] = ws_ok[1];
+  s.ws_ok[2] = ws_ok[2];
   s.device = device;
   s.sm_count = prop.multiProcessorCount;
   s.inited = true;
@@ -351,7 +354,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
     std::lock_guard<std::mutex> lock(s.mu);
     if (!s.inited) return ATTN_ERR_NOT_INITIALIZED;
     d_err = s.d_err;
-    use_ws = (D == 32 && s.ws_ok[0]) || (D == 64 && s.ws_ok[1]);
+    use_ws = (D == 32 && s.ws_ok[0]) || (D == 64 && s.ws_ok[1]) || (D == 128 && s.ws_ok[2]);
     if (use_ws) {
       sched = s.d_sched + static_cast<size_t>(s.sched_next % kSchedSlots) * kSchedStride;
       ++s.sched_next;
@@ -397,7 +400,13 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
   if (static_cast<long long>(B) * H * p.n_qtiles >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (use_ws) return D == 32 ? launch_ws<32>(p, encode, sm_count, sched, st) : launch_ws<64>(p, encode, sm_count, sched, st);
+  if (use_ws) {
+    switch (D) {
+      case 32: return launch_ws<32>(p, encode, sm_count, sched, st);
+      case 64: return launch_ws<64>(p, encode, sm_count, sched, st);
+      default: return launch_ws<128>(p, encode, sm_count, sched, st);
+    }
+  }
   cudaError_t e;
   switch (D) {
     case 32: e = launch_simple<32>(p, st); break;
@@ -423,7 +432,7 @@ int attn_fwd_kernel(int D) {
   if (!s.inited) return ATTN_ERR_NOT_INITIALIZED;
   if (D == 32) return s.ws_ok[0] ? 1 : 0;
   if (D == 64) return s.ws_ok[1] ? 1 : 0;
-  if (D == 128) return 0;
+  if (D == 128) return s.ws_ok[2] ? 1 : 0;
   return ATTN_ERR_UNSUPPORTED;
 }
 

@@ -66,11 +66,14 @@ struct WsCfg {
   using G = TileGeom<D>;
   static constexpr int kThreads = 640;
   static constexpr int kLaunchRegs = 96;  // per thread at launch; the run-time split adds up to it
-  static constexpr int kStages = 4;                      // K/V ring depth
-  static constexpr int kSBufs = 3;                       // S/P buffers in TMEM
+  // D = 128: 32 KB tiles and 128-column O accumulators; one Q slot (the next unit's Q is loaded
+  // after the current unit's epilogues), a 2-stage ring and two S/P buffers fit shared memory and TMEM.
+  static constexpr int kQSlots = D == 128 ? 1 : 2;       // units whose Q tiles are resident at once
+  static constexpr int kStages = D == 128 ? 2 : 4;       // K/V ring depth
+  static constexpr int kSBufs = D == 128 ? 2 : 3;        // S/P buffers in TMEM
   static constexpr int kTileBytes = G::kBytes;           // one 128 x D bf16 tile
-  static constexpr int kOffQ = 0;                        // [2 slots][2 tiles] Q^ / output staging
-  static constexpr int kOffK = kOffQ + 4 * kTileBytes;   // [kStages] K^ (transformed in place)
+  static constexpr int kOffQ = 0;                        // [kQSlots][2 tiles] Q^ / output staging
+  static constexpr int kOffK = kOffQ + 2 * kQSlots * kTileBytes;  // [kStages] K^ (transformed in place)
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   // barrier indices
@@ -191,9 +194,79 @@ struct RopeHalf {
   }
 };
 
+// D = 128: the same arithmetic in two passes over shared memory (the row is widened twice), so that
+// the fp32 row and the cos/sin entries never need to be live at once: the sum of squares chunk by
+// chunk (the same per-residue order as below), then the rotation in two groups of four chunk pairs
+// (c, c + 8), each with its eight table entries.
+__device__ __forceinline__ void transform_half_row_d128(uint8_t* tile, int row, int h, int pos, const AttnParams& p) {
+  constexpr int D = 128, NC = D / 8;
+  float r = 1.0f;
+  if (p.use_norm) {
+    uint64_t acc0 = 0, acc1 = 0;  // (P_{4h}, P_{4h+1}), (P_{4h+2}, P_{4h+3})
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const uint2 u = *reinterpret_cast<const uint2*>(tile + tile_off<D>(row, c) + 8 * h);
+      const uint64_t a = bf16x2_to_f2<D>(u.x), b = bf16x2_to_f2<D>(u.y);
+      acc0 = f2_fma(a, a, acc0);
+      acc1 = f2_fma(b, b, acc1);
+    }
+    const uint64_t mine = f2_add(acc0, acc1);
+    const uint64_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
+    const uint64_t e = h == 0 ? f2_add(mine, other) : f2_add(other, mine);
+    const float ss = __fadd_rn(f2_lo(e), f2_hi(e));
+    const float ms = __fmul_rn(ss, 1.0f / D);
+    r = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, p.eps)));  // = 1 / sqrt(.), both correctly rounded
+  }
+  if (p.rope != nullptr) {
+    const uint64_t r2 = f2_pack(r, r), nr2 = f2_pack(-r, -r);
+    const float4* src = p.rope + pos;
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp) {
+      float4 cs[8];  // table entries k = 8 grp + kk, k = 2c + q
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int k = 8 * grp + kk;
+        const int i2 = 4 * (k >> 1) + 2 * h + (k & 1);
+        cs[kk] = __ldg(src + static_cast<size_t>(i2) * p.rope_T);
+      }
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int c = 4 * grp + cc;
+        const uint2 u1 = *reinterpret_cast<const uint2*>(tile + tile_off<D>(row, c) + 8 * h);
+        const uint2 u2 = *reinterpret_cast<const uint2*>(tile + tile_off<D>(row, c + NC / 2) + 8 * h);
+        const uint32_t w1[2] = {u1.x, u1.y}, w2[2] = {u2.x, u2.y};
+        uint32_t wa[2], wb[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float4 t = cs[2 * cc + q];
+          const uint64_t cos2 = f2_pack(t.x, t.y), sin2 = f2_pack(t.z, t.w);
+          const uint64_t c2 = f2_mul(cos2, r2), s2 = f2_mul(sin2, r2), sn2 = f2_mul(sin2, nr2);
+          const uint64_t x1 = bf16x2_to_f2<D>(w1[q]), x2 = bf16x2_to_f2<D>(w2[q]);
+          wa[q] = f2_to_bf16x2(f2_fma(x1, c2, f2_mul(x2, s2)));
+          wb[q] = f2_to_bf16x2(f2_fma(x2, c2, f2_mul(x1, sn2)));
+        }
+        *reinterpret_cast<uint2*>(tile + tile_off<D>(row, c) + 8 * h) = make_uint2(wa[0], wa[1]);
+        *reinterpret_cast<uint2*>(tile + tile_off<D>(row, c + NC / 2) + 8 * h) = make_uint2(wb[0], wb[1]);
+      }
+    }
+  } else {
+    const uint64_t r2 = f2_pack(r, r);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      uint2* w = reinterpret_cast<uint2*>(tile + tile_off<D>(row, c) + 8 * h);
+      const uint2 u = *w;
+      *w = make_uint2(f2_to_bf16x2(f2_mul(bf16x2_to_f2<D>(u.x), r2)), f2_to_bf16x2(f2_mul(bf16x2_to_f2<D>(u.y), r2)));
+    }
+  }
+}
+
 template <int D>
 __device__ __forceinline__ void transform_half_row_inplace(uint8_t* tile, int row, int h, int pos, RopeHalf<D>& tab,
                                                            const AttnParams& p) {
+  if constexpr (D == 128) {
+    transform_half_row_d128(tile, row, h, pos, p);
+    return;
+  }
   constexpr int NC = D / 8;  // chunks per row; this thread owns 2 words (4 elements) of each
   uint64_t x[2 * NC];        // x[2c], x[2c+1]: elements 8c + 4h + {0,1} and {2,3} as fp32 pairs
 #pragma unroll
@@ -381,6 +454,12 @@ __global__ void __launch_bounds__(640, 1)
   auto q_tile = [&](int slot, int t) { return smem + Cfg::kOffQ + (2 * slot + t) * TB; };
   auto k_tile = [&](int st) { return smem + Cfg::kOffK + st * TB; };
   auto v_tile = [&](int st) { return smem + Cfg::kOffV + st * TB; };
+  // One 128-row tile by TMA: D > 64 goes as 64-column boxes into the 16 KB sub-tiles of the layout.
+  constexpr int kBoxes = D > 64 ? D / 64 : 1;
+  auto load_tile = [&](uint8_t* dst, const CUtensorMap* map, uint64_t* full, int h, int t, int b, uint64_t pol) {
+#pragma unroll
+    for (int x = 0; x < kBoxes; ++x) tma_load_4d_hint(dst + x * kTile * 128, map, full, 64 * x, h, t, b, pol);
+  };
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -451,8 +530,8 @@ __global__ void __launch_bounds__(640, 1)
       UnitGeom g;
       g.r_out = 0;
       for (uint32_t ul = 0;; ++ul) {
-        const int slot = ul & 1;
-        const uint32_t uph = (ul >> 1) & 1;
+        const int slot = ul % Cfg::kQSlots;
+        const uint32_t uph = (ul / Cfg::kQSlots) & 1;
         if (!mbar_wait_or_abort(bar(Cfg::kBarQEmpty + slot), uph ^ 1, abort_flag)) {
           ok = false;
           break;
@@ -490,10 +569,9 @@ __global__ void __launch_bounds__(640, 1)
         const bool two = g.valid(1);
         mbar_arrive_expect_tx(bar(Cfg::kBarQFull + slot), (two ? 2 : 1) * TB);
         q_armed[slot] = static_cast<int>(uph);
-        tma_load_4d_hint(q_tile(slot, 0), &maps.q, bar(Cfg::kBarQFull + slot), 0, g.h, g.qs0, g.b, pol_stream);
+        load_tile(q_tile(slot, 0), &maps.q, bar(Cfg::kBarQFull + slot), g.h, g.qs0, g.b, pol_stream);
         if (two)
-          tma_load_4d_hint(q_tile(slot, 1), &maps.q, bar(Cfg::kBarQFull + slot), 0, g.h, g.qs0 + kTile, g.b,
-                           pol_stream);
+          load_tile(q_tile(slot, 1), &maps.q, bar(Cfg::kBarQFull + slot), g.h, g.qs0 + kTile, g.b, pol_stream);
         // key steps from ke_all down; the first r_in are already resident (no load)
         for (int i = g.r_in; i < g.n_steps(); ++i, ++kcnt) {
           const int j = g.ke_all - i;
@@ -505,9 +583,9 @@ __global__ void __launch_bounds__(640, 1)
             break;
           }
           mbar_arrive_expect_tx(bar(Cfg::kBarKFull + st), TB);
-          tma_load_4d_hint(k_tile(st), &maps.k, bar(Cfg::kBarKFull + st), 0, g.hk, j * kTile, g.b, pol_keep);
+          load_tile(k_tile(st), &maps.k, bar(Cfg::kBarKFull + st), g.hk, j * kTile, g.b, pol_keep);
           mbar_arrive_expect_tx(bar(Cfg::kBarVFull + st), TB);
-          tma_load_4d_hint(v_tile(st), &maps.v, bar(Cfg::kBarVFull + st), 0, g.hk, j * kTile, g.b, pol_keep);
+          load_tile(v_tile(st), &maps.v, bar(Cfg::kBarVFull + st), g.hk, j * kTile, g.b, pol_keep);
         }
         if (!ok) break;
       }
@@ -547,8 +625,8 @@ __global__ void __launch_bounds__(640, 1)
       bool ok = true;
       uint32_t gS = 0, kc = 0, scnt0 = 0, scnt1 = 0;
       for (uint32_t ul = 0; ok; ++ul) {
-        const int slot = ul & 1;
-        const uint32_t uph = (ul >> 1) & 1;
+        const int slot = ul % Cfg::kQSlots;
+        const uint32_t uph = (ul / Cfg::kQSlots) & 1;
         if (!mbar_wait_or_abort(bar(Cfg::kBarUnit + slot), uph, abort_flag)) { ok = false; break; }
         const int unit = unit_id[slot];
         if (unit < 0) break;
@@ -607,8 +685,8 @@ __global__ void __launch_bounds__(640, 1)
       bool ok = true;
       uint32_t gS = 0, kc = 0, pcnt = 0;
       for (uint32_t ul = 0; ok; ++ul) {
-        const int slot = ul & 1;
-        const uint32_t uph = (ul >> 1) & 1;
+        const int slot = ul % Cfg::kQSlots;
+        const uint32_t uph = (ul / Cfg::kQSlots) & 1;
         if (!mbar_wait_or_abort(bar(Cfg::kBarUnit + slot), uph, abort_flag)) { ok = false; break; }
         const int unit = unit_id[slot];
         if (unit < 0) break;
@@ -647,7 +725,9 @@ __global__ void __launch_bounds__(640, 1)
           const bool first = j == g.ke(t);  // the unit's first P.V of this tile starts O_t
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t bd = make_sdesc(va + ks * 16 * G::kRowBytes, 16, G::kSBO, G::kSwizzle);
+            // V as the MN-major B operand; for D = 128 its two 64-column sub-tiles are kBytes / 2 apart
+            const uint64_t bd = make_sdesc(va + ks * 16 * G::kRowBytes, D >= 128 ? G::kBytes / 2 : 16, G::kSBO,
+                                           G::kSwizzle);
             umma_ts(tmem + Cfg::col_o(t), pa + ks * 8, bd, idesc_o, (!first || ks > 0) ? 1u : 0u);
           }
           umma_commit(bar(Cfg::kBarBufFree + b));
@@ -669,8 +749,8 @@ __global__ void __launch_bounds__(640, 1)
     bool ok = true;
     RopeHalf<D> tab;
     for (uint32_t ul = 0; ok; ++ul) {
-      const int slot = ul & 1;
-      const uint32_t uph = (ul >> 1) & 1;
+      const int slot = ul % Cfg::kQSlots;
+      const uint32_t uph = (ul / Cfg::kQSlots) & 1;
       ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarQFull + slot), uph, abort_flag));
       if (!ok) break;
       const int unit = unit_id[slot];
@@ -718,8 +798,8 @@ __global__ void __launch_bounds__(640, 1)
     uint32_t gS = 0;  // global S-job index, counted over both query tiles (as the MMA issuer does)
     bool ok = true;
     for (uint32_t ul = 0; ok; ++ul) {
-      const int slot = ul & 1;
-      const uint32_t uph = (ul >> 1) & 1;
+      const int slot = ul % Cfg::kQSlots;
+      const uint32_t uph = (ul / Cfg::kQSlots) & 1;
       ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarUnit + slot), uph, abort_flag));
       if (!ok) break;
       const int unit = unit_id[slot];
@@ -816,7 +896,8 @@ __global__ void __launch_bounds__(640, 1)
       fence_proxy_async_smem();
       named_bar_sync(1 + t, 128);
       if (r == 0) {
-        tma_store_4d(&maps.out, stage, 0, g.h, qs, g.b);
+#pragma unroll
+        for (int x = 0; x < kBoxes; ++x) tma_store_4d(&maps.out, stage + x * kTile * 128, 64 * x, g.h, qs, g.b);
         bulk_commit_group();
         bulk_wait_group_read0();
         mbar_arrive(bar(Cfg::kBarQEmpty + slot));

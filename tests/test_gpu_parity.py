@@ -194,12 +194,12 @@ def test_destroy_and_reinit():
     assert torch.equal(o1, o2)
 
 
-def test_fast_kernel_is_used_for_d32_d64():
+def test_fast_kernel_is_used_for_every_head_dim():
     from sliding_window_attention_04_b300 import attn
 
     assert attn.attn_fwd_kernel(32) == "ws"
     assert attn.attn_fwd_kernel(64) == "ws"
-    assert attn.attn_fwd_kernel(128) == "simple"
+    assert attn.attn_fwd_kernel(128) == "ws"
 
 
 def test_many_calls_reuse_ticket_slots():
