@@ -44,7 +44,8 @@ def check_sampled(q, k, v, layer, rope_base, eps, n, seed, what):
                            return_tensors=True)
     # properties over every element: finite, and each output is a convex combination of v rows
     assert torch.isfinite(out_t).all() and torch.isfinite(lse_t).all(), what
-    vmax = v.float().abs().amax(dim=1).cuda()  # [B, H, D] max over positions
+    vmax = v.float().abs().amax(dim=1).cuda()  # [B, H_kv, D] max over positions
+    vmax = vmax.repeat_interleave(H // v.shape[2], dim=1)  # query head h reads K/V head h // (H // H_kv)
     assert (out_t.float().abs() <= vmax[:, None] * (1 + 2 ** -7) + 1e-6).all(), what
     rows = sample_rows(B, H, T, layer.window, n, seed)
     ref, lref = oracle.attn_rows(q, k, v, rows, window=layer.window, causal=layer.causal, rope_base=rope_base,
@@ -83,3 +84,25 @@ def test_sweep_sampled(T):
     for li, layer in enumerate(w.layers):
         q, k, v = make_qkv(w.B, w.T, w.H, w.D, seed=layer_seed(w.index, 10 * li + T // 1024))
         check_sampled(q, k, v, layer, w.rope_base, w.eps, 300, T + li, f"{w.name} layer {li}")
+
+
+@pytest.mark.parametrize("window", [1024, 2048])
+def test_autoresearch_d128_shape_sampled(window):
+    """The autoresearch default attention shape (habr "Autoresearch" deep dive, train.py listing:
+    head_dim 128, sequence_len 2048; NEXT-2): B = 128, H = 4, T = 2048, D = 128, one S layer
+    (W = T/2) and one full-causal layer, sampled rows against the oracle. This size runs many
+    units per CTA through the D = 128 configuration's single Q slot."""
+    from types import SimpleNamespace
+
+    q, k, v = make_qkv(128, 2048, 4, 128, seed=7000 + window)
+    layer = SimpleNamespace(window=window, causal=True)
+    check_sampled(q, k, v, layer, 10000.0, 1e-6, 300, 7100 + window, f"autoresearch D128 w={window}")
+
+
+def test_gqa_shape_sampled():
+    """Grouped K/V heads at a multi-wave size (H = 12 query heads over 4 K/V heads, D = 64)."""
+    from types import SimpleNamespace
+
+    q, _, _ = make_qkv(16, 1024, 12, 64, seed=7300)
+    _, k, v = make_qkv(16, 1024, 4, 64, seed=7301)
+    check_sampled(q, k, v, SimpleNamespace(window=512, causal=True), 10000.0, 1e-6, 300, 7302, "gqa 12/4")
