@@ -157,6 +157,21 @@ def config_dict(w):
             "parallelism": "replicas (one full workload per GPU)"}
 
 
+def max_over_ranks(values, dist=None, device=None):
+    """Per-rank timings -> their maximum over all ranks (the slowest rank sets the job's time)."""
+    if dist is None:
+        return [float(x) for x in values]
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_tflops(flops_per_rank_step, steps, world, elapsed_ms):
+    """Whole-job throughput: every rank runs its own replica (weak scaling), so the job does world
+    times the work of one rank in the max-over-ranks time."""
+    return flops_per_rank_step * steps * world / (elapsed_ms / 1e3) / 1e12
+
+
 def run_reference(args, w, rank):
     """The reference arm: the float64 oracle on the host cores, a bounded sample per step."""
     import oracle
@@ -285,13 +300,10 @@ def main():
     st = attn.attn_device_status()
     if st != 0:
         raise SystemExit(f"device status after the timed region: {attn.status_string(st)}")
-    if dist:
-        t = torch.tensor([elapsed_ms, kernel_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms, kernel_ms = float(t[0]), float(t[1])
+    elapsed_ms, kernel_ms = max_over_ranks([elapsed_ms, kernel_ms], dist, device)
 
     n_launch = args.steps * len(w.layers)
-    value = step_flops * args.steps * world / (elapsed_ms / 1e3) / 1e12
+    value = whole_job_tflops(step_flops, args.steps, world, elapsed_ms)
     achieved = step_flops * args.steps / (kernel_ms / 1e3) / 1e12  # per GPU, kernel time only
     peak, peak_sustained, peak_kind = peaks()
 
@@ -321,12 +333,10 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize(device)
     e2e_ms = e0.elapsed_time(e1)
+    (e2e_ms,) = max_over_ranks([e2e_ms], dist, device)
     if dist:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
         dist.barrier()
-    e2e_value = step_flops * args.e2e_steps * world / (e2e_ms / 1e3) / 1e12
+    e2e_value = whole_job_tflops(step_flops, args.e2e_steps, world, e2e_ms)
     h2d = sum(t.numel() * t.element_size() for hl in host for t in hl)
     d2h = sum(t.numel() * t.element_size() for t in h_out + h_lse)
 
