@@ -17,8 +17,9 @@
 //   17     S issuer (lane 0): S = Q^ K^^T jobs in stream order; TMEM owner
 //   18, 19 P.V issuers of query tiles 0 and 1 (lane 0): O_t += P V in order
 //
-// TMEM (512 columns): three rotating 128-column S/P buffers and O_0, O_1 (D columns each). The
-// S jobs (one per query tile and key tile, in stream order) take the buffers round-robin.
+// TMEM (512 columns): kSBufs rotating 128-column S/P buffers (three; two at D = 128) and O_0, O_1
+// (D columns each). The S jobs (one per query tile and key tile, in stream order) take the buffers
+// round-robin.
 // Every wait on a phase-parity barrier is exact: the waiter is never two phases away from the
 // barrier. S-done and S-seen are per query tile (the next S of a tile is issued only after its
 // softmax has seen the previous one). P-written and P.V-done have two slots per tile, used by the
