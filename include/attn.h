@@ -74,8 +74,8 @@ int attn_init(int device);
  * that pair, builds the cos/sin table on the device (a cudaMalloc and a synchronous copy);
  * every later call allocates nothing and does not synchronise the host.
  *
- * The persistent kernel (D = 32, 64) hands out work through a pair of device counters owned by
- * the library; each call takes the next of 256 such pairs, and the kernel resets its pair when
+ * The persistent kernel (D = 32, 64, 128) hands out work through a pair of device counters owned
+ * by the library; each call takes the next of 256 such pairs, and the kernel resets its pair when
  * it finishes. Calls issued one after another on a stream can therefore be repeated without
  * limit, and up to 256 calls may run at the same time on different streams.
  */
