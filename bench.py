@@ -228,12 +228,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers of the workload (profiling captures); 0 = all")
+    ap.add_argument("--workload", default="",
+                    help="another workload by name prefix (extra measurements and captures; the bench "
+                         "line is the ANDREA-120M workload)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    w = configs.workloads()[WORKLOAD_INDEX]
+    w = configs.by_name(args.workload) if args.workload else configs.workloads()[WORKLOAD_INDEX]
     if args.layers > 0:
         import dataclasses
 

@@ -116,8 +116,16 @@ def sweep_workloads() -> List[Workload]:
     return out
 
 
+def extra_workloads() -> List[Workload]:
+    """Shapes beyond the five workloads, for extra measurements: the autoresearch default attention
+    shape (habr "Autoresearch" deep dive, train.py listing: sequence_len 2048, head_dim 128; 4 heads
+    per layer at the default depth, B = 128), one S layer (W = T/2) and one L layer."""
+    return [Workload("autoresearch default shape B128 H4 T2048 D128", 5, 128, 4, 2048, 128,
+                     (Layer(1024, True), Layer(2048, True)))]
+
+
 def by_name(prefix: str) -> Workload:
-    for w in workloads() + sweep_workloads():
+    for w in workloads() + sweep_workloads() + extra_workloads():
         if w.name.startswith(prefix):
             return w
     raise KeyError(prefix)
