@@ -164,13 +164,18 @@ int launch_ws(const swa::AttnParams& p, PFN_cuTensorMapEncodeTiled_v12000 encode
       encode_tile_map(encode, &maps.v, p.v, p.B, p.Hkv, p.T, D) != CUDA_SUCCESS ||
       encode_tile_map(encode, &maps.out, p.out, p.B, p.H, p.T, D) != CUDA_SUCCESS)
     return ATTN_ERR_CUDA;
-  // work is handed out in chunks of two 256-row query blocks of one head (see the kernel)
+  // work is handed out in chunks of two 256-row query blocks of one head (see the kernel), heads in
+  // groups whose K and V fit in half of L2 together, so a group's blocks share them there
   const long long n_qb = (p.T + 2 * swa::kTile - 1) / (2 * swa::kTile);
+  swa::AttnParams pk = p;
+  const long long kv_head_bytes = 2LL * p.T * D * 2 / p.kv_group;  // K + V per query head (a group shares them)
+  const long long hg = (64LL << 20) / kv_head_bytes;
+  pk.head_group = static_cast<int>(hg < 1 ? 1 : (hg > (1 << 20) ? (1 << 20) : hg));
   const long long chunks = static_cast<long long>(p.B) * p.H * ((n_qb + 1) / 2);
   if (chunks >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
   const int grid = static_cast<int>(chunks < sm_count ? chunks : sm_count);
   swa::attn_fwd_ws_kernel<D><<<grid, swa::WsCfg<D>::kThreads, swa::WsCfg<D>::kSmemBytes, stream>>>(
-      p, maps, sched, static_cast<int>(chunks));
+      pk, maps, sched, static_cast<int>(chunks));
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

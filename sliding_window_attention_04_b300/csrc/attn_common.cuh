@@ -31,6 +31,7 @@ struct AttnParams {
   float eps;
   float scale_log2;        // log2(e) / sqrt(D)
   int n_qtiles;            // ceil(T / 128)
+  int head_group;          // persistent kernel: heads per ticket group (their K/V fit in L2 together)
 };
 
 // Byte offset of 16-byte chunk `chunk` (8 bf16 along D) of row `row` inside a 128-row operand

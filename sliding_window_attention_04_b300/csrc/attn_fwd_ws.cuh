@@ -541,8 +541,14 @@ __global__ void __launch_bounds__(640, 1)
         if (c_left == 0) {
           const int c = atomicAdd(sched, 1);
           if (c < n_chunks) {
-            const int rank = c / n_bh;
-            c_bh = c - rank * n_bh;
+            // groups of head_group heads in turn; inside a group the heaviest pair of every head
+            // first, then the next pair of every head, ...
+            const int cpb = (n_qb + 1) / 2;  // pairs per head
+            const int grp = c / (p.head_group * cpb);
+            const int rem = c - grp * p.head_group * cpb;
+            const int gsize = min(p.head_group, n_bh - grp * p.head_group);
+            const int rank = rem / gsize;
+            c_bh = grp * p.head_group + (rem - rank * gsize);
             c_qb = n_qb - 1 - 2 * rank;
             c_left = c_qb >= 1 ? 2 : 1;
           }

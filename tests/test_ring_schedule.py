@@ -47,14 +47,23 @@ def shared_steps(a, nb):
     return R if (1 <= R <= S and R <= a["n"] and R <= nb["n"]) else 0
 
 
-def cta_units(B, H, T, window, causal, tickets):
+def ticket_decode(c, n_bh, n_qb, head_group):
+    """Ticket c -> (head, highest query block of its pair): groups of head_group heads in turn, inside a
+    group the heaviest pair of every head first (the producer's decode in attn_fwd_ws.cuh)."""
+    cpb = (n_qb + 1) // 2
+    grp, rem = divmod(c, head_group * cpb)
+    gsize = min(head_group, n_bh - grp * head_group)
+    rank, i = divmod(rem, gsize)
+    return grp * head_group + i, n_qb - 1 - 2 * rank
+
+
+def cta_units(B, H, T, window, causal, tickets, head_group=1 << 20):
     """The units one CTA runs for the given tickets, with r_in / r_out as the producer sets them."""
     n_qb = (T + 2 * KT - 1) // (2 * KT)
     n_bh = B * H
     units = []
     for c in tickets:
-        rank, bh = divmod(c, n_bh)
-        qb = n_qb - 1 - 2 * rank
+        bh, qb = ticket_decode(c, n_bh, n_qb, head_group)
         left, r_prev = (2 if qb >= 1 else 1), 0
         while left:
             g = unit_geom(T, window, causal, bh, qb)
@@ -106,7 +115,20 @@ def test_ring_positions_releases_and_order(B, H, T):
                 per.setdefault(rnd.randrange(3), []).append(c)
             parts += list(per.values())
         for tickets in parts:
-            check_ring(cta_units(B, H, T, window, causal, tickets))
+            for head_group in (1, 2, 5, 1 << 20):
+                check_ring(cta_units(B, H, T, window, causal, tickets, head_group))
+
+
+@pytest.mark.parametrize("n_bh,n_qb,head_group", [(384, 4, 256), (512, 8, 64), (192, 4, 512), (7, 3, 2),
+                                                  (5, 1, 3), (6, 5, 4)])
+def test_tickets_cover_every_pair_once_heaviest_first_in_a_group(n_bh, n_qb, head_group):
+    n_tickets = n_bh * ((n_qb + 1) // 2)
+    seen = [ticket_decode(c, n_bh, n_qb, head_group) for c in range(n_tickets)]
+    assert sorted(seen) == sorted((bh, n_qb - 1 - 2 * r) for bh in range(n_bh) for r in range((n_qb + 1) // 2))
+    for c in range(1, n_tickets):  # inside a group the pairs come heaviest (highest query block) first
+        (b0, q0), (b1, q1) = seen[c - 1], seen[c]
+        if b0 // head_group == b1 // head_group:
+            assert q1 <= q0
 
 
 def test_reuse_on_the_120m_shape():
