@@ -31,9 +31,9 @@
 // two sit in different buffers); only the O rescale and the epilogue wait for that P.V. A
 // softmax warpgroup reads S from its buffer and writes P (bf16, 64 columns) into the buffer's upper
 // half once that half has been read, so P needs no space of its own; the P.V MMA reads P from
-// there, and its completion frees the buffer for the S job three places later. With three
-// buffers for two query tiles the S of a tile's next key tile is normally computed while its
-// softmax still works on the current one.
+// there, and its completion frees the buffer for the S job kSBufs places later. With three
+// buffers for two query tiles (D <= 64) the S of a tile's next key tile is normally computed while
+// its softmax still works on the current one.
 //
 // Three single-thread MMA issuers each run a plain in-order loop of blocking waits: the S issuer
 // (S jobs in stream order) and one P.V issuer per query tile, which wakes as soon as its tile's P
@@ -45,7 +45,7 @@
 // by element; tiles without any masked entry skip the mask tests. The running max is updated lazily:
 // O and l are rescaled only when the tile max exceeds the current reference by more than
 // kRescaleLog2. At the end of a unit the softmax warps normalise O_t, stage it as bf16 in the (now
-// free) Q tile buffer, store it with one TMA store, and write the per-row log-sum-exp.
+// free) Q tile buffer, store it by TMA (one box; two at D = 128), and write the per-row log-sum-exp.
 //
 // Registers: the kernel is compiled to 96 per thread (640 x 96 = 61440); at start the warpgroups
 // re-divide them with setmaxnreg: softmax 128, prologue 80, producer/MMA group 64, i.e.
