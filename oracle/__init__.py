@@ -162,4 +162,39 @@ def attn_probs(q, k, v, b: int, h: int, window: int = -1, causal: bool = True, r
     return p
 
 
-__all__ = ["attn_fwd", "attn_rows", "attn_probs", "qk_prologue", "round_bf16", "num_threads"]
+def _bf16_values(x) -> np.ndarray:
+    """bf16 tensor / uint16 bit patterns -> their values as float64 (exact)."""
+    return (_bits(x).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def value_gate(v, ve, x_gate, w_gate) -> np.ndarray:
+    """Value-embedding gate (habr "Autoresearch" deep dive, train.py listing, CausalSelfAttention.forward,
+    "Value Residual (ResFormer)"): for every (b, t, K/V head h)
+        gate = 2 * sigmoid(sum_c x_gate[b, t, c] * w_gate[h, c])      (c < 32 channels)
+        v'   = v + gate * ve
+    with each step rounded to bf16 as the listing's bf16 tensors are: the logit (the exact sum of the
+    exact products, rounded once), the sigmoid (rounded once), x2 (exact), the product with ve
+    (rounded), the sum with v (rounded). Everything else is float64.
+
+    v, ve: [B, T, Hkv, D]; x_gate: [B, T, C]; w_gate: [Hkv, C] (bf16 tensors or uint16 bit patterns).
+    Returns float64 [B, T, Hkv, D] holding bf16 values (the gated v the attention then reads)."""
+    import math
+
+    vv, ee = _bf16_values(v), _bf16_values(ve)
+    xx, ww = _bf16_values(x_gate), _bf16_values(w_gate)
+    B, T, Hkv, D = vv.shape
+    assert ee.shape == vv.shape and xx.shape[:2] == (B, T) and ww.shape == (Hkv, xx.shape[2])
+    logit = np.empty((B, T, Hkv))
+    for b in range(B):
+        for t in range(T):
+            for h in range(Hkv):
+                # products of two bf16 values are exact in float64; fsum adds them with one rounding
+                logit[b, t, h] = math.fsum(float(a) * float(w) for a, w in zip(xx[b, t], ww[h]))
+    logit = round_bf16(logit)
+    sig = round_bf16(1.0 / (1.0 + np.exp(-logit)))
+    gate = 2.0 * sig
+    prod = round_bf16(gate[..., None] * ee)
+    return round_bf16(vv + prod)
+
+
+__all__ = ["attn_fwd", "attn_rows", "attn_probs", "qk_prologue", "round_bf16", "num_threads", "value_gate"]

@@ -414,3 +414,51 @@ def test_f32_rounding_agrees_with_f64_except_near_ties():
         a, b = np.minimum(y32[diff], y64[diff]), np.maximum(y32[diff], y64[diff])
         assert ((a <= mid) & (mid <= b)).all()
     assert diff.mean() < 1e-3
+
+
+# ---------------------------------------------------------------------------------------------
+# Value-embedding gate (NEXT-3; habr "Autoresearch" deep dive, train.py listing,
+# CausalSelfAttention.forward, "Value Residual (ResFormer)"): v' = v + 2 sigmoid(x[..., :32] W^T) ve.
+
+
+def _gate_inputs(seed, B=2, T=5, Hkv=3, D=8, C=32, w_scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    bf = lambda *s, scale=1.0: (torch.randn(*s, generator=g) * scale).to(torch.bfloat16)
+    return bf(B, T, Hkv, D), bf(B, T, Hkv, D), bf(B, T, C), bf(Hkv, C, scale=w_scale)
+
+
+def test_value_gate_closed_forms():
+    v, ve, x, w = _gate_inputs(1)
+    vv, ee = f64(v), f64(ve)
+    # zero gate weights: gate = 2 sigmoid(0) = 1 exactly, so v' = bf16(v + ve)
+    got = oracle.value_gate(v, ve, x, torch.zeros_like(w))
+    assert np.array_equal(got, oracle.round_bf16(vv + ee))
+    # ve = 0 leaves v unchanged
+    assert np.array_equal(oracle.value_gate(v, torch.zeros_like(ve), x, w), vv)
+    # saturated logits: sum 32 * 4 = 128 -> sigmoid rounds to 1 (gate 2); -128 -> gate about 2e-56
+    ones = torch.ones_like(x)
+    got = oracle.value_gate(v, ve, ones, torch.full_like(w, 4.0))
+    assert np.array_equal(got, oracle.round_bf16(vv + 2.0 * ee))
+    got = oracle.value_gate(v, ve, ones, torch.full_like(w, -4.0))
+    assert np.array_equal(got, vv)
+
+
+def test_value_gate_matches_torch_bf16_evaluation():
+    """The same expression evaluated by PyTorch on bf16 CPU tensors (each op rounds its result to
+    bf16; the linear layer accumulates in fp32). The two agree wherever their gate logits agree;
+    the logits differ by at most one bf16 step where fp32 accumulation rounds a near-tie the
+    other way."""
+    import torch.nn.functional as F
+
+    v, ve, x, w = _gate_inputs(2, B=4, T=16, Hkv=4, D=16)
+    got = oracle.value_gate(v, ve, x, w)
+    logit_t = F.linear(x, w)  # bf16 [B, T, Hkv]
+    gate_t = 2 * torch.sigmoid(logit_t)
+    ref = (v + gate_t.unsqueeze(-1) * ve).to(torch.float64).numpy()
+    xx, ww = f64(x), f64(w)
+    logit_o = oracle.round_bf16(np.einsum("btc,hc->bth", xx, ww))
+    same = logit_o == logit_t.to(torch.float64).numpy()
+    assert same.mean() > 0.98
+    step = np.abs(logit_o - logit_t.to(torch.float64).numpy())[~same]
+    assert (step <= np.abs(logit_o[~same]) * 2.0 ** -7 + 1e-30).all()  # one bf16 step at most
+    np.testing.assert_array_equal(got[same], ref[same])
