@@ -382,7 +382,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
     }
   }
 
-  swa::AttnParams p;
+  swa::AttnParams p{};  // every field set below or zero
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);
   p.v = static_cast<const __nv_bfloat16*>(v);
@@ -546,7 +546,7 @@ int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, flo
   noalloc_prepare_kernel<<<prep_blocks, 256, 0, st>>>(scratch, T, D, rope_base);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
 
-  swa::AttnParams p;
+  swa::AttnParams p{};  // every field set below or zero
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);
   p.v = static_cast<const __nv_bfloat16*>(v);
