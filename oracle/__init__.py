@@ -197,4 +197,7 @@ def value_gate(v, ve, x_gate, w_gate) -> np.ndarray:
     return round_bf16(vv + prod)
 
 
-__all__ = ["attn_fwd", "attn_rows", "attn_probs", "qk_prologue", "round_bf16", "num_threads", "value_gate"]
+from .attn_backward import attn_bwd, attn_fwd_f64  # noqa: E402  (backward oracle, NEXT-1)
+
+__all__ = ["attn_fwd", "attn_rows", "attn_probs", "qk_prologue", "round_bf16", "num_threads", "value_gate",
+           "attn_bwd", "attn_fwd_f64"]
