@@ -16,8 +16,11 @@ fixed sequence of correctly rounded single-precision operations as the CUDA kern
 in attn_oracle.c), "f64" evaluates it in double. Everything after the rounding (scores, mask,
 softmax, weighted sum) is float64 in both modes.
 
-Parity status: every function here is pinned by `tests/test_oracle_pins.py` (worked example,
-closed forms, invariants, library special cases, pure-Python brute force for T <= 8).
+Parity status: every function here is pinned: the forward and its helpers, the grouped K/V heads
+and the value-embedding gate by `tests/test_oracle_pins.py` (worked example, closed forms,
+invariants, library special cases, pure-Python brute force for T <= 8); the backward
+(`attn_backward.py`) by `tests/test_oracle_backward.py` (finite differences, autograd); the Polar
+Express orthogonalisation (`polar_express.py`) by `tests/test_oracle_polar.py` (SVD).
 """
 from __future__ import annotations
 
