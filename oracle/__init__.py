@@ -10,11 +10,12 @@ bf16 bit patterns: q in [B, T, H, D] layout, k and v in [B, T, Hkv, D] with H a 
 (grouped K/V heads: query head h uses K/V head h // (H // Hkv); Hkv = H is multi-head attention),
 and returns float64 numpy arrays.
 
-`qk_precision` selects how the QK-norm + RoPE prologue is evaluated before q^ and k^ are
-rounded to bf16: "f32" (default, used for parity) takes that quantisation decision with the same
-fixed sequence of correctly rounded single-precision operations as the CUDA kernel (spelled out
-in attn_oracle.c), "f64" evaluates it in double. Everything after the rounding (scores, mask,
-softmax, weighted sum) is float64 in both modes.
+The prologue (RoPE, QK-norm) is evaluated in float64 in the listing's order and then rounded
+to bf16. Where an exact value lies so close to a bf16 rounding midpoint that a single-precision
+evaluation may round it the other way, both roundings are correct; `qk_prologue(...,
+return_amb=True)` reports each element's ambiguity radius, and `attn_fwd` / `attn_rows` with
+`return_slack=True` report how far those choices can move each output element and each LSE
+(attn_oracle.c, steps 3 and 6). Everything after the rounding is float64.
 
 Parity status: every function here is pinned: the forward and its helpers, the grouped K/V heads
 and the value-embedding gate by `tests/test_oracle_pins.py` (worked example, closed forms,
@@ -43,12 +44,12 @@ def _load():
         f64p = ctypes.POINTER(ctypes.c_double)
         i32p = ctypes.POINTER(ctypes.c_int32)
         ci, cd, cl = ctypes.c_int, ctypes.c_double, ctypes.c_long
-        lib.oracle_attn_fwd.argtypes = [u16p, u16p, u16p, f64p, f64p, ci, ci, ci, ci, ci, ci, ci, cd, cd, ci, ci, ci]
-        lib.oracle_attn_rows.argtypes = [u16p, u16p, u16p, i32p, cl, f64p, f64p, ci, ci, ci, ci, ci, ci, ci,
-                                         cd, cd, ci, ci, ci]
-        lib.oracle_attn_probs.argtypes = [u16p, u16p, u16p, ci, ci, f64p, ci, ci, ci, ci, ci, ci, ci, cd, cd, ci,
-                                          ci]
-        lib.oracle_qk_prologue.argtypes = [u16p, f64p, ci, ci, ci, ci, cd, cd, ci, ci, ci]
+        lib.oracle_attn_fwd.argtypes = [u16p, u16p, u16p, f64p, f64p, f64p, f64p, ci, ci, ci, ci, ci, ci, ci, cd,
+                                        cd, ci, cd, ci]
+        lib.oracle_attn_rows.argtypes = [u16p, u16p, u16p, i32p, cl, f64p, f64p, f64p, f64p, ci, ci, ci, ci, ci,
+                                         ci, ci, cd, cd, ci, cd, ci]
+        lib.oracle_attn_probs.argtypes = [u16p, u16p, u16p, ci, ci, f64p, ci, ci, ci, ci, ci, ci, ci, cd, cd, ci]
+        lib.oracle_qk_prologue.argtypes = [u16p, f64p, f64p, ci, ci, ci, ci, cd, cd, ci, cd, ci]
         lib.oracle_round_bf16.argtypes = [cd]
         lib.oracle_round_bf16.restype = cd
         lib.oracle_num_threads.restype = ci
@@ -73,15 +74,6 @@ def _p(a, ct):
     return a.ctypes.data_as(ctypes.POINTER(ct))
 
 
-_PREC = {"f64": 0, "f32": 1}
-
-
-def _prec(p: str) -> int:
-    if p not in _PREC:
-        raise ValueError(f"qk_precision must be 'f32' or 'f64', not {p!r}")
-    return _PREC[p]
-
-
 def _check(rc: int):
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (code {rc})")
@@ -99,15 +91,19 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
 
 
 def qk_prologue(x, rope_base: float = 10000.0, eps: float = 1e-6, round_qk: bool = True,
-                nthreads: int = 0, qk_precision: str = "f32") -> np.ndarray:
-    """RoPE then RMSNorm of every [.., D] row of x ([B, T, H, D]); float64 [B, T, H, D]."""
+                nthreads: int = 0, return_amb: bool = False, amb_scale: float = 1.0):
+    """RoPE then RMSNorm of every [.., D] row of x ([B, T, H, D]), rounded to bf16; float64
+    [B, T, H, D]. With return_amb, also the ambiguity radius of every element (attn_oracle.c,
+    step 3; amb_scale multiplies the evaluation budget, 1 for the stated one)."""
     xb = _bits(x)
     B, T, H, D = xb.shape
     y = np.empty((B, T, H, D), dtype=np.float64)
-    _check(_load().oracle_qk_prologue(_p(xb, ctypes.c_uint16), _p(y, ctypes.c_double), B, T, H, D,
-                                      float(rope_base), float(eps), int(round_qk), _prec(qk_precision),
+    amb = np.empty((B, T, H, D), dtype=np.float64) if return_amb else None
+    _check(_load().oracle_qk_prologue(_p(xb, ctypes.c_uint16), _p(y, ctypes.c_double),
+                                      _p(amb, ctypes.c_double) if return_amb else None, B, T, H, D,
+                                      float(rope_base), float(eps), int(round_qk), float(amb_scale),
                                       int(nthreads)))
-    return y
+    return (y, amb) if return_amb else y
 
 
 def _kv_heads(qb, kb, vb) -> int:
@@ -119,24 +115,34 @@ def _kv_heads(qb, kb, vb) -> int:
 
 
 def attn_fwd(q, k, v, window: int = -1, causal: bool = True, rope_base: float = 10000.0,
-             eps: float = 1e-6, round_qk: bool = True, nthreads: int = 0, qk_precision: str = "f32"):
-    """Full forward. Returns (out float64 [B, T, H, D], lse float64 [B, H, T], natural log)."""
+             eps: float = 1e-6, round_qk: bool = True, nthreads: int = 0, return_slack: bool = False,
+             amb_scale: float = 1.0):
+    """Full forward. Returns (out float64 [B, T, H, D], lse float64 [B, H, T], natural log), and
+    with return_slack also (out_slack [B, T, H, D], lse_slack [B, H, T]): how far the near-tie
+    choices of q^, k^ can move each value (attn_oracle.c, step 6; amb_scale widens step 3's budget
+    for tests)."""
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     B, T, H, D = qb.shape
     Hkv = _kv_heads(qb, kb, vb)
     out = np.empty((B, T, H, D), dtype=np.float64)
     lse = np.empty((B, H, T), dtype=np.float64)
+    os_ = np.empty((B, T, H, D), dtype=np.float64) if return_slack else None
+    ls_ = np.empty((B, H, T), dtype=np.float64) if return_slack else None
     _check(_load().oracle_attn_fwd(_p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
-                                   _p(out, ctypes.c_double), _p(lse, ctypes.c_double), B, H, Hkv, T, D,
+                                   _p(out, ctypes.c_double), _p(lse, ctypes.c_double),
+                                   _p(os_, ctypes.c_double) if return_slack else None,
+                                   _p(ls_, ctypes.c_double) if return_slack else None, B, H, Hkv, T, D,
                                    int(window), int(bool(causal)), float(rope_base), float(eps),
-                                   int(round_qk), _prec(qk_precision), int(nthreads)))
-    return out, lse
+                                   int(round_qk), float(amb_scale), int(nthreads)))
+    return (out, lse, os_, ls_) if return_slack else (out, lse)
 
 
 def attn_rows(q, k, v, rows, window: int = -1, causal: bool = True, rope_base: float = 10000.0,
-              eps: float = 1e-6, round_qk: bool = True, nthreads: int = 0, qk_precision: str = "f32"):
+              eps: float = 1e-6, round_qk: bool = True, nthreads: int = 0, return_slack: bool = False,
+              amb_scale: float = 1.0):
     """Selected query rows only. rows: int array [n, 3] of (b, h, i).
-    Returns (out float64 [n, D], lse float64 [n])."""
+    Returns (out float64 [n, D], lse float64 [n]), and with return_slack also
+    (out_slack [n, D], lse_slack [n])."""
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     B, T, H, D = qb.shape
     Hkv = _kv_heads(qb, kb, vb)
@@ -144,15 +150,19 @@ def attn_rows(q, k, v, rows, window: int = -1, causal: bool = True, rope_base: f
     n = r.shape[0]
     out = np.empty((n, D), dtype=np.float64)
     lse = np.empty((n,), dtype=np.float64)
+    os_ = np.empty((n, D), dtype=np.float64) if return_slack else None
+    ls_ = np.empty((n,), dtype=np.float64) if return_slack else None
     _check(_load().oracle_attn_rows(_p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
                                     _p(r, ctypes.c_int32), n, _p(out, ctypes.c_double), _p(lse, ctypes.c_double),
+                                    _p(os_, ctypes.c_double) if return_slack else None,
+                                    _p(ls_, ctypes.c_double) if return_slack else None,
                                     B, H, Hkv, T, D, int(window), int(bool(causal)), float(rope_base), float(eps),
-                                    int(round_qk), _prec(qk_precision), int(nthreads)))
-    return out, lse
+                                    int(round_qk), float(amb_scale), int(nthreads)))
+    return (out, lse, os_, ls_) if return_slack else (out, lse)
 
 
 def attn_probs(q, k, v, b: int, h: int, window: int = -1, causal: bool = True, rope_base: float = 10000.0,
-               eps: float = 1e-6, round_qk: bool = True, qk_precision: str = "f32") -> np.ndarray:
+               eps: float = 1e-6, round_qk: bool = True) -> np.ndarray:
     """The attention weight matrix p [T, T] (queries x keys) of head (b, h)."""
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     B, T, H, D = qb.shape
@@ -160,8 +170,7 @@ def attn_probs(q, k, v, b: int, h: int, window: int = -1, causal: bool = True, r
     p = np.empty((T, T), dtype=np.float64)
     _check(_load().oracle_attn_probs(_p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
                                      int(b), int(h), _p(p, ctypes.c_double), B, H, Hkv, T, D, int(window),
-                                     int(bool(causal)), float(rope_base), float(eps), int(round_qk),
-                                     _prec(qk_precision)))
+                                     int(bool(causal)), float(rope_base), float(eps), int(round_qk)))
     return p
 
 

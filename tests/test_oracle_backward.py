@@ -33,8 +33,7 @@ def _inputs(B, T, H, Hkv, D, seed):
 def test_f64_forward_matches_c_oracle(B, T, H, Hkv, D, window, causal, base, eps):
     q, k, v = _inputs(B, T, H, Hkv, D, 300 + T)
     out, lse = ob.attn_fwd_f64(q, k, v, window, causal, base, eps)
-    ref, lref = oracle.attn_fwd(q, k, v, window=window, causal=causal, rope_base=base, eps=eps, round_qk=False,
-                                qk_precision="f64")
+    ref, lref = oracle.attn_fwd(q, k, v, window=window, causal=causal, rope_base=base, eps=eps, round_qk=False)
     np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
     np.testing.assert_allclose(lse, lref, rtol=0, atol=1e-12)
 

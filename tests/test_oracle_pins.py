@@ -173,54 +173,49 @@ def test_zero_query_counts_large():
 
 def test_rmsnorm_values():
     x = bf16(np.array([3.0, 4.0]).reshape(1, 1, 1, 2))
-    y = oracle.qk_prologue(x, rope_base=0.0, eps=0.0, round_qk=False, qk_precision="f64")
+    y = oracle.qk_prologue(x, rope_base=0.0, eps=0.0, round_qk=False)
     np.testing.assert_allclose(y.ravel(), [3 / math.sqrt(12.5), 4 / math.sqrt(12.5)], rtol=1e-15)
-    y = oracle.qk_prologue(x, rope_base=0.0, eps=0.0, round_qk=False, qk_precision="f32")
-    np.testing.assert_allclose(y.ravel(), [3 / math.sqrt(12.5), 4 / math.sqrt(12.5)], rtol=2e-7)
     ones = bf16(np.ones((1, 1, 1, 8)))
-    for prec, tol in (("f64", 1e-15), ("f32", 2e-7)):
-        y = oracle.qk_prologue(ones, rope_base=0.0, eps=0.25, round_qk=False, qk_precision=prec)
-        np.testing.assert_allclose(y.ravel(), 1 / math.sqrt(1.25), rtol=tol)
+    y = oracle.qk_prologue(ones, rope_base=0.0, eps=0.25, round_qk=False)
+    np.testing.assert_allclose(y.ravel(), 1 / math.sqrt(1.25), rtol=1e-15)
 
 
 def test_rmsnorm_identities():
     B, T, H, D = 2, 5, 3, 32
     x, _, _ = make_qkv(B, T, H, D, seed=21)
     eps = 0.3
-    y = oracle.qk_prologue(x, rope_base=0.0, eps=eps, round_qk=False, qk_precision="f64")
+    y = oracle.qk_prologue(x, rope_base=0.0, eps=eps, round_qk=False)
     xx = f64(x)
     ms = (xx ** 2).mean(-1)
     np.testing.assert_allclose((y ** 2).sum(-1), D * ms / (ms + eps), rtol=1e-13)
     # scale invariance with eps = 0 (2x is exact in bf16)
-    for prec in ("f64", "f32"):
-        y1 = oracle.qk_prologue(x, rope_base=0.0, eps=0.0, round_qk=False, qk_precision=prec)
-        y2 = oracle.qk_prologue((x.float() * 2).to(torch.bfloat16), rope_base=0.0, eps=0.0, round_qk=False,
-                                qk_precision=prec)
-        assert np.array_equal(y1, y2)
+    y1 = oracle.qk_prologue(x, rope_base=0.0, eps=0.0, round_qk=False)
+    y2 = oracle.qk_prologue((x.float() * 2).to(torch.bfloat16), rope_base=0.0, eps=0.0, round_qk=False)
+    assert np.array_equal(y1, y2)
 
 
 def test_rope_literal_values():
     """D = 4, base 10000: pair 0 is (x0, x2) at angle t, pair 1 is (x1, x3) at angle t/100."""
-    for prec, tol in (("f64", 1e-15), ("f32", 1e-7)):
-        def rot(vec, t):
-            x = np.zeros((1, t + 1, 1, 4))
-            x[0, t, 0] = vec
-            return oracle.qk_prologue(bf16(x), rope_base=10000.0, eps=-1.0, round_qk=False,
-                                      qk_precision=prec)[0, t, 0]
+    tol = 1e-15
 
-        np.testing.assert_allclose(rot([1, 0, 0, 0], 1), [math.cos(1), 0, -math.sin(1), 0], atol=tol)
-        np.testing.assert_allclose(rot([0, 0, 1, 0], 1), [math.sin(1), 0, math.cos(1), 0], atol=tol)
-        np.testing.assert_allclose(rot([0, 1, 0, 0], 1), [0, math.cos(0.01), 0, -math.sin(0.01)], atol=tol)
-        np.testing.assert_allclose(rot([0, 0, 0, 1], 3), [0, math.sin(0.03), 0, math.cos(0.03)], atol=tol)
-        np.testing.assert_allclose(rot([0.5, -2, 1, 3], 0), [0.5, -2, 1, 3], atol=0)
+    def rot(vec, t):
+        x = np.zeros((1, t + 1, 1, 4))
+        x[0, t, 0] = vec
+        return oracle.qk_prologue(bf16(x), rope_base=10000.0, eps=-1.0, round_qk=False)[0, t, 0]
+
+    np.testing.assert_allclose(rot([1, 0, 0, 0], 1), [math.cos(1), 0, -math.sin(1), 0], atol=tol)
+    np.testing.assert_allclose(rot([0, 0, 1, 0], 1), [math.sin(1), 0, math.cos(1), 0], atol=tol)
+    np.testing.assert_allclose(rot([0, 1, 0, 0], 1), [0, math.cos(0.01), 0, -math.sin(0.01)], atol=tol)
+    np.testing.assert_allclose(rot([0, 0, 0, 1], 3), [0, math.sin(0.03), 0, math.cos(0.03)], atol=tol)
+    np.testing.assert_allclose(rot([0.5, -2, 1, 3], 0), [0.5, -2, 1, 3], atol=0)
 
 
 def test_rope_norm_preserving_and_commutes_with_norm():
     B, T, H, D = 1, 40, 2, 64
     x, _, _ = make_qkv(B, T, H, D, seed=23)
-    r = oracle.qk_prologue(x, rope_base=10000.0, eps=-1.0, round_qk=False, qk_precision="f64")
+    r = oracle.qk_prologue(x, rope_base=10000.0, eps=-1.0, round_qk=False)
     np.testing.assert_allclose((r ** 2).sum(-1), (f64(x) ** 2).sum(-1), rtol=1e-13)
-    both = oracle.qk_prologue(x, rope_base=10000.0, eps=1e-6, round_qk=False, qk_precision="f64")
+    both = oracle.qk_prologue(x, rope_base=10000.0, eps=1e-6, round_qk=False)
     # normalise first, then rotate: apply RoPE to the normalised row by solving with the
     # rotation of the raw row (RoPE is linear, the norm is a per-row scale)
     ms = (f64(x) ** 2).mean(-1, keepdims=True)
@@ -232,8 +227,8 @@ def test_rope_relative_position():
     T, D = 24, 32
     a = np.random.default_rng(0).standard_normal(D)
     b = np.random.default_rng(1).standard_normal(D)
-    qa = oracle.qk_prologue(bf16(np.tile(a, (1, T, 1, 1))), eps=1e-6, round_qk=False, qk_precision="f64")[0, :, 0]
-    kb = oracle.qk_prologue(bf16(np.tile(b, (1, T, 1, 1))), eps=1e-6, round_qk=False, qk_precision="f64")[0, :, 0]
+    qa = oracle.qk_prologue(bf16(np.tile(a, (1, T, 1, 1))), eps=1e-6, round_qk=False)[0, :, 0]
+    kb = oracle.qk_prologue(bf16(np.tile(b, (1, T, 1, 1))), eps=1e-6, round_qk=False)[0, :, 0]
     S = qa @ kb.T
     for off in range(-T + 1, T):
         d = np.diagonal(S, offset=off)
@@ -276,8 +271,8 @@ def test_round_bf16_matches_torch_and_brute():
 
 def test_round_qk_rounds_prologue_to_bf16():
     x, _, _ = make_qkv(1, 9, 2, 32, seed=41)
-    a = oracle.qk_prologue(x, round_qk=True, qk_precision="f64")
-    b = oracle.qk_prologue(x, round_qk=False, qk_precision="f64")
+    a = oracle.qk_prologue(x, round_qk=True)
+    b = oracle.qk_prologue(x, round_qk=False)
     assert np.array_equal(a, oracle.round_bf16(b))
     assert not np.array_equal(a, b)
 
@@ -292,7 +287,7 @@ def test_brute_force_small(T):
     q, k, v = make_qkv(B, T, H, D, seed=100 + T)
     qn, kn, vn = (f64(t).tolist() for t in (q, k, v))
     for window, causal in itertools.product(range(-1, 9), (True, False)):
-        out, lse = oracle.attn_fwd(q, k, v, window=window, causal=causal, qk_precision="f64")
+        out, lse = oracle.attn_fwd(q, k, v, window=window, causal=causal)
         bo, bl = brute.forward(qn, kn, vn, window, causal, 10000.0, 1e-6)
         np.testing.assert_allclose(out, np.array(bo), rtol=0, atol=1e-12)
         np.testing.assert_allclose(lse, np.array(bl), rtol=0, atol=1e-12)
@@ -352,7 +347,7 @@ def test_gqa_brute_force():
         ke = [[[kn[b][t][h // (H // Hkv)] for h in range(H)] for t in range(T)] for b in range(1)]
         ve = [[[vn[b][t][h // (H // Hkv)] for h in range(H)] for t in range(T)] for b in range(1)]
         for window, causal in ((-1, True), (1, True), (2, False)):
-            out, lse = oracle.attn_fwd(q, k, v, window=window, causal=causal, qk_precision="f64")
+            out, lse = oracle.attn_fwd(q, k, v, window=window, causal=causal)
             bo, bl = brute.forward(qn, ke, ve, window, causal, 10000.0, 1e-6)
             np.testing.assert_allclose(out, np.array(bo), rtol=0, atol=1e-12)
             np.testing.assert_allclose(lse, np.array(bl), rtol=0, atol=1e-12)
@@ -366,54 +361,194 @@ def test_gqa_rejects_non_divisor_heads():
 
 
 # ---------------------------------------------------------------------------------------------
-# The single-precision prologue (the precision in which q^, k^ are quantised to bf16) computes
-# the same function as the double one, up to its rounding.
+# Near ties of the bf16 rounding of q^, k^ (attn_oracle.c, steps 3 and 6). A single-precision
+# evaluation of RoPE and the norm may round an element that lies within its error of a bf16
+# midpoint the other way; the oracle's ambiguity radius must cover every such evaluation, and the
+# slack it derives must bound every output that those choices lead to.
+
+U = 2.0 ** -24
+
+
+def _angles32(T, D, base):
+    i = np.arange(D // 2, dtype=np.float64)
+    th = np.arange(T, dtype=np.float64)[:, None] * np.power(base, -2.0 * i / D)[None, :]
+    return np.cos(th).astype(np.float32), np.sin(th).astype(np.float32)
+
+
+def _fp32_variants(x, rope_base, eps):
+    """Several single-precision evaluations of RoPE + norm of x [B, T, H, D] (float32 numpy, each
+    operation rounded): the listing's order with numpy's pairwise sums; norm first with the scale
+    folded into cos / sin; and a strictly sequential sum of squares from the last element down."""
+    B, T, H, D = x.shape
+    half = D // 2
+    x = x.astype(np.float32)
+    f = np.float32
+    c, s = _angles32(T, D, rope_base) if rope_base > 0 else (None, None)
+    c4 = None if c is None else c[None, :, None, :]
+    s4 = None if s is None else s[None, :, None, :]
+    e32 = f(eps)
+    outs = []
+
+    def rope(v):
+        x1, x2 = v[..., :half], v[..., half:]
+        return np.concatenate([x1 * c4 + x2 * s4, x2 * c4 - x1 * s4], axis=-1).astype(np.float32)
+
+    # (a) listing order: rotate, then normalise
+    y = rope(x) if rope_base > 0 else x.copy()
+    if eps >= 0:
+        ms = (y * y).sum(-1, keepdims=True, dtype=np.float32) / f(D)
+        y = y * (f(1) / np.sqrt(ms + e32))
+    outs.append(y.astype(np.float32))
+    # (b) norm first, the scale folded into cos and sin
+    r = np.ones(x.shape[:-1] + (1,), np.float32)
+    if eps >= 0:
+        ms = (x * x).sum(-1, keepdims=True, dtype=np.float32) * f(1.0 / D)
+        r = (f(1) / np.sqrt(ms + e32)).astype(np.float32)
+    if rope_base > 0:
+        cr, sr = (c4 * r).astype(np.float32), (s4 * r).astype(np.float32)
+        x1, x2 = x[..., :half], x[..., half:]
+        y = np.concatenate([x1 * cr + x2 * sr, x2 * cr - x1 * sr], axis=-1)
+    else:
+        y = x * r
+    outs.append(y.astype(np.float32))
+    # (c) sequential sum of squares from the last element down, reciprocal square root last
+    acc = np.zeros(x.shape[:-1], np.float32)
+    for d in range(D - 1, -1, -1):
+        acc = (acc + x[..., d] * x[..., d]).astype(np.float32)
+    r = np.ones(x.shape[:-1] + (1,), np.float32)
+    if eps >= 0:
+        r = (f(1) / np.sqrt((acc / f(D) + e32).astype(np.float32)))[..., None].astype(np.float32)
+    y = rope(x * r) if rope_base > 0 else x * r
+    outs.append(y.astype(np.float32))
+    return outs
 
 
 @pytest.mark.parametrize("D,rope_base,eps", [(32, 10000.0, 1e-6), (64, 10000.0, 1e-6), (128, 10000.0, 1e-6),
                                              (64, 0.0, 1e-6), (64, 10000.0, -1.0), (64, 500.0, 0.3)])
-def test_f32_prologue_tracks_f64(D, rope_base, eps):
-    """Error bound of the fp32 sequence: the sum of D squares carries a relative error of at most
-    (D - 1) 2^-24, so r is within about D 2^-25 + 2^-23 relative, and each output, a sum of two
-    products of |x| with |c|, |s| <= r, is within 2^-16 (|x1| + |x2|) r of the exact value."""
-    T = 300
-    x, _, _ = make_qkv(1, T, 2, D, seed=61 + D)
+def test_ambiguity_radius_covers_single_precision_evaluations(D, rope_base, eps):
+    """Every single-precision evaluation rounds each element to a bf16 value within the oracle's
+    ambiguity radius of the oracle's value; the radius is 0 for almost every element, and where an
+    evaluation does round the other way the radius is positive."""
+    x, _, _ = make_qkv(2, 512, 8, D, seed=61 + D)
     x = (x.float() * 3).to(torch.bfloat16)
-    y32 = oracle.qk_prologue(x, rope_base=rope_base, eps=eps, round_qk=False, qk_precision="f32")
-    y64 = oracle.qk_prologue(x, rope_base=rope_base, eps=eps, round_qk=False, qk_precision="f64")
-    xx = f64(x)
-    r = 1 / np.sqrt((xx ** 2).mean(-1, keepdims=True) + eps) if eps >= 0 else np.ones_like(xx[..., :1])
-    if rope_base > 0:
-        half = D // 2
-        mag = np.abs(xx[..., :half]) + np.abs(xx[..., half:])
-        mag = np.concatenate([mag, mag], axis=-1)
-    else:
-        mag = np.abs(xx)
-    bound = 2.0 ** -16 * mag * r + 1e-30
-    assert (np.abs(y32 - y64) <= bound).all()
-    assert np.abs(y32 - y64).max() > 0  # the two modes are genuinely different evaluations
+    y, amb = oracle.qk_prologue(x, rope_base=rope_base, eps=eps, return_amb=True)
+    flips = 0
+    for y32 in _fp32_variants(f64(x), rope_base, eps):
+        r32 = torch.tensor(y32).to(torch.bfloat16).double().numpy()
+        dev = np.abs(r32 - y)
+        assert (dev <= amb).all(), (dev - amb).max()
+        flips += int((dev > 0).sum())
+    assert flips > 0  # the evaluations do disagree with the double rounding somewhere
+    assert 0 < (amb > 0).mean() < 0.02
 
 
-def test_f32_rounding_agrees_with_f64_except_near_ties():
-    D, T = 64, 512
-    x, _, _ = make_qkv(2, T, 4, D, seed=71)
-    a32 = oracle.qk_prologue(x, round_qk=True, qk_precision="f32")
-    a64 = oracle.qk_prologue(x, round_qk=True, qk_precision="f64")
-    y64 = oracle.qk_prologue(x, round_qk=False, qk_precision="f64")
-    y32 = oracle.qk_prologue(x, round_qk=False, qk_precision="f32")
-    assert np.array_equal(a32, oracle.round_bf16(y32))
-    diff = a32 != a64
-    # where they differ, the two roundings are neighbouring bf16 values and the midpoint between
-    # them lies between the fp32 and the double evaluation (a near-tie, nothing else)
-    if diff.any():
-        lo = np.minimum(a32[diff], a64[diff])
-        hi = np.maximum(a32[diff], a64[diff])
-        mid = (lo + hi) / 2
-        assert (oracle.round_bf16(mid + (hi - lo) / 4) == hi).all()
-        assert (oracle.round_bf16(mid - (hi - lo) / 4) == lo).all()
-        a, b = np.minimum(y32[diff], y64[diff]), np.maximum(y32[diff], y64[diff])
-        assert ((a <= mid) & (mid <= b)).all()
-    assert diff.mean() < 1e-3
+def test_ambiguity_radius_literal_cases():
+    """Exact small values (no RoPE, no norm) have no ambiguity; a value placed within the budget
+    of a midpoint has a radius of one bf16 step, one placed outside it has none."""
+    x = bf16(np.array([1.0, -2.5, 0.75, 3.0]).reshape(1, 1, 1, 4))
+    y, amb = oracle.qk_prologue(x, rope_base=0.0, eps=-1.0, return_amb=True)
+    assert np.array_equal(y.ravel(), [1.0, -2.5, 0.75, 3.0]) and not amb.any()
+    # with the norm on: the row (1, 1/2, 1/2, 1/2) has mean square 7/16, so y = x r with
+    # r = 1 / sqrt(7/16 + eps); choose eps so that y_0 = target, which for the target below sits
+    # 2^-30 above the midpoint 1 + 2^-8 between 1 and 1 + 2^-7 (and y_1..3 = target / 2 the same
+    # way above the midpoint 1/2 + 2^-9)
+    row = bf16(np.array([1.0, 0.5, 0.5, 0.5]).reshape(1, 1, 1, 4))
+    for offset, near in ((2.0 ** -30, True), (2.0 ** -14, False)):
+        target = 1.0 + 2.0 ** -8 + offset
+        y, amb = oracle.qk_prologue(row, rope_base=0.0, eps=1.0 / target ** 2 - 7.0 / 16.0, return_amb=True)
+        assert np.array_equal(y.ravel(), [1 + 2.0 ** -7] + [0.5 + 2.0 ** -8] * 3)  # above the midpoints
+        if near:  # within the evaluation budget of them: either neighbour is correct
+            assert np.array_equal(amb.ravel(), [2.0 ** -7] + [2.0 ** -8] * 3)
+        else:
+            assert not amb.any()
+
+
+def _brute_head(qh, kh, v, window, causal):
+    """float64 softmax attention of one head from given q^, k^ (no prologue), v [T, D]."""
+    T, D = qh.shape
+    S = qh @ kh.T / math.sqrt(D)
+    vis = np.array([[brute.visible(i, j, window, causal) for j in range(T)] for i in range(T)])
+    S = np.where(vis, S, -np.inf)
+    m = S.max(1, keepdims=True)
+    w = np.exp(S - m)
+    z = w.sum(1, keepdims=True)
+    return (w / z) @ v, (m + np.log(z)).ravel()
+
+
+@pytest.mark.parametrize("T,window,causal", [(1, -1, True), (4, -1, True), (6, 2, True), (5, 1, False),
+                                             (8, -1, False)])
+def test_slack_bounds_every_choice(T, window, causal):
+    """Brute force: with the budget widened 2^8-fold (many ambiguous elements), every choice of
+    q^, k^ within the radii, at the corners of the box and at random points inside it, gives
+    outputs within the slack of the oracle's; and the slack is 0 for rows that no ambiguous
+    element touches."""
+    D, scale = 8, 2.0 ** 8
+    rng = np.random.default_rng(T * 31 + window)
+    q, k, v = make_qkv(1, T, 2, D, seed=700 + T)
+    out, lse, os_, ls_ = oracle.attn_fwd(q, k, v, window=window, causal=causal, return_slack=True,
+                                         amb_scale=scale)
+    yq, aq = oracle.qk_prologue(q, return_amb=True, amb_scale=scale)
+    yk, ak = oracle.qk_prologue(k, return_amb=True, amb_scale=scale)
+    assert (aq > 0).any() and (ak > 0).any()
+    vv = f64(v)
+    for h in range(2):
+        Q, K, AQ, AK, V = yq[0, :, h], yk[0, :, h], aq[0, :, h], ak[0, :, h], vv[0, :, h]
+        o0, l0 = _brute_head(Q, K, V, window, causal)
+        np.testing.assert_allclose(o0, out[0, :, h], atol=1e-13)
+        worst_o, worst_l = np.zeros_like(o0), np.zeros_like(l0)
+        for n in range(600):
+            if n < 2:
+                sq, sk = np.full(Q.shape, 1 - 2 * n), np.full(K.shape, 2 * n - 1)
+            elif n < 300:
+                sq, sk = rng.choice([-1.0, 0.0, 1.0], Q.shape), rng.choice([-1.0, 0.0, 1.0], K.shape)
+            else:
+                sq, sk = rng.uniform(-1, 1, Q.shape), rng.uniform(-1, 1, K.shape)
+            o, l = _brute_head(Q + sq * AQ, K + sk * AK, V, window, causal)
+            worst_o = np.maximum(worst_o, np.abs(o - o0))
+            worst_l = np.maximum(worst_l, np.abs(l - l0))
+        assert (worst_l <= ls_[0, h] + 1e-12).all(), (worst_l - ls_[0, h]).max()
+        assert (worst_o <= os_[0, :, h] + 1e-12).all(), (worst_o - os_[0, :, h]).max()
+        assert (ls_[0, h] > 0).any()
+
+
+def test_slack_of_a_single_key_row_is_attained():
+    """Row 0 under the causal mask sees one key, so its lse is the score q^_0 . k^_0 / sqrt(D) and
+    its output is v_0: the lse slack equals the largest possible move of that score up to the
+    second-order term, and the output slack is 0."""
+    D, scale = 16, 2.0 ** 9
+    for seed in range(5):
+        q, k, v = make_qkv(1, 1, 1, D, seed=800 + seed)
+        out, lse, os_, ls_ = oracle.attn_fwd(q, k, v, causal=True, return_slack=True, amb_scale=scale)
+        yq, aq = oracle.qk_prologue(q, return_amb=True, amb_scale=scale)
+        yk, ak = oracle.qk_prologue(k, return_amb=True, amb_scale=scale)
+        Q, K, AQ, AK = yq.ravel(), yk.ravel(), aq.ravel(), ak.ravel()
+        first = (AQ * np.abs(K) + np.abs(Q) * AK).sum() / math.sqrt(D)
+        second = (AQ * AK).sum() / math.sqrt(D)
+        assert first + second > 0
+        # the corner with each perturbation aligned to the other factor's sign moves s by >= first - second
+        best = ((Q + AQ * np.sign(K)) @ (K + AK * np.sign(Q)) - Q @ K) / math.sqrt(D)
+        assert best >= first - second - 1e-15
+        assert abs(ls_.item() - (first + second)) <= 1e-12 * max(1.0, first)
+        assert os_.max() == 0.0
+
+
+def test_slack_zero_without_rounding_or_ambiguity():
+    q, k, v = make_qkv(1, 40, 2, 32, seed=905)
+    _, _, os_, ls_ = oracle.attn_fwd(q, k, v, window=7, round_qk=False, return_slack=True)
+    assert not os_.any() and not ls_.any()
+    # raw mode on small integers: q^, k^ are the inputs themselves, exactly bf16
+    qi, ki = (torch.randint(-3, 4, (1, 40, 2, 32)).to(torch.bfloat16) for _ in range(2))
+    _, _, os_, ls_ = oracle.attn_fwd(qi, ki, v, rope_base=0.0, eps=-1.0, return_slack=True)
+    assert not os_.any() and not ls_.any()
+    # and the slack outputs leave out and lse unchanged
+    a = oracle.attn_fwd(q, k, v, window=7)
+    b = oracle.attn_fwd(q, k, v, window=7, return_slack=True)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    rows = [(0, 1, 39), (0, 0, 3)]
+    ro, rl, ros, rls = oracle.attn_rows(q, k, v, rows, window=7, return_slack=True)
+    for n, (bb, h, i) in enumerate(rows):
+        assert np.array_equal(ro[n], b[0][bb, i, h]) and rl[n] == b[1][bb, h, i]
+        assert np.array_equal(ros[n], b[2][bb, i, h]) and rls[n] == b[3][bb, h, i]
 
 
 # ---------------------------------------------------------------------------------------------
