@@ -10,3 +10,13 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (B300, sm_103a) and the built CUDA library")
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """After a run of the GPU parity tests: how much of the oracle's near-tie slack each
+    comparison used (see gpu_helpers)."""
+    helpers = sys.modules.get("gpu_helpers")
+    if helpers is None:
+        return
+    for line in helpers.slack_table():
+        terminalreporter.write_line(line)

@@ -1,6 +1,7 @@
 """Parity of the CUDA path (through the C ABI) with the float64 oracle on the same seeded inputs.
 
-Tolerances: max |out - oracle| <= 2e-2 on the bf16 output; |lse - oracle| <= 1e-3 * max(1, |lse|).
+Tolerances: max |out - oracle| <= 2e-2 on the bf16 output; |lse - oracle| <= 1e-3 * max(1, |lse|),
+each widened by the oracle's near-tie slack of that element (gpu_helpers).
 """
 import itertools
 
@@ -8,8 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
-from gpu_helpers import assert_close, gpu_fwd
+from gpu_helpers import assert_close, gpu_fwd, oracle_fwd
 from sliding_window_attention_04_b300 import configs
 from sliding_window_attention_04_b300.inputs import layer_seed, make_qkv
 
@@ -26,8 +26,8 @@ def lib():
 
 def check(q, k, v, window, causal, rope_base=10000.0, eps=1e-6, what=""):
     out, lse = gpu_fwd(q, k, v, window=window, causal=causal, rope_base=rope_base, eps=eps)
-    ref, lref = oracle.attn_fwd(q, k, v, window=window, causal=causal, rope_base=rope_base, eps=eps)
-    return assert_close(out, ref, lse, lref, what or f"w={window} c={causal}")
+    ref, lref, os_, ls_ = oracle_fwd(q, k, v, window=window, causal=causal, rope_base=rope_base, eps=eps)
+    return assert_close(out, ref, lse, lref, what or f"w={window} c={causal}", os_, ls_)
 
 
 def test_tiny_workload_full():
@@ -221,8 +221,8 @@ def test_many_calls_reuse_ticket_slots():
     for o, l in outs:
         assert torch.equal(o, ref) and torch.equal(l, lref)
     out, lse = ref.cpu().double().numpy(), lref.cpu().double().numpy()
-    r, lr = oracle.attn_fwd(q.cpu(), k.cpu(), v.cpu(), window=200, causal=True)
-    assert_close(out, r, lse, lr, "many calls")
+    r, lr, os_, ls_ = oracle_fwd(q.cpu(), k.cpu(), v.cpu(), window=200, causal=True)
+    assert_close(out, r, lse, lr, "many calls", os_, ls_)
 
 
 @pytest.mark.parametrize("D,H,Hkv,T,window", [(64, 4, 2, 513, 127), (64, 6, 1, 300, -1), (32, 4, 2, 300, 100),
