@@ -19,8 +19,10 @@
  *  - lse: fp32, layout [B, H, T].
  *  - Positions are 0..T-1 for every batch row. The softmax scale is fixed at 1/sqrt(D).
  *  - Q^ and K^ are rounded to bf16 before the products (as the listing's bf16 autocast does);
- *    the norm and rotation before that rounding are evaluated in fp32 with a fixed sequence of
- *    correctly rounded operations, so the rounded values are reproducible.
+ *    the norm and rotation before that rounding are evaluated in fp32 (correctly rounded
+ *    operations, cos / sin of the double-precision angle). Where the exact value lies within
+ *    that evaluation's error of a bf16 rounding midpoint, either neighbouring bf16 value may
+ *    result; everywhere else the rounded value is the exact one's.
  *  - Return value: ATTN_OK (0) or one of the negative ATTN_ERR_* codes below. Argument errors
  *    are detected on the host before anything is launched.
  *  - Calls are asynchronous on the given stream; results are ready when the stream is.
@@ -77,7 +79,9 @@ int attn_init(int device);
  * The persistent kernel (D = 32, 64, 128) hands out work through a pair of device counters owned
  * by the library; each call takes the next of 256 such pairs, and the kernel resets its pair when
  * it finishes. Calls issued one after another on a stream can therefore be repeated without
- * limit, and up to 256 calls may run at the same time on different streams.
+ * limit. A pair last used by a call on another stream is taken only after that call's kernel
+ * has finished: the new call's stream waits for it (an event the library records after every
+ * launch), so up to 256 calls run at the same time on different streams and further ones wait.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int T, int D,
              int window, int causal, float rope_base, float eps, void* stream);
@@ -145,15 +149,28 @@ int attn_selftest_wait_timeout(void* stream);
  *  - The first call on a device does a one-time set-up on the host (checks the device, raises the
  *    kernels' shared-memory limits, looks up the array's device address); make that first call
  *    before any stream capture.
- *  - Each call enqueues, on `stream`, a small kernel that clears the error word and rebuilds the
- *    table for (T, D, rope_base) in the array (cos / sin evaluated in double on the device,
- *    stored as fp32), then the attention kernel. All calls share the one array and it keeps the
- *    last call's contents: calls whose work overlaps on the GPU (other streams, other threads)
- *    race on it and must be serialised by the caller.
- *  - A bounded-wait timeout of this path is recorded in that shared error word only; it is not
- *    reported by attn_device_status. */
+ *  - Each call with rope_base > 0 enqueues, on `stream`, a small kernel that rebuilds the table
+ *    for (T, D, rope_base) in the array (cos / sin evaluated in double on the device, stored as
+ *    fp32), then the attention kernel. All calls share the one array and it keeps the last call's
+ *    contents: calls whose work overlaps on the GPU (other streams, other threads) race on it and
+ *    must be serialised by the caller.
+ *  - A bounded-wait timeout of this path is recorded in that shared error word, where it stays
+ *    until attn_noalloc_status reads and clears it; attn_device_status does not see it. */
 int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int T,
                      int D, int window, int causal, float rope_base, float eps, void* stream);
+
+/* attn_noalloc_status — read and clear the error word of attn_fwd_noalloc on the current device.
+ * The pages have no counterpart. Waits for `stream` (which must belong to the current device),
+ * copies the word out of the library's fixed array and writes zero back, both through copies to
+ * and from host variables: nothing is allocated. Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT if an
+ * attn_fwd_noalloc kernel gave up on a bounded wait since the last read, or ATTN_ERR_CUDA /
+ * ATTN_ERR_NO_DEVICE. Like attn_fwd_noalloc, its first call on a device does the one-time set-up. */
+int attn_noalloc_status(void* stream);
+
+/* attn_noalloc_selftest_wait_timeout — the bounded-wait self test of attn_selftest_wait_timeout,
+ * writing its timeout code to attn_fwd_noalloc's error word instead of attn_init's, so that
+ * attn_noalloc_status can be tested on hardware without any fault. Allocates nothing. */
+int attn_noalloc_selftest_wait_timeout(void* stream);
 
 #ifdef __cplusplus
 }

@@ -26,7 +26,8 @@ ATTN_ERR_NO_DEVICE = -6
 ATTN_ERR_SCRATCH_LIMIT = -7
 
 EXPORTED = ("attn_init", "attn_fwd", "attn_destroy", "attn_status_string", "attn_device_status",
-            "attn_selftest_wait_timeout", "attn_fwd_noalloc", "attn_fwd_kernel", "attn_fwd_gqa")
+            "attn_selftest_wait_timeout", "attn_fwd_noalloc", "attn_fwd_kernel", "attn_fwd_gqa",
+            "attn_noalloc_status", "attn_noalloc_selftest_wait_timeout")
 
 
 class AttnError(RuntimeError):
@@ -61,6 +62,10 @@ def _load() -> ctypes.CDLL:
     lib.attn_fwd_noalloc.restype = c_int
     lib.attn_fwd_kernel.argtypes = [c_int]
     lib.attn_fwd_kernel.restype = c_int
+    lib.attn_noalloc_status.argtypes = [c_void_p]
+    lib.attn_noalloc_status.restype = c_int
+    lib.attn_noalloc_selftest_wait_timeout.argtypes = [c_void_p]
+    lib.attn_noalloc_selftest_wait_timeout.restype = c_int
     return lib
 
 
@@ -132,6 +137,18 @@ def attn_fwd_noalloc_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, lse_p
                                     ctypes.c_void_p(out_ptr), ctypes.c_void_p(lse_ptr or None), int(B), int(H),
                                     int(T), int(D), int(window), int(causal), float(rope_base), float(eps),
                                     ctypes.c_void_p(stream or None)))
+
+
+def attn_noalloc_status(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Read and clear attn_fwd_noalloc's error word (waits for `stream`); returns the status code."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(lib.attn_noalloc_status(ctypes.c_void_p(s.cuda_stream or None)))
+
+
+def attn_noalloc_selftest_wait_timeout(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """The bounded-wait self test on attn_fwd_noalloc's error word; returns the status code of the launch."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(lib.attn_noalloc_selftest_wait_timeout(ctypes.c_void_p(s.cuda_stream or None)))
 
 
 def _check_input(name: str, t: torch.Tensor, shape=None):

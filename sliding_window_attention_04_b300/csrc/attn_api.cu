@@ -24,11 +24,19 @@ struct RopeTable {
 };
 
 // Ticket counters of the persistent kernel: one (ticket, exits) pair per slot, 128 bytes apart.
-// Each call takes the next slot; the kernel's last CTA resets its pair to zero on exit, so calls
-// that follow each other on a stream reuse slots safely, and up to kSchedSlots calls may be in
-// flight at once on different streams.
+// Each call takes the next slot; the kernel's last CTA resets its pair to zero on exit. A slot is
+// only ever reused after its previous kernel has finished: on the same stream by stream order, on
+// another stream because the new call's stream first waits for an event recorded after the
+// previous kernel of that slot (so more than kSchedSlots calls in flight at once on different
+// streams are serialised, never corrupted).
 constexpr int kSchedSlots = 256;
 constexpr int kSchedStride = 32;  // ints per slot
+
+struct SchedSlot {
+  cudaEvent_t done = nullptr;    // recorded on `stream` right after the slot's last launch
+  cudaStream_t stream = nullptr;
+  bool used = false;
+};
 
 struct State {
   std::mutex mu;
@@ -38,6 +46,7 @@ struct State {
   int* d_err = nullptr;
   int* d_sched = nullptr;
   unsigned sched_next = 0;
+  SchedSlot slots[kSchedSlots];
   bool ws_ok[3] = {false, false, false};  // warp-specialised kernel usable for D = 32, 64, 128
   std::map<std::pair<int, float>, RopeTable> tables;  // (D, base) -> table
   std::vector<float4*> retired;                       // outgrown tables, freed at destroy
@@ -185,9 +194,9 @@ constexpr size_t kNoAllocHeaderBytes = 256;
 constexpr size_t kNoAllocTablePairs = size_t(1) << 19;  // T * D / 2 <= 524288 pairs (4 MiB)
 constexpr size_t kNoAllocBytes = kNoAllocHeaderBytes + kNoAllocTablePairs * sizeof(float2);
 
-// Fills the cos / sin table for (T, D, base) in the layout of build_table ([D/4][T] float4) and
-// clears the error word. Runs on the caller's stream right before the attention kernel, so each
-// call starts from a clean state.
+// Fills the cos / sin table for (T, D, base) in the layout of build_table ([D/4][T] float4). Runs
+// on the caller's stream right before the attention kernel. The error word is left alone: it
+// keeps a timeout until attn_noalloc_status reads and clears it.
 __global__ void noalloc_prepare_kernel(unsigned char* scratch, int T, int D, float base) {
   float* table = reinterpret_cast<float*>(scratch + kNoAllocHeaderBytes);
   const int half = D / 2;
@@ -202,7 +211,6 @@ __global__ void noalloc_prepare_kernel(unsigned char* scratch, int T, int D, flo
     dst[0] = static_cast<float>(cs);
     dst[2] = static_cast<float>(sn);
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(scratch) = 0;
 }
 
 struct NoAllocDevice {
@@ -240,12 +248,16 @@ int noalloc_setup(int* dev_out, unsigned char** scratch_out) {
   if (it == noalloc_devices().end()) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
       return ATTN_ERR_CUDA;
+    }
     if (major != 10 || minor != 3) return ATTN_ERR_NO_DEVICE;
     if (set_kernel_attrs<32>() != cudaSuccess || set_kernel_attrs<64>() != cudaSuccess ||
-        set_kernel_attrs<128>() != cudaSuccess)
+        set_kernel_attrs<128>() != cudaSuccess) {
+      cudaGetLastError();
       return ATTN_ERR_CUDA;
+    }
     unsigned char* ptr = nullptr;
     if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
       cudaGetLastError();
@@ -293,11 +305,20 @@ int attn_init(int device) {
     const size_t sched_bytes = sizeof(int) * kSchedSlots * kSchedStride;
     if ((r = cudaMalloc(&d_sched, sched_bytes)) != cudaSuccess) return r;
     if ((r = cudaMemset(d_sched, 0, sched_bytes)) != cudaSuccess) return r;
+    for (int i = 0; i < kSchedSlots; ++i) {
+      s.slots[i] = SchedSlot{};
+      if ((r = cudaEventCreateWithFlags(&s.slots[i].done, cudaEventDisableTiming)) != cudaSuccess) return r;
+    }
     return cudaDeviceSynchronize();
   });
   if (e != cudaSuccess) {
+    cudaGetLastError();
     if (d_err) cudaFree(d_err);
     if (d_sched) cudaFree(d_sched);
+    for (SchedSlot& sl : s.slots) {
+      if (sl.done) cudaEventDestroy(sl.done);
+      sl = SchedSlot{};
+    }
     return ATTN_ERR_CUDA;
   }
   void* fn = nullptr;
@@ -305,8 +326,16 @@ int attn_init(int device) {
   if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qres) !=
           cudaSuccess ||
       qres != cudaDriverEntryPointSuccess || fn == nullptr) {
-    cudaFree(d_err);
-    cudaFree(d_sched);
+    cudaGetLastError();
+    with_device(device, [&]() -> cudaError_t {
+      cudaFree(d_err);
+      cudaFree(d_sched);
+      for (SchedSlot& sl : s.slots) {
+        if (sl.done) cudaEventDestroy(sl.done);
+        sl = SchedSlot{};
+      }
+      return cudaSuccess;
+    });
     return ATTN_ERR_CUDA;
   }
   s.encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
@@ -348,38 +377,26 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
   if (D != 32 && D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
 
   State& s = state();
+  // Held until the launch is enqueued: the ticket slot is chosen, ordered after its previous user
+  // and marked with this launch as one step, so no other thread can take the same slot in between.
+  std::lock_guard<std::mutex> lock(s.mu);
+  if (!s.inited) return ATTN_ERR_NOT_INITIALIZED;
+  const bool use_ws = (D == 32 && s.ws_ok[0]) || (D == 64 && s.ws_ok[1]) || (D == 128 && s.ws_ok[2]);
   float4* table = nullptr;
   int table_T = 0;
-  int* d_err = nullptr;
-  int* sched = nullptr;
-  bool use_ws = false;
-  int sm_count = 0;
-  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(s.mu);
-    if (!s.inited) return ATTN_ERR_NOT_INITIALIZED;
-    d_err = s.d_err;
-    use_ws = (D == 32 && s.ws_ok[0]) || (D == 64 && s.ws_ok[1]) || (D == 128 && s.ws_ok[2]);
-    if (use_ws) {
-      sched = s.d_sched + static_cast<size_t>(s.sched_next % kSchedSlots) * kSchedStride;
-      ++s.sched_next;
+  if (rope_base > 0.f) {
+    RopeTable& t = s.tables[std::make_pair(D, rope_base)];
+    if (t.T < T) {
+      float4* fresh = nullptr;
+      const int want = T;
+      if (with_device(s.device, [&] { return build_table(D, rope_base, want, &fresh); }) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+      if (t.ptr) s.retired.push_back(t.ptr);
+      t.ptr = fresh;
+      t.T = want;
     }
-    sm_count = s.sm_count;
-    encode = s.encode_tiled;
-    if (rope_base > 0.f) {
-      RopeTable& t = s.tables[std::make_pair(D, rope_base)];
-      if (t.T < T) {
-        float4* fresh = nullptr;
-        const int want = T;
-        if (with_device(s.device, [&] { return build_table(D, rope_base, want, &fresh); }) != cudaSuccess)
-          return ATTN_ERR_CUDA;
-        if (t.ptr) s.retired.push_back(t.ptr);
-        t.ptr = fresh;
-        t.T = want;
-      }
-      table = t.ptr;
-      table_T = t.T;
-    }
+    table = t.ptr;
+    table_T = t.T;
   }
 
   swa::AttnParams p{};  // every field set below or zero
@@ -390,7 +407,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
   p.lse = lse;
   p.rope = table;
   p.rope_T = table_T;
-  p.err = d_err;
+  p.err = s.d_err;
   p.B = B;
   p.H = H;
   p.Hkv = Hkv;
@@ -406,11 +423,28 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (use_ws) {
-    switch (D) {
-      case 32: return launch_ws<32>(p, encode, sm_count, sched, st);
-      case 64: return launch_ws<64>(p, encode, sm_count, sched, st);
-      default: return launch_ws<128>(p, encode, sm_count, sched, st);
+    SchedSlot& slot = s.slots[s.sched_next % kSchedSlots];
+    int* sched = s.d_sched + static_cast<size_t>(s.sched_next % kSchedSlots) * kSchedStride;
+    // a slot last used on another stream: this launch waits for that kernel to finish first
+    if (slot.used && slot.stream != st && cudaStreamWaitEvent(st, slot.done, 0) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
     }
+    int rc;
+    switch (D) {
+      case 32: rc = launch_ws<32>(p, s.encode_tiled, s.sm_count, sched, st); break;
+      case 64: rc = launch_ws<64>(p, s.encode_tiled, s.sm_count, sched, st); break;
+      default: rc = launch_ws<128>(p, s.encode_tiled, s.sm_count, sched, st); break;
+    }
+    if (rc != ATTN_OK) return rc;
+    if (cudaEventRecord(slot.done, st) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    slot.used = true;
+    slot.stream = st;
+    ++s.sched_next;
+    return ATTN_OK;
   }
   cudaError_t e;
   switch (D) {
@@ -451,10 +485,13 @@ void attn_destroy(void) {
     for (float4* ptr : s.retired) cudaFree(ptr);
     if (s.d_err) cudaFree(s.d_err);
     if (s.d_sched) cudaFree(s.d_sched);
+    for (SchedSlot& sl : s.slots)
+      if (sl.done) cudaEventDestroy(sl.done);
     return cudaSuccess;
   });
+  for (SchedSlot& sl : s.slots) sl = SchedSlot{};
   s.d_sched = nullptr;
-  s.ws_ok[0] = s.ws_ok[1] = false;
+  s.ws_ok[0] = s.ws_ok[1] = s.ws_ok[2] = false;
   s.tables.clear();
   s.retired.clear();
   s.d_err = nullptr;
@@ -543,8 +580,10 @@ int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, flo
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t pairs = rope_base > 0.f ? static_cast<size_t>(T) * (D / 2) : 0;
   const int prep_blocks = static_cast<int>(pairs == 0 ? 1 : (pairs + 255) / 256 < 1184 ? (pairs + 255) / 256 : 1184);
-  noalloc_prepare_kernel<<<prep_blocks, 256, 0, st>>>(scratch, T, D, rope_base);
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  if (pairs > 0) {
+    noalloc_prepare_kernel<<<prep_blocks, 256, 0, st>>>(scratch, T, D, rope_base);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  }
 
   swa::AttnParams p{};  // every field set below or zero
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -573,6 +612,35 @@ int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, flo
     default: e = launch_simple<128>(p, st); break;
   }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_noalloc_status(void* stream) {
+  int dev = -1;
+  unsigned char* scratch = nullptr;
+  const int rc = noalloc_setup(&dev, &scratch);
+  if (rc != ATTN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int h = 0;
+  const int zero = 0;
+  // the word sits at offset 0 of the scratch array; copies to and from pageable host variables,
+  // completed before returning (nothing is allocated)
+  if (cudaMemcpyFromSymbolAsync(&h, g_noalloc_scratch, sizeof(int), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess ||
+      cudaMemcpyToSymbolAsync(g_noalloc_scratch, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  return h == 0 ? ATTN_OK : ATTN_ERR_DEVICE_TIMEOUT;
+}
+
+int attn_noalloc_selftest_wait_timeout(void* stream) {
+  int dev = -1;
+  unsigned char* scratch = nullptr;
+  const int rc = noalloc_setup(&dev, &scratch);
+  if (rc != ATTN_OK) return rc;
+  selftest_wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(reinterpret_cast<int*>(scratch));
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -93,7 +93,8 @@ struct WsCfg {
   static constexpr int kBarPFull = kBarBufFree + kSBufs;  // [2 tiles][2] softmax t wrote P of job n -> P.V issuer t
   static constexpr int kBarPVDone = kBarPFull + 4;        // [2 tiles][2] P.V job n of tile t done -> softmax, S issuer
   static constexpr int kBarFinal = kBarPVDone + 4;        // [3] MMA drain at exit (S issuer, P.V issuers)
-  static constexpr int kNumBars = kBarFinal + 3;
+  static constexpr int kBarEpi = kBarFinal + 3;           // [2] tile t's four softmax warps are done with the unit
+  static constexpr int kNumBars = kBarEpi + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, unit ids, unit geometry
   static constexpr int kSmemBytes = kOffMisc + 128 + 1024;  // + alignment slack
   // TMEM columns
@@ -491,6 +492,7 @@ __global__ void __launch_bounds__(640, 1)
       mbar_init(bar(Cfg::kBarBufFree + i), 1);
     }
     for (int i = 0; i < 3; ++i) mbar_init(bar(Cfg::kBarFinal + i), 1);
+    for (int i = 0; i < 2; ++i) mbar_init(bar(Cfg::kBarEpi + i), 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -868,9 +870,19 @@ __global__ void __launch_bounds__(640, 1)
         ++n;
       }
       if (!ok) break;
+      // Each of the tile's four warps arrives on the epilogue barrier once per unit (after staging
+      // its rows of the output); warp 0 alone waits for the four, with the bounded wait, before the
+      // slot is released (and the output stored). Warps 1-3 cannot arrive for the next unit before
+      // warp 0 has arrived for it, so the barrier is never two phases ahead of that wait.
+      const bool stores = (warp & 3) == 0;
       if (!g.valid(t)) {  // this query tile lies past T
-        named_bar_sync(1 + t, 128);
-        if (r == 0) mbar_arrive(bar(Cfg::kBarQEmpty + slot));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(Cfg::kBarEpi + t));
+        if (stores) {
+          ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarEpi + t), ul & 1, abort_flag));
+          if (ok && r == 0) mbar_arrive(bar(Cfg::kBarQEmpty + slot));
+        }
+        if (!ok) break;
         continue;
       }
       // ---- epilogue: O / l -> bf16 staged in this tile's Q buffer, one TMA store; LSE ----
@@ -901,14 +913,19 @@ __global__ void __launch_bounds__(640, 1)
         p.lse[(static_cast<size_t>(g.b) * p.H + g.h) * p.T + i_row] = (m_fin + __log2f(l_run)) * 0.69314718055994531f;
       }
       fence_proxy_async_smem();
-      named_bar_sync(1 + t, 128);
-      if (r == 0) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Cfg::kBarEpi + t));
+      if (stores) {
+        ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarEpi + t), ul & 1, abort_flag));
+        if (ok && r == 0) {
 #pragma unroll
-        for (int x = 0; x < kBoxes; ++x) tma_store_4d(&maps.out, stage + x * kTile * 128, 64 * x, g.h, qs, g.b);
-        bulk_commit_group();
-        bulk_wait_group_read0();
-        mbar_arrive(bar(Cfg::kBarQEmpty + slot));
+          for (int x = 0; x < kBoxes; ++x) tma_store_4d(&maps.out, stage + x * kTile * 128, 64 * x, g.h, qs, g.b);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(bar(Cfg::kBarQEmpty + slot));
+        }
       }
+      if (!ok) break;
     }
     if (!ok && lane == 0) fail();
     if (r == 0) bulk_wait_group0();

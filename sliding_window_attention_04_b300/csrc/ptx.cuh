@@ -158,11 +158,6 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
-// Named barrier over `count` threads (a multiple of 32); id 0 is __syncthreads'.
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // Per-warpgroup register budget changes (all four warps of a warpgroup execute them).
 template <uint32_t N>
 __device__ __forceinline__ void regs_inc() {
