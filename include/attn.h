@@ -77,11 +77,15 @@ int attn_init(int device);
  * every later call allocates nothing and does not synchronise the host.
  *
  * The persistent kernel (D = 32, 64, 128) hands out work through a pair of device counters owned
- * by the library; each call takes the next of 256 such pairs, and the kernel resets its pair when
- * it finishes. Calls issued one after another on a stream can therefore be repeated without
- * limit. A pair last used by a call on another stream is taken only after that call's kernel
- * has finished: the new call's stream waits for it (an event the library records after every
- * launch), so up to 256 calls run at the same time on different streams and further ones wait.
+ * by the library, and the kernel resets its pair when it finishes. Calls issued one after another
+ * on a stream can therefore be repeated without limit. Outside stream capture each call takes the
+ * next of 128 such pairs; a pair last used by a call on another stream is taken only after that
+ * call's kernel has finished (the new call's stream waits for an event the library records after
+ * every launch), so up to 128 calls run at the same time on different streams and further ones
+ * wait. A call made while `stream` is being captured into a CUDA graph takes the next of another
+ * 128 pairs and records no event (a captured launch cannot wait for work outside its graph):
+ * graph launches that run at the same time on different streams must together hold at most 128
+ * captured attention calls. Tensor maps of the buffers are cached by (pointer, shape).
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int T, int D,
              int window, int causal, float rope_base, float eps, void* stream);

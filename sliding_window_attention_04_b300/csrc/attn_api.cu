@@ -24,11 +24,14 @@ struct RopeTable {
 };
 
 // Ticket counters of the persistent kernel: one (ticket, exits) pair per slot, 128 bytes apart.
-// Each call takes the next slot; the kernel's last CTA resets its pair to zero on exit. A slot is
-// only ever reused after its previous kernel has finished: on the same stream by stream order, on
-// another stream because the new call's stream first waits for an event recorded after the
-// previous kernel of that slot (so more than kSchedSlots calls in flight at once on different
-// streams are serialised, never corrupted).
+// Each call takes a slot; the kernel's last CTA resets its pair to zero on exit. Calls made outside
+// stream capture take the next slot of the first kSchedSlots / 2, round robin, and a slot is only
+// ever reused after its previous kernel has finished: on the same stream by stream order, on another
+// stream because the new call's stream first waits for an event recorded after the previous kernel
+// of that slot (so more calls in flight than slots are serialised, never corrupted). Calls made
+// while the stream is being captured into a CUDA graph take the next slot of the other half; they
+// cannot wait for work outside the capture, so graph launches that run at the same time must hold
+// fewer captured calls than that half.
 constexpr int kSchedSlots = 256;
 constexpr int kSchedStride = 32;  // ints per slot
 
@@ -38,6 +41,21 @@ struct SchedSlot {
   bool used = false;
 };
 
+// Tensor maps depend only on the base pointer and the shape; they are cached so that repeated calls
+// on the same buffers skip the encoding.
+struct MapKey {
+  const void* base;
+  int B, H, T, D;
+  bool operator<(const MapKey& o) const {
+    if (base != o.base) return base < o.base;
+    if (B != o.B) return B < o.B;
+    if (H != o.H) return H < o.H;
+    if (T != o.T) return T < o.T;
+    return D < o.D;
+  }
+};
+constexpr size_t kMapCacheMax = 1024;
+
 struct State {
   std::mutex mu;
   bool inited = false;
@@ -45,8 +63,10 @@ struct State {
   int sm_count = 0;
   int* d_err = nullptr;
   int* d_sched = nullptr;
-  unsigned sched_next = 0;
+  unsigned sched_next = 0;    // next eager slot (first half)
+  unsigned capture_next = 0;  // next slot of calls under stream capture (second half)
   SchedSlot slots[kSchedSlots];
+  std::map<MapKey, CUtensorMap> maps;
   bool ws_ok[3] = {false, false, false};  // warp-specialised kernel usable for D = 32, 64, 128
   std::map<std::pair<int, float>, RopeTable> tables;  // (D, base) -> table
   std::vector<float4*> retired;                       // outgrown tables, freed at destroy
@@ -164,15 +184,31 @@ cudaError_t launch_simple(const swa::AttnParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// The cached tensor map of a [B, T, H, D] bf16 tensor at `base` (encoded on first use).
+const CUtensorMap* cached_map(std::map<MapKey, CUtensorMap>& cache, PFN_cuTensorMapEncodeTiled_v12000 encode,
+                              const void* base, int B, int H, int T, int D) {
+  const MapKey key{base, B, H, T, D};
+  auto it = cache.find(key);
+  if (it != cache.end()) return &it->second;
+  CUtensorMap m;
+  if (encode_tile_map(encode, &m, base, B, H, T, D) != CUDA_SUCCESS) return nullptr;
+  if (cache.size() >= kMapCacheMax) cache.clear();
+  return &cache.emplace(key, m).first->second;
+}
+
 template <int D>
-int launch_ws(const swa::AttnParams& p, PFN_cuTensorMapEncodeTiled_v12000 encode, int sm_count, int* sched,
-              cudaStream_t stream) {
+int launch_ws(const swa::AttnParams& p, std::map<MapKey, CUtensorMap>& cache,
+              PFN_cuTensorMapEncodeTiled_v12000 encode, int sm_count, int* sched, cudaStream_t stream) {
   swa::WsMaps maps;
-  if (encode_tile_map(encode, &maps.q, p.q, p.B, p.H, p.T, D) != CUDA_SUCCESS ||
-      encode_tile_map(encode, &maps.k, p.k, p.B, p.Hkv, p.T, D) != CUDA_SUCCESS ||
-      encode_tile_map(encode, &maps.v, p.v, p.B, p.Hkv, p.T, D) != CUDA_SUCCESS ||
-      encode_tile_map(encode, &maps.out, p.out, p.B, p.H, p.T, D) != CUDA_SUCCESS)
-    return ATTN_ERR_CUDA;
+  const CUtensorMap* mq = cached_map(cache, encode, p.q, p.B, p.H, p.T, D);
+  const CUtensorMap* mk = cached_map(cache, encode, p.k, p.B, p.Hkv, p.T, D);
+  const CUtensorMap* mv = cached_map(cache, encode, p.v, p.B, p.Hkv, p.T, D);
+  const CUtensorMap* mo = cached_map(cache, encode, p.out, p.B, p.H, p.T, D);
+  if (!mq || !mk || !mv || !mo) return ATTN_ERR_CUDA;
+  maps.q = *mq;
+  maps.k = *mk;
+  maps.v = *mv;
+  maps.out = *mo;
   // work is handed out in chunks of two 256-row query blocks of one head (see the kernel), heads in
   // groups whose K and V fit in half of L2 together, so a group's blocks share them there
   const long long n_qb = (p.T + 2 * swa::kTile - 1) / (2 * swa::kTile);
@@ -342,6 +378,7 @@ int attn_init(int device) {
   s.d_err = d_err;
   s.d_sched = d_sched;
   s.sched_next = 0;
+  s.capture_next = 0;
   s.ws_ok[0] = ws_ok[0];
   s.ws_ok[1] = ws_ok[1];
   s.ws_ok[2] = ws_ok[2];
@@ -418,25 +455,42 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
   p.use_norm = eps >= 0.f ? 1 : 0;
   p.eps = eps >= 0.f ? eps : 0.f;
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+  // With the QK-norm on, |q^|, |k^| <= sqrt(D) (after the bf16 rounding at most 2^-9 more each), so
+  // every scaled score lies within sqrt(D) log2(e) (1 + 2^-8); 1 % above that is the fixed softmax
+  // reference of the persistent kernel.
+  p.ref_log2 = eps >= 0.f ? static_cast<float>(std::sqrt(static_cast<double>(D)) * 1.4426950408889634 * 1.01) : 0.f;
   p.n_qtiles = (T + swa::kTile - 1) / swa::kTile;
   if (static_cast<long long>(B) * H * p.n_qtiles >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (use_ws) {
-    SchedSlot& slot = s.slots[s.sched_next % kSchedSlots];
-    int* sched = s.d_sched + static_cast<size_t>(s.sched_next % kSchedSlots) * kSchedStride;
-    // a slot last used on another stream: this launch waits for that kernel to finish first
-    if (slot.used && slot.stream != st && cudaStreamWaitEvent(st, slot.done, 0) != cudaSuccess) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    const bool capturing = cap != cudaStreamCaptureStatusNone;
+    constexpr int kHalf = kSchedSlots / 2;
+    const int idx = capturing ? kHalf + static_cast<int>(s.capture_next % kHalf)
+                              : static_cast<int>(s.sched_next % kHalf);
+    SchedSlot& slot = s.slots[idx];
+    int* sched = s.d_sched + static_cast<size_t>(idx) * kSchedStride;
+    // an eager slot last used on another stream: this launch waits for that kernel to finish first
+    if (!capturing && slot.used && slot.stream != st && cudaStreamWaitEvent(st, slot.done, 0) != cudaSuccess) {
       cudaGetLastError();
       return ATTN_ERR_CUDA;
     }
     int rc;
     switch (D) {
-      case 32: rc = launch_ws<32>(p, s.encode_tiled, s.sm_count, sched, st); break;
-      case 64: rc = launch_ws<64>(p, s.encode_tiled, s.sm_count, sched, st); break;
-      default: rc = launch_ws<128>(p, s.encode_tiled, s.sm_count, sched, st); break;
+      case 32: rc = launch_ws<32>(p, s.maps, s.encode_tiled, s.sm_count, sched, st); break;
+      case 64: rc = launch_ws<64>(p, s.maps, s.encode_tiled, s.sm_count, sched, st); break;
+      default: rc = launch_ws<128>(p, s.maps, s.encode_tiled, s.sm_count, sched, st); break;
     }
     if (rc != ATTN_OK) return rc;
+    if (capturing) {
+      ++s.capture_next;
+      return ATTN_OK;
+    }
     if (cudaEventRecord(slot.done, st) != cudaSuccess) {
       cudaGetLastError();
       return ATTN_ERR_CUDA;
@@ -490,6 +544,8 @@ void attn_destroy(void) {
     return cudaSuccess;
   });
   for (SchedSlot& sl : s.slots) sl = SchedSlot{};
+  s.maps.clear();
+  s.capture_next = 0;
   s.d_sched = nullptr;
   s.ws_ok[0] = s.ws_ok[1] = s.ws_ok[2] = false;
   s.tables.clear();

@@ -30,6 +30,8 @@ struct AttnParams {
   int use_norm;
   float eps;
   float scale_log2;        // log2(e) / sqrt(D)
+  float ref_log2;          // > 0: a bound on every scaled score (log2 units), used as a fixed softmax
+                           // reference; 0: no bound known (QK-norm off), running maximum instead
   int n_qtiles;            // ceil(T / 128)
   int head_group;          // persistent kernel: heads per ticket group (their K/V fit in L2 together)
 };

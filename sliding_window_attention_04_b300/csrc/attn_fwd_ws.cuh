@@ -19,28 +19,33 @@
 //
 // TMEM (512 columns): kSBufs rotating 128-column S/P buffers (three; two at D = 128) and O_0, O_1
 // (D columns each). The S jobs (one per query tile and key tile, in stream order) take the buffers
-// round-robin.
+// round-robin. A softmax warpgroup reads S from its buffer and writes P (bf16, 64 columns) into the
+// buffer's upper half once that half has been read, so P needs no space of its own; the P.V MMA
+// reads P from there, and its completion frees the buffer for the S job kSBufs places later. With
+// three buffers for two query tiles (D <= 64) the S of a tile's next key tile is normally computed
+// while its softmax still works on the current one.
+//
+// Three single-thread MMA issuers each run a plain in-order loop of blocking waits: the S issuer and
+// one P.V issuer per query tile, which wakes as soon as its tile's P is written, so one tile's softmax
+// never holds up the other tile's MMAs. (Measured: the tensor pipe accepts a new tcgen05.mma only
+// about every 64 cycles, so a thread that issues stays blocked while its MMAs run; one thread issuing
+// every MMA spends those cycles serially with all of its waits and was slower than three.)
+//
 // Every wait on a phase-parity barrier is exact: the waiter is never two phases away from the
-// barrier. S-done and S-seen are per query tile (the next S of a tile is issued only after its
-// softmax has seen the previous one). P-written and P.V-done have two slots per tile, used by the
-// tile's even and odd jobs, and S job n of a tile is issued only after the tile's P.V job n - 2 has
-// completed; so P of job n + 2 cannot be written before P.V job n is issued, and a softmax that
-// waits for P.V job n - 1 (O rescale, epilogue) knows that job n - 3 has completed. Buffer-free is
-// per buffer and waited only by the S issuer, which issues the buffer's next S only after the P.V
-// that read it. A softmax writes the P of its next job while the previous P.V may still run (the
-// two sit in different buffers); only the O rescale and the epilogue wait for that P.V. A
-// softmax warpgroup reads S from its buffer and writes P (bf16, 64 columns) into the buffer's upper
-// half once that half has been read, so P needs no space of its own; the P.V MMA reads P from
-// there, and its completion frees the buffer for the S job kSBufs places later. With three
-// buffers for two query tiles (D <= 64) the S of a tile's next key tile is normally computed while
-// its softmax still works on the current one.
+// barrier. S-done, P-written and P.V-done have two slots per tile, used by the tile's even and odd
+// jobs, and S job n of a tile is issued only after the tile's P.V job n - 2 has completed: that P.V
+// needed P of job n - 2, so the S-done and P-written slots of job n - 2 have been consumed before
+// job n can complete or its P be written, and a softmax that waits for P.V job n - 1 (O rescale,
+// epilogue) knows that job n - 3 has completed. Buffer-free is per buffer and waited only by the S
+// issuer, which issues the buffer's next S only after the P.V that read it. A softmax writes the P of
+// its next job while the previous P.V may still run (the two sit in different buffers); only the O
+// rescale and the epilogue wait for that P.V. (tests/test_pipeline_model.py runs every role's waits
+// and arrivals under random interleavings and checks these claims.)
 //
-// Three single-thread MMA issuers each run a plain in-order loop of blocking waits: the S issuer
-// (S jobs in stream order) and one P.V issuer per query tile, which wakes as soon as its tile's P
-// is written, so one tile's softmax never holds up the other tile's MMAs.
-//
-// Softmax of one S tile (softmax_tile): the row max over the four 32-column blocks (reducing TMEM
-// loads), then the exponentials block by block. A row's block that the mask removes entirely
+// Softmax of one S tile. With the QK-norm on (softmax_tile_fixed) every scaled score is bounded, so
+// the exponentials use a fixed reference and need no maximum and no rescale. Otherwise (softmax_tile)
+// the row max over the four 32-column blocks comes first (reducing TMEM loads), then the exponentials
+// block by block. A row's block that the mask removes entirely
 // gets zero P without exponentials, and only a block that the mask edge cuts is masked element
 // by element; tiles without any masked entry skip the mask tests. The running max is updated lazily:
 // O and l are rescaled only when the tile max exceeds the current reference by more than
@@ -80,16 +85,15 @@ struct WsCfg {
   // barrier indices
   static constexpr int kBarQFull = 0;                     // [2] TMA -> prologue
   static constexpr int kBarQReady = 2;                    // [2] prologue -> MMA
-  static constexpr int kBarQEmpty = 4;                    // [2] slot free (epilogues, P.V issuers) -> producer
+  static constexpr int kBarQEmpty = 4;                    // [2] slot free (epilogue stores, P.V issuers) -> producer
   static constexpr int kBarUnit = 6;                      // [2] producer -> MMA, softmax (unit id)
   static constexpr int kBarKFull = 8;                     // [kStages] TMA -> prologue
   static constexpr int kBarKReady = kBarKFull + kStages;  // [kStages] prologue -> S issuer
   static constexpr int kBarVFull = kBarKReady + kStages;  // [kStages] TMA -> P.V issuers
   static constexpr int kBarKFree = kBarVFull + kStages;   // [kStages] S jobs of the step done -> producer
   static constexpr int kBarVFree = kBarKFree + kStages;   // [kStages] both P.V issuers done with V -> producer
-  static constexpr int kBarSFull = kBarVFree + kStages;   // [2] S job of tile t done -> softmax t
-  static constexpr int kBarSSeen = kBarSFull + 2;         // [2] softmax t has seen its S -> S issuer
-  static constexpr int kBarBufFree = kBarSSeen + 2;       // [kSBufs] P.V job done -> S issuer
+  static constexpr int kBarSFull = kBarVFree + kStages;   // [2 tiles][2] S job n of tile t done -> softmax t
+  static constexpr int kBarBufFree = kBarSFull + 4;       // [kSBufs] P.V job done -> S issuer
   static constexpr int kBarPFull = kBarBufFree + kSBufs;  // [2 tiles][2] softmax t wrote P of job n -> P.V issuer t
   static constexpr int kBarPVDone = kBarPFull + 4;        // [2 tiles][2] P.V job n of tile t done -> softmax, S issuer
   static constexpr int kBarFinal = kBarPVDone + 4;        // [3] MMA drain at exit (S issuer, P.V issuers)
@@ -358,29 +362,40 @@ __device__ __forceinline__ float block_max(uint32_t (&s)[32], float red, uint32_
   return fmax3(m0, m1, fmaxf(m2, m3));
 }
 
-// P = exp2(s * scale - m) of one block (masked columns hold -inf and give 0), accumulated into the
-// row sum (two packed accumulators), packed to bf16 and stored into 16 TMEM columns at tP. A block
-// with no visible column stores zeros.
-__device__ __forceinline__ void exp_store(const uint32_t (&s)[32], bool empty, uint64_t scale2, uint64_t negm2,
-                                          uint32_t tP, uint64_t& sumA, uint64_t& sumB) {
+// P = exp2(s * scale - m) of one block (masked columns hold -inf and give 0), packed to bf16 and
+// stored into 16 TMEM columns at tP; returns the block's sum of P (fp32). A block with no visible
+// column stores zeros. The exponentials stay scalar and are summed by a scalar tree: measured on one
+// warp, that is faster than summing them as packed pairs, which costs register moves and a longer
+// dependency chain.
+__device__ __forceinline__ float exp_store(const uint32_t (&s)[32], bool empty, uint64_t scale2, uint64_t negm2,
+                                           uint32_t tP) {
   uint32_t pk[16];
+  float sum = 0.f;
   if (empty) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) pk[c] = 0u;
   } else {
+    float p[32];
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), scale2, negm2);
-      const float p0 = ex2_approx(f2_lo(x2));
-      const float p1 = ex2_approx(f2_hi(x2));
-      const uint64_t pp = f2_pack(p0, p1);
-      if (c & 1) sumB = f2_add(sumB, pp);
-      else sumA = f2_add(sumA, pp);
-      pk[c] = pack_bf16x2(p0, p1);
+      p[2 * c] = ex2_approx(f2_lo(x2));
+      p[2 * c + 1] = ex2_approx(f2_hi(x2));
     }
+    float t[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) t[c] = p[2 * c] + p[2 * c + 1];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) t[c] += t[c + 8];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) t[c] += t[c + 4];
+    sum = (t[0] + t[2]) + (t[1] + t[3]);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
   }
   __syncwarp();  // the TMEM store is warp-collective; `empty` may differ between rows
   tmem_st16(tP, pk);
+  return sum;
 }
 
 // Softmax of one S tile held in TMEM at tS for this thread's row (lane): the row sees columns
@@ -419,7 +434,7 @@ __device__ __forceinline__ float softmax_tile(bool masked, uint32_t tS, int lo, 
   alpha = grow ? ex2_approx(m_used - m_new) : 1.0f;  // 0 when m_used = -inf
   const float m_use = m_new == -INFINITY ? 0.f : m_new;
   const uint64_t negm2 = f2_pack(-m_use, -m_use);
-  uint64_t sumA = 0, sumB = 0;  // pairs of fp32 zeros
+  float rowsum = 0.f;
 #pragma unroll 1
   for (int i = 0; i < 4; ++i) {
     const int bk = i < 2 ? 3 - i : i - 2;
@@ -430,10 +445,50 @@ __device__ __forceinline__ float softmax_tile(bool masked, uint32_t tS, int lo, 
     tmem_ld_wait();
     reg_fence<32>(a);
     if (v != 0xFFFFFFFFu) mask_block(a, v);
-    exp_store(a, v == 0u, scale2, negm2, tS + 64 + 16 * bk, sumA, sumB);
+    rowsum += exp_store(a, v == 0u, scale2, negm2, tS + 64 + 16 * bk);
   }
-  const uint64_t sum2 = f2_add(sumA, sumB);
-  return f2_lo(sum2) + f2_hi(sum2);
+  return rowsum;
+}
+
+// Softmax of one S tile against a fixed reference R (p.ref_log2 > 0): with the QK-norm on, every
+// q^ and k^ row has norm at most sqrt(D), so |q^ . k^| <= D and every scaled score lies in [-R, R]
+// for R just above sqrt(D) log2(e). P = exp2(s * scale - R) then lies in [2^-2R, 1]: no running
+// maximum, no max pass and no O rescale are needed, and the result is the same softmax. The four
+// 32-column blocks go in the order 3, 2, 0, 1 (P of block b is written at column 64 + 16 b, over S
+// columns already read), and the TMEM load of the next block is issued before the exponentials of
+// the current one so its latency overlaps them (two register buffers, one loop iteration per pair
+// of blocks). Returns the row sum of P.
+__device__ __forceinline__ float softmax_tile_fixed(bool masked, uint32_t tS, int lo, int hi, uint64_t scale2,
+                                                    uint64_t negr2) {
+  float rowsum = 0.f;
+  uint32_t a[32], c[32];
+  __syncwarp();
+  tmem_ld32(tS + 96, a);  // block 3
+#pragma unroll 1
+  for (int k = 0; k < 2; ++k) {
+    const int b0 = k == 0 ? 3 : 0, b1 = k == 0 ? 2 : 1;
+    tmem_ld_wait();
+    reg_fence<32>(a);
+    __syncwarp();
+    tmem_ld32(tS + 32 * b1, c);
+    {
+      const uint32_t v = masked ? block_vis(lo - 32 * b0, hi - 32 * b0) : 0xFFFFFFFFu;
+      if (v != 0xFFFFFFFFu) mask_block(a, v);
+      rowsum += exp_store(a, v == 0u, scale2, negr2, tS + 64 + 16 * b0);
+    }
+    tmem_ld_wait();
+    reg_fence<32>(c);
+    if (k == 0) {
+      __syncwarp();
+      tmem_ld32(tS, a);  // block 0, for the next iteration
+    }
+    {
+      const uint32_t v = masked ? block_vis(lo - 32 * b1, hi - 32 * b1) : 0xFFFFFFFFu;
+      if (v != 0xFFFFFFFFu) mask_block(c, v);
+      rowsum += exp_store(c, v == 0u, scale2, negr2, tS + 64 + 16 * b1);
+    }
+  }
+  return rowsum;
 }
 
 template <int D>
@@ -474,10 +529,9 @@ __global__ void __launch_bounds__(640, 1)
       mbar_init(bar(Cfg::kBarQReady + i), 8);
       mbar_init(bar(Cfg::kBarQEmpty + i), 4);
       mbar_init(bar(Cfg::kBarUnit + i), 1);
-      mbar_init(bar(Cfg::kBarSFull + i), 1);
-      mbar_init(bar(Cfg::kBarSSeen + i), 4);
     }
     for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(Cfg::kBarSFull + i), 1);
       mbar_init(bar(Cfg::kBarPFull + i), 4);
       mbar_init(bar(Cfg::kBarPVDone + i), 1);
     }
@@ -488,9 +542,7 @@ __global__ void __launch_bounds__(640, 1)
       mbar_init(bar(Cfg::kBarKFree + i), 1);
       mbar_init(bar(Cfg::kBarVFree + i), 2);
     }
-    for (int i = 0; i < NB; ++i) {
-      mbar_init(bar(Cfg::kBarBufFree + i), 1);
-    }
+    for (int i = 0; i < NB; ++i) mbar_init(bar(Cfg::kBarBufFree + i), 1);
     for (int i = 0; i < 3; ++i) mbar_init(bar(Cfg::kBarFinal + i), 1);
     for (int i = 0; i < 2; ++i) mbar_init(bar(Cfg::kBarEpi + i), 4);
     *abort_flag = 0;
@@ -655,11 +707,12 @@ __global__ void __launch_bounds__(640, 1)
             if (!g.has(t, j)) continue;
             const int b = gS % NB;
             uint32_t& sc = t == 0 ? scnt0 : scnt1;
-            // S job n of tile t waits for the tile's P.V job n - 2: when its softmax then waits for
-            // P.V job n - 1 (O rescale, epilogue), job n - 3 is known to be complete and job n + 1
-            // cannot be, so that two-slot parity wait is exact.
+            // S job n of tile t (on S-done slot n & 1) waits for the buffer's previous P.V and for the
+            // tile's P.V job n - 2. That P.V needed P of job n - 2, so the tile's softmax has consumed
+            // the S-done slot of job n - 2; and a softmax that waits for P.V job n - 1 (O rescale,
+            // epilogue) knows that job n - 3 has completed and job n + 1 cannot have: every two-slot
+            // parity wait is exact.
             if (!mbar_wait_or_abort(bar(Cfg::kBarBufFree + b), ((gS / NB) & 1) ^ 1, abort_flag) ||
-                !mbar_wait_or_abort(bar(Cfg::kBarSSeen + t), (sc & 1) ^ 1, abort_flag) ||
                 (sc >= 2 && !mbar_wait_or_abort(bar(Cfg::kBarPVDone + 2 * t + (sc & 1)), ((sc - 2) >> 1) & 1,
                                                 abort_flag))) {
               ok = false;
@@ -673,7 +726,7 @@ __global__ void __launch_bounds__(640, 1)
               const uint64_t bd = make_sdesc(ka + G::kstep_off(ks), 16, G::kSBO, G::kSwizzle);
               umma_ss(tmem + Cfg::col_buf(b), ad, bd, idesc_s, ks > 0 ? 1u : 0u);
             }
-            umma_commit(bar(Cfg::kBarSFull + t));
+            umma_commit(bar(Cfg::kBarSFull + 2 * t + (sc & 1)));
             ++sc;
             ++gS;
           }
@@ -803,6 +856,8 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t tO = tmem + lane_base + Cfg::col_o(t);
     const float scale = p.scale_log2;
     const uint64_t scale2 = f2_pack(scale, scale);
+    const bool fixed_ref = p.ref_log2 > 0.f;
+    const uint64_t negr2 = f2_pack(-p.ref_log2, -p.ref_log2);
     uint32_t n = 0;   // P tiles written so far by this warpgroup (all units)
     uint32_t gS = 0;  // global S-job index, counted over both query tiles (as the MMA issuer does)
     bool ok = true;
@@ -816,7 +871,7 @@ __global__ void __launch_bounds__(640, 1)
       const UnitGeom g = unit_geo[slot];
       const int qs = g.qs0 + kTile * t;
       const int i_row = qs + r;
-      float m_used = -INFINITY;  // reference max of this row (log2 units)
+      float m_used = fixed_ref ? p.ref_log2 : -INFINITY;  // reference max of this row (log2 units)
       float l_run = 0.f;         // sum of exp2(score - m_used)
       for (int j = g.ke_all; j >= g.kb_all; --j) {  // key steps downwards, as the MMA issuers
         const bool h0 = g.has(0, j), h1 = g.has(1, j);
@@ -834,18 +889,19 @@ __global__ void __launch_bounds__(640, 1)
           hi = p.causal ? i_row - k0 : (p.window >= 0 ? i_row + p.window - k0 : kTile);
           hi = min(hi, p.T - 1 - k0);
         }
-        // S of this tile's n-th job: the MMA issues the next one only after every warp has seen
-        // this one, so the barrier is never more than one phase ahead of this wait.
-        ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarSFull + t), n & 1, abort_flag));
+        // S of this tile's n-th job, on slot n & 1: S job n + 2 is issued only after this job's P.V,
+        // which needs this job's P, so the slot is never two phases ahead of this wait.
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait_or_abort(bar(Cfg::kBarSFull + 2 * t + (n & 1)), (n >> 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) mbar_arrive(bar(Cfg::kBarSSeen + t));
 
-        float m_new, alpha;
-        const float rowsum = softmax_tile(masked, tS, lo, hi, scale, scale2, m_used, m_new, alpha);
-        // O rescale (rare): after the tile's previous P.V job (n - 1) has completed; the next one is
-        // issued only after this job's P is announced.
-        if (j < g.ke(t) && __any_sync(0xffffffffu, alpha != 1.0f)) {  // not the unit's first job
+        float m_new = m_used, alpha = 1.0f;
+        const float rowsum = fixed_ref ? softmax_tile_fixed(masked, tS, lo, hi, scale2, negr2)
+                                       : softmax_tile(masked, tS, lo, hi, scale, scale2, m_used, m_new, alpha);
+        // O rescale (running maximum only, rare): after the tile's previous P.V job (n - 1) has
+        // completed; the next one is issued only after this job's P is announced.
+        if (!fixed_ref && j < g.ke(t) && __any_sync(0xffffffffu, alpha != 1.0f)) {  // not the unit's first job
           ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarPVDone + 2 * t + ((n - 1) & 1)),
                                                           ((n - 1) >> 1) & 1, abort_flag));
           if (!ok) break;
@@ -870,18 +926,15 @@ __global__ void __launch_bounds__(640, 1)
         ++n;
       }
       if (!ok) break;
-      // Each of the tile's four warps arrives on the epilogue barrier once per unit (after staging
-      // its rows of the output); warp 0 alone waits for the four, with the bounded wait, before the
-      // slot is released (and the output stored). Warps 1-3 cannot arrive for the next unit before
-      // warp 0 has arrived for it, so the barrier is never two phases ahead of that wait.
+      // The tile's four warps meet on the epilogue barrier once per unit (after staging their rows of
+      // the output): each arrives, then waits for the phase, with the bounded wait. Every warp waits,
+      // so none can arrive for a later unit before all four have arrived for this one.
       const bool stores = (warp & 3) == 0;
       if (!g.valid(t)) {  // this query tile lies past T
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(Cfg::kBarEpi + t));
-        if (stores) {
-          ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarEpi + t), ul & 1, abort_flag));
-          if (ok && r == 0) mbar_arrive(bar(Cfg::kBarQEmpty + slot));
-        }
+        ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarEpi + t), ul & 1, abort_flag));
+        if (ok && stores && r == 0) mbar_arrive(bar(Cfg::kBarQEmpty + slot));
         if (!ok) break;
         continue;
       }
@@ -915,15 +968,13 @@ __global__ void __launch_bounds__(640, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(Cfg::kBarEpi + t));
-      if (stores) {
-        ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarEpi + t), ul & 1, abort_flag));
-        if (ok && r == 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarEpi + t), ul & 1, abort_flag));
+      if (ok && stores && r == 0) {
 #pragma unroll
-          for (int x = 0; x < kBoxes; ++x) tma_store_4d(&maps.out, stage + x * kTile * 128, 64 * x, g.h, qs, g.b);
-          bulk_commit_group();
-          bulk_wait_group_read0();
-          mbar_arrive(bar(Cfg::kBarQEmpty + slot));
-        }
+        for (int x = 0; x < kBoxes; ++x) tma_store_4d(&maps.out, stage + x * kTile * 128, 64 * x, g.h, qs, g.b);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(bar(Cfg::kBarQEmpty + slot));
       }
       if (!ok) break;
     }
