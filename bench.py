@@ -37,14 +37,16 @@ WORKLOAD_INDEX = 2  # ANDREA-120M shape
 FALLBACK_PEAK_TFLOPS = 1800.0
 
 
+FWD_SOURCES = ("attn_api.cu", "attn_common.cuh", "attn_fwd_simple.cuh", "attn_fwd_ws.cuh", "ptx.cuh")
+
+
 def kernel_hash() -> str:
-    """Hash of the CUDA sources: ties committed ncu counters to the kernel they were taken on."""
+    """Hash of the forward's CUDA sources: ties committed ncu counters to the kernel they were taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sliding_window_attention_04_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            h.update(name.encode())
-            h.update(open(os.path.join(csrc, name), "rb").read())
+    for name in FWD_SOURCES:
+        h.update(name.encode())
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -149,13 +151,31 @@ def oracle_sample_rows(w, budget_s: float) -> int:
     return int(max(1, min(w.B, budget_s / max(per_row * len(w.layers), 1e-9))))
 
 
+L2_BYTES = 126 * 2 ** 20
+
+
+def needs_flush(w) -> bool:
+    """True when a step's inputs (each layer its own q, k, v) are less than twice the L2 capacity: the
+    timed steps are then separated by an L2 flush instead of relying on the step's own size."""
+    return len(w.layers) * 3 * 2 * w.B * w.T * w.H * w.D < 2 * L2_BYTES
+
+
 def config_dict(w):
+    step_gb = len(w.layers) * 3 * 2 * w.B * w.T * w.H * w.D / 1e9
+    if needs_flush(w):
+        l2 = (f"flushed: a step reads {step_gb * 1e3:.1f} MB of inputs, less than twice the 126 MiB L2, so "
+              f"each timed step is its own CUDA-graph replay between CUDA events, preceded (outside the "
+              f"events) by a {2 * L2_BYTES >> 20} MiB write that evicts L2")
+        launch = "each timed step one CUDA-graph replay of the step (captured, replayed once untimed)"
+    else:
+        l2 = (f"no flush: a step reads {step_gb:.2f} GB of inputs, each layer its own, more than twice the "
+              f"126 MiB L2")
+        launch = "the K timed steps as one CUDA graph (captured, replayed once untimed, then once timed)"
     return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "D": w.D,
             "layers": f"{len(w.layers)} layers, windows " + ",".join(str(l.window) for l in w.layers),
             "qk_norm_eps": w.eps, "rope_base": w.rope_base, "mask": "causal + sliding window (W=T/2 on S)",
-            "l2": f"no flush: inputs larger than L2 (a layer reads {3 * 2 * w.B * w.T * w.H * w.D / 1e6:.0f} MB, "
-                  f"a step {len(w.layers) * 3 * 2 * w.B * w.T * w.H * w.D / 1e9:.2f} GB)",
-            "launch": "the K timed steps as one CUDA graph (captured, replayed once untimed, then once timed)",
+            "l2": l2,
+            "launch": launch,
             "parallelism": "replicas (one full workload per GPU)"}
 
 
@@ -267,14 +287,10 @@ def main():
     stream = torch.cuda.current_stream(device)
     step_flops = sum(configs.attn_flops(w.B, w.H, w.T, w.D, l.window, l.causal) for l in w.layers)
 
-    def step(strm, ev=None):
+    def step(strm):
         for li, layer in enumerate(w.layers):
-            if ev is not None:
-                ev[2 * li].record(strm)
             attn.attn_fwd(dev[li][0], dev[li][1], dev[li][2], window=layer.window, causal=layer.causal,
                           rope_base=w.rope_base, eps=w.eps, out=outs[li], lse=lses[li], stream=strm)
-            if ev is not None:
-                ev[2 * li + 1].record(strm)
 
     for _ in range(args.warmup):
         step(stream)
@@ -284,35 +300,42 @@ def main():
         raise SystemExit(f"device status after warm-up: {attn.status_string(st)}")
 
     # ---- timed region: K steps, device-resident inputs ----
-    # The K steps are captured once into a CUDA graph, replayed once untimed, then once in the timed
-    # region: the host's per-call work (argument checks, ticket slot, launch) stays out of the
-    # measurement and the kernels run back to back. (Events recorded inside a graph cannot be timed,
-    # so the average launch duration is the replay's time over its launches, inter-kernel gaps
-    # included.)
+    # The steps are captured into a CUDA graph, replayed once untimed, then timed: the host's per-call
+    # work (argument checks, ticket slot, launch) stays out of the measurement and the kernels run back
+    # to back. Large steps: one graph of all K steps, one pair of events around its replay (events
+    # recorded inside a graph cannot be timed, so the average launch duration is the replay's time
+    # over its launches, inter-kernel gaps included). Small steps: one graph of one step, K replays,
+    # each between its own pair of events and after an L2-evicting write outside them.
+    flush = needs_flush(w)
     graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream(device)
     cap.wait_stream(stream)
     with torch.cuda.graph(graph, stream=cap):
-        for kstep in range(args.steps):
+        for _ in range(1 if flush else args.steps):
             step(cap)
     stream.wait_stream(cap)
     graph.replay()
+    scrub = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device) if flush else None
     torch.cuda.synchronize(device)
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps if flush else 1)]
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
     if dist:
         dist.barrier()
     torch.cuda.synchronize(device)
-    t_start.record(stream)
-    graph.replay()
-    t_end.record(stream)
+    for e0, e1 in evs:
+        if flush:
+            scrub.fill_(1)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
     torch.cuda.synchronize(device)
     if dist:
         dist.barrier()
     clocks = sampler.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
     kernel_ms = elapsed_ms  # every launch of the graph is this kernel, back to back
     st = attn.attn_device_status()
     if st != 0:
@@ -392,7 +415,8 @@ def main():
                      "peak_kind": f"{peak_kind} dense bf16 burst (sustained {peak_sustained})",
                      "kernel": "attn_fwd (one launch per layer)",
                      "achieved_basis": "algorithmic unmasked FLOPs per launch / mean launch time (CUDA events "
-                                       "around the graph replay of all timed launches, gaps included)"},
+                                       "around the graph replays of the timed launches, gaps between "
+                                       "launches of a replay included)"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": args.e2e_steps},

@@ -455,8 +455,8 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
   p.use_norm = eps >= 0.f ? 1 : 0;
   p.eps = eps >= 0.f ? eps : 0.f;
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
-  // With the QK-norm on, |q^|, |k^| <= sqrt(D) (after the bf16 rounding at most 2^-9 more each), so
-  // every scaled score lies within sqrt(D) log2(e) (1 + 2^-8); 1 % above that is the fixed softmax
+  // With the QK-norm on, |q^|, |k^| <= sqrt(D) (after the bf16 rounding at most 2^-8 more each), so
+  // every scaled score lies within sqrt(D) log2(e) (1 + 2^-8)^2; 1 % above that is the fixed softmax
   // reference of the persistent kernel.
   p.ref_log2 = eps >= 0.f ? static_cast<float>(std::sqrt(static_cast<double>(D)) * 1.4426950408889634 * 1.01) : 0.f;
   p.n_qtiles = (T + swa::kTile - 1) / swa::kTile;
