@@ -1,8 +1,8 @@
 /*
- * attn.h — C ABI of the B300 (sm_103a) attention forward library (libswa_attn.so).
+ * attn.h — C ABI of the B300 (sm_103a) attention library (libswa_attn.so).
  *
- * The one operation is the forward pass of a decoder's multi-head attention as the pages
- * define it:
+ * The operation is the forward pass of a decoder's multi-head attention as the pages define it
+ * (and, in attn_bwd, its gradient):
  *   out = softmax(Q^ K^^T / sqrt(D)) V                ("geometry_of_andrea" page,
  *                                                      "O que a Atenção Calcula",
  *                                                      "Escalonamento por sqrt(d_k)")
@@ -26,10 +26,13 @@
  *  - Return value: ATTN_OK (0) or one of the negative ATTN_ERR_* codes below. Argument errors
  *    are detected on the host before anything is launched.
  *  - Calls are asynchronous on the given stream; results are ready when the stream is.
- *  - Results are deterministic: the same inputs give bit-identical outputs.
+ *  - Results are deterministic: the same inputs give bit-identical outputs (except attn_bwd's dq,
+ *    whose per-key-tile contributions are summed in the order they arrive).
  */
 #ifndef SWA_ATTN_H
 #define SWA_ATTN_H
+
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -111,6 +114,43 @@ int attn_fwd_gqa(const void* q, const void* k, const void* v, void* out, float* 
  * register split needs). ATTN_ERR_UNSUPPORTED for other D, ATTN_ERR_NOT_INITIALIZED
  * before attn_init. Both kernels compute the same function (see attn_fwd). */
 int attn_fwd_kernel(int D);
+
+/* attn_bwd_workspace_bytes — size of the scratch buffer attn_bwd needs for this shape (0 for a
+ * non-positive size). */
+size_t attn_bwd_workspace_bytes(int B, int H, int H_kv, int T, int D);
+
+/* attn_bwd — gradients of sum(out * dout) with respect to q, k and v for the forward that
+ * attn_fwd / attn_fwd_gqa compute with the same arguments. The pages train the model (habr
+ * "Autoresearch" deep dive, train.py listing: loss.backward() through CausalSelfAttention.forward,
+ * i.e. apply_rotary_emb, norm and the attention call under bf16 autocast), so this is that
+ * forward's derivative taken where the listing's backward takes it: at the bf16 Q^, K^ (the cast
+ * passes gradients through unchanged), then back through the RMSNorm and the rotation:
+ *   P = exp(Q^ K^^T / sqrt(D) - lse) on the visible keys, dV = P^T dO, dP = dO V^T,
+ *   delta_i = dO_i . out_i, dS = P (dP - delta), dQ^ = dS K^ / sqrt(D), dK^ = dS^T Q^ / sqrt(D),
+ *   d(x r) = r dy - (r^3 / D) (x . dy) x for the norm, and the rotation by -angle for RoPE.
+ * With grouped K/V heads, dk and dv sum over the query heads sharing a K/V head.
+ *
+ *  q          [in]  bf16 [B, T, H, D], 16-byte aligned.
+ *  k, v       [in]  bf16 [B, T, H_kv, D], 16-byte aligned.
+ *  out        [in]  bf16 [B, T, H, D]: the forward's output for these inputs.
+ *  lse        [in]  fp32 [B, H, T]: the forward's log-sum-exp (natural log), 4-byte aligned.
+ *  dout       [in]  bf16 [B, T, H, D]: gradient of the loss with respect to out.
+ *  dq         [out] fp32 [B, T, H, D];  dk, dv [out] fp32 [B, T, H_kv, D]; 16-byte aligned.
+ *  workspace  [tmp] device buffer of at least attn_bwd_workspace_bytes(B, H, H_kv, T, D) bytes,
+ *                   256-byte aligned, owned by the caller; its contents on entry do not matter
+ *                   and it must not be used by other work until the stream reaches the end of
+ *                   this call.
+ *  B, H, H_kv, T, D, window, causal, rope_base, eps, stream: as attn_fwd_gqa. D = 32, 64, 128.
+ * Outputs must not overlap an input, each other or the workspace (ATTN_ERR_INVALID_ARG).
+ * Accuracy: P and dS are rounded to bf16 for their products (fp32 accumulation), delta is taken
+ * from the bf16 out; dq, dk, dv are fp32. Launches three kernels on `stream`: a prologue pass
+ * (Q^, K^, delta), the tcgen05 kernel (one CTA per batch row, K/V head and 128-key tile) and the
+ * dq pass. Returns ATTN_OK, ATTN_ERR_NOT_INITIALIZED, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED
+ * or ATTN_ERR_CUDA; a bounded wait that gives up is reported through attn_device_status.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout,
+             float* dq, float* dk, float* dv, void* workspace, size_t workspace_bytes, int B, int H, int H_kv, int T,
+             int D, int window, int causal, float rope_base, float eps, void* stream);
 
 /* attn_destroy — free the cos/sin tables and the error word; idempotent. The caller must make
  * sure no attn_fwd work is still running. After it, attn_init may be called again. */

@@ -143,13 +143,16 @@ def _abs_prologue_back(tol: np.ndarray, rx: np.ndarray, r: np.ndarray, ang, eps:
 
 
 def attn_bwd(q, k, v, dout, window: int = -1, causal: bool = True, rope_base: float = 10000.0,
-             eps: float = 1e-6, round_qk: bool = False, return_tol: bool = False):
+             eps: float = 1e-6, round_qk: bool = False, return_tol: bool = False, out_used=None, lse_used=None):
     """Gradients (dq [B, T, H, D], dk, dv [B, T, Hkv, D]) of sum(out * dout) for the float64 forward.
 
     round_qk: evaluate at the bf16-rounded q^, k^ of the forward oracle (q, k must then be bf16
     tensors or uint16 bit patterns). return_tol (needs round_qk): also (tol_dq, tol_dk, tol_dv), the
     element bounds of the bf16-operand implementation described in the module docstring, for inputs
-    out rounded to bf16 and lse rounded to fp32."""
+    out rounded to bf16 and lse rounded to fp32; or, when given, for the out ([B, T, H, D]) and lse
+    ([B, H, T], natural log) the implementation was actually handed (a forward's own results): delta
+    then moves by sum_d |dO_id| |out_used_id - out_id| and every weight of row i by the factor
+    exp(|lse_used_i - lse_i|) - 1 (first order: the difference itself)."""
     assert round_qk or not return_tol, "the bounds describe the rounded evaluation"
     if round_qk:
         from . import qk_prologue
@@ -196,14 +199,20 @@ def attn_bwd(q, k, v, dout, window: int = -1, causal: bool = True, rope_base: fl
                 aqk, ak_ = np.abs(qh), np.abs(kh)
                 lse = m + np.log(z)
                 s0 = np.where(ok, s, 0.0)
+                lse_move = 0.0 if lse_used is None else np.abs(_as_f64(lse_used)[b, h][:, None] - lse)
                 # relative error of each weight P_ij = exp(s_ij - lse_i) before its bf16 rounding
                 eta = ((aq @ ak_.T + aqk @ ak.T + aq @ ak.T) * sc      # other valid roundings of q^, k^
                        + D * f * (aqk @ ak_.T) * sc                     # fp32 accumulation of the score
-                       + 4 * f * (1.0 + np.abs(s0) + np.abs(lse)))      # lse in fp32, scaling, exp2
+                       + 4 * f * (1.0 + np.abs(s0) + np.abs(lse))       # lse in fp32, scaling, exp2
+                       + lse_move)                                      # the lse handed in
                 eta = np.where(ok, eta, 0.0)
                 tv[b, :, hk] += ((u + eta + T * f) * p).T @ np.abs(do)
                 d_dp = D * f * (np.abs(do) @ np.abs(v[b, :, hk]).T)
-                d_delta = (u + D * f) * np.sum(np.abs(do) * np.abs(o), axis=1, keepdims=True)
+                if out_used is None:
+                    d_delta = (u + D * f) * np.sum(np.abs(do) * np.abs(o), axis=1, keepdims=True)
+                else:
+                    d_delta = (np.sum(np.abs(do) * np.abs(_as_f64(out_used)[b, :, h] - o), axis=1, keepdims=True)
+                               + D * f * np.sum(np.abs(do) * np.abs(o), axis=1, keepdims=True))
                 d_ds = (u + 2 * f) * np.abs(ds) + eta * p * np.abs(dp - delta) + p * (d_dp + d_delta)
                 d_ds = np.where(ok, d_ds, 0.0)
                 t_dqh = (d_ds @ ak_ + np.abs(ds) @ ak + T * f * (np.abs(ds) @ ak_)) * sc

@@ -27,7 +27,7 @@ ATTN_ERR_SCRATCH_LIMIT = -7
 
 EXPORTED = ("attn_init", "attn_fwd", "attn_destroy", "attn_status_string", "attn_device_status",
             "attn_selftest_wait_timeout", "attn_fwd_noalloc", "attn_fwd_kernel", "attn_fwd_gqa",
-            "attn_noalloc_status", "attn_noalloc_selftest_wait_timeout")
+            "attn_noalloc_status", "attn_noalloc_selftest_wait_timeout", "attn_bwd_workspace_bytes", "attn_bwd")
 
 
 class AttnError(RuntimeError):
@@ -66,6 +66,10 @@ def _load() -> ctypes.CDLL:
     lib.attn_noalloc_status.restype = c_int
     lib.attn_noalloc_selftest_wait_timeout.argtypes = [c_void_p]
     lib.attn_noalloc_selftest_wait_timeout.restype = c_int
+    lib.attn_bwd_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int]
+    lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_bwd.argtypes = [c_void_p] * 10 + [ctypes.c_size_t] + [c_int] * 7 + [c_float, c_float, c_void_p]
+    lib.attn_bwd.restype = c_int
     return lib
 
 
@@ -211,3 +215,57 @@ def attn_fwd_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, **kwargs):
     """attn_fwd with grouped K/V heads (k, v: [B, T, H_kv, D]); the same call as attn_fwd, which
     accepts both shapes."""
     return attn_fwd(q, k, v, **kwargs)
+
+
+def attn_bwd_workspace_bytes(B: int, H: int, H_kv: int, T: int, D: int) -> int:
+    return int(lib.attn_bwd_workspace_bytes(B, H, H_kv, T, D))
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
+             dout: torch.Tensor, window: int = -1, causal: bool = True, rope_base: float = 10000.0,
+             eps: float = 1e-6, workspace: Optional[torch.Tensor] = None, dq: Optional[torch.Tensor] = None,
+             dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Gradients (dq [B, T, H, D], dk, dv [B, T, H_kv, D], fp32) of sum(out * dout) for the forward
+    attn_fwd computes with the same arguments; out and lse are that forward's results. `workspace`
+    (uint8, at least attn_bwd_workspace_bytes(...) bytes) is allocated when not given."""
+    _check_input("q", q)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, D]")
+    B, T, H, D = q.shape
+    _check_input("k", k)
+    if k.dim() != 4 or k.shape[0] != B or k.shape[1] != T or k.shape[3] != D:
+        raise ValueError(f"k has shape {tuple(k.shape)}, expected [B, T, H_kv, D] = [{B}, {T}, H_kv, {D}]")
+    H_kv = k.shape[2]
+    if H_kv < 1 or H % H_kv != 0:
+        raise ValueError(f"H = {H} is not a multiple of H_kv = {H_kv}")
+    _check_input("v", v, k.shape)
+    _check_input("out", out, q.shape)
+    _check_input("dout", dout, q.shape)
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, T) or \
+            lse.device != q.device:
+        raise ValueError("lse must be a contiguous float32 [B, H, T] tensor on q's device")
+    nbytes = attn_bwd_workspace_bytes(B, H, H_kv, T, D)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    elif workspace.dtype != torch.uint8 or not workspace.is_contiguous() or workspace.numel() < nbytes:
+        raise ValueError(f"workspace must be a contiguous uint8 tensor of at least {nbytes} bytes")
+
+    def grad(t, name, shape):
+        if t is None:
+            return torch.empty(shape, dtype=torch.float32, device=q.device)
+        if t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} must be a contiguous float32 tensor of shape {tuple(shape)}")
+        return t
+
+    dq = grad(dq, "dq", q.shape)
+    dk = grad(dk, "dk", k.shape)
+    dv = grad(dv, "dv", k.shape)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), workspace.numel(), B, H, H_kv,
+                      T, D, int(window), int(bool(causal)), float(rope_base), float(eps),
+                      ctypes.c_void_p(s.cuda_stream or None))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+    return dq, dk, dv

@@ -13,6 +13,7 @@
 #include <vector>
 
 #include "attn.h"
+#include "attn_internal.h"
 #include "attn_fwd_simple.cuh"
 #include "attn_fwd_ws.cuh"
 
@@ -310,6 +311,40 @@ int noalloc_setup(int* dev_out, unsigned char** scratch_out) {
 
 }  // namespace
 
+namespace swa_host {
+
+int locked(const std::function<int(const LibCtx&)>& f) {
+  State& s = state();
+  std::lock_guard<std::mutex> lock(s.mu);
+  if (!s.inited) return ATTN_ERR_NOT_INITIALIZED;
+  const LibCtx ctx{s.device, s.sm_count, s.d_err, s.encode_tiled};
+  return f(ctx);
+}
+
+int rope_table_locked(int D, float base, int T, const float4** table, int* table_T) {
+  State& s = state();
+  RopeTable& t = s.tables[std::make_pair(D, base)];
+  if (t.T < T) {
+    float4* fresh = nullptr;
+    if (with_device(s.device, [&] { return build_table(D, base, T, &fresh); }) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (t.ptr) s.retired.push_back(t.ptr);
+    t.ptr = fresh;
+    t.T = T;
+  }
+  *table = t.ptr;
+  *table_T = t.T;
+  return ATTN_OK;
+}
+
+CUresult encode_bf16_tile_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* map, const void* base, int B,
+                              int H, int T, int D) {
+  return encode_tile_map(encode, map, base, B, H, T, D);
+}
+
+cudaError_t on_device(int dev, const std::function<cudaError_t()>& f) { return with_device(dev, f); }
+
+}  // namespace swa_host
+
 extern "C" {
 
 int attn_init(int device) {
@@ -419,22 +454,9 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
   std::lock_guard<std::mutex> lock(s.mu);
   if (!s.inited) return ATTN_ERR_NOT_INITIALIZED;
   const bool use_ws = (D == 32 && s.ws_ok[0]) || (D == 64 && s.ws_ok[1]) || (D == 128 && s.ws_ok[2]);
-  float4* table = nullptr;
+  const float4* table = nullptr;
   int table_T = 0;
-  if (rope_base > 0.f) {
-    RopeTable& t = s.tables[std::make_pair(D, rope_base)];
-    if (t.T < T) {
-      float4* fresh = nullptr;
-      const int want = T;
-      if (with_device(s.device, [&] { return build_table(D, rope_base, want, &fresh); }) != cudaSuccess)
-        return ATTN_ERR_CUDA;
-      if (t.ptr) s.retired.push_back(t.ptr);
-      t.ptr = fresh;
-      t.T = want;
-    }
-    table = t.ptr;
-    table_T = t.T;
-  }
+  if (rope_base > 0.f && swa_host::rope_table_locked(D, rope_base, T, &table, &table_T) != ATTN_OK) return ATTN_ERR_CUDA;
 
   swa::AttnParams p{};  // every field set below or zero
   p.q = static_cast<const __nv_bfloat16*>(q);

@@ -124,3 +124,45 @@ def test_binding_rejects_cpu_tensors(binding):
     x = torch.zeros((1, 4, 1, 32), dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         binding.attn_fwd(x, x, x)
+
+
+def call_bwd(b, **kw):
+    a = dict(q=FAKE, k=FAKE + (1 << 24), v=FAKE + (2 << 24), out=FAKE + (3 << 24), lse=FAKE + (4 << 24),
+             dout=FAKE + (5 << 24), dq=FAKE + (6 << 24), dk=FAKE + (7 << 24), dv=FAKE + (8 << 24),
+             ws=FAKE + (9 << 24), ws_bytes=None, B=1, H=2, H_kv=2, T=64, D=64, window=-1, causal=1,
+             rope_base=10000.0, eps=1e-6)
+    a.update(kw)
+    if a["ws_bytes"] is None:
+        a["ws_bytes"] = b.attn_bwd_workspace_bytes(a["B"], a["H"], a["H_kv"], a["T"], a["D"])
+    return b.lib.attn_bwd(a["q"], a["k"], a["v"], a["out"], a["lse"], a["dout"], a["dq"], a["dk"], a["dv"], a["ws"],
+                          a["ws_bytes"], a["B"], a["H"], a["H_kv"], a["T"], a["D"], a["window"], a["causal"],
+                          a["rope_base"], a["eps"], None)
+
+
+def test_bwd_workspace_size(binding):
+    B, H, Hkv, T, D = 2, 4, 2, 300, 64
+    n = binding.attn_bwd_workspace_bytes(B, H, Hkv, T, D)
+    # q^ and k^ in bf16, delta and the dq^ accumulator in fp32, each part padded to 256 bytes
+    parts = [B * T * H * D * 2, B * T * Hkv * D * 2, B * H * T * 4, B * T * H * D * 4]
+    assert sum(parts) <= n <= sum(parts) + 4 * 256
+    assert n % 256 == 0
+    assert binding.attn_bwd_workspace_bytes(0, H, Hkv, T, D) == 0
+    assert binding.attn_bwd_workspace_bytes(B, H, Hkv, -1, D) == 0
+
+
+def test_bwd_host_validation_codes(binding):
+    E = binding
+    for name in ("q", "k", "v", "out", "lse", "dout", "dq", "dk", "dv", "ws"):
+        assert call_bwd(binding, **{name: 0}) == E.ATTN_ERR_INVALID_ARG, name
+    assert call_bwd(binding, dq=FAKE + (6 << 24) + 8) == E.ATTN_ERR_INVALID_ARG  # misaligned
+    assert call_bwd(binding, ws=FAKE + (9 << 24) + 16) == E.ATTN_ERR_INVALID_ARG  # workspace not 256-aligned
+    assert call_bwd(binding, ws_bytes=1024) == E.ATTN_ERR_INVALID_ARG  # workspace too small
+    assert call_bwd(binding, H_kv=3) == E.ATTN_ERR_INVALID_ARG
+    assert call_bwd(binding, causal=2) == E.ATTN_ERR_INVALID_ARG
+    assert call_bwd(binding, eps=float("inf")) == E.ATTN_ERR_INVALID_ARG
+    assert call_bwd(binding, dq=FAKE + 4096) == E.ATTN_ERR_INVALID_ARG  # dq overlaps q
+    assert call_bwd(binding, dv=FAKE + (9 << 24) + 256) == E.ATTN_ERR_INVALID_ARG  # dv overlaps the workspace
+    assert call_bwd(binding, dk=FAKE + (6 << 24) + 1024) == E.ATTN_ERR_INVALID_ARG  # dk overlaps dq
+    assert call_bwd(binding, D=48) == E.ATTN_ERR_UNSUPPORTED
+    assert call_bwd(binding) == E.ATTN_ERR_NOT_INITIALIZED
+    assert call_bwd(binding, H=4, H_kv=1, D=128, T=300, window=100) == E.ATTN_ERR_NOT_INITIALIZED

@@ -195,7 +195,7 @@ def _bf16(x):
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
 
 
-def _emulated_kernel_grads(q, k, v, dout, window, causal, base, eps, sign_p=None, sign_ds=None):
+def _emulated_kernel_grads(q, k, v, dout, window, causal, base, eps, sign_p=None, sign_ds=None, out_lse=None):
     """A bf16-operand backward in float32 numpy: P = exp(s - lse) from the fp32 lse, rounded to bf16 for
     dV; dS = P (dP - delta) with delta from the bf16 output, rounded to bf16 for dq^, dk^; the norm and
     RoPE backward in float32. sign_p / sign_ds (per b, h: [T, T] arrays of +-1) push P and dS by a full
@@ -203,6 +203,8 @@ def _emulated_kernel_grads(q, k, v, dout, window, causal, base, eps, sign_p=None
     qh_all = oracle.qk_prologue(q, base, eps, round_qk=True)
     kh_all = oracle.qk_prologue(k, base, eps, round_qk=True)
     out, lse = oracle.attn_fwd(q, k, v, window=window, causal=causal, rope_base=base, eps=eps)
+    if out_lse is not None:
+        out, lse = out_lse
     qf, kf, vf, dof = (ob._as_f64(t) for t in (q, k, v, dout))
     B, T, H, D = qf.shape
     Hkv = kf.shape[2]
@@ -258,3 +260,25 @@ def test_tolerance_covers_a_bf16_operand_backward(B, T, H, Hkv, D, window, causa
     moved = np.abs(gv - dv)[..., d0]
     assert np.all(moved <= tv[..., d0] / 2)
     assert np.max(moved / np.maximum(tv[..., d0] / 2, 1e-30)) > 0.6
+
+
+def test_tolerance_follows_the_out_and_lse_handed_in():
+    """With out_used / lse_used (a forward's own results, off the exact ones), the bounds hold for the
+    emulated backward fed with them, and they exceed the plain bounds by the move those inputs cause."""
+    B, T, H, Hkv, D, window, causal, base, eps = 1, 9, 2, 2, 8, 4, True, 10000.0, 1e-6
+    q, k, v = _inputs(B, T, H, Hkv, D, 31)
+    rng = np.random.default_rng(5)
+    dout = torch.from_numpy(rng.standard_normal(q.shape)).to(torch.bfloat16)
+    out, lse = oracle.attn_fwd(q, k, v, window=window, causal=causal, rope_base=base, eps=eps)
+    out_used = _bf16(out + 0.01 * rng.standard_normal(out.shape))
+    lse_used = (lse + 1e-4 * rng.choice([-1.0, 1.0], size=lse.shape)).astype(np.float32).astype(np.float64)
+    dq, dk, dv, tq, tk, tv = ob.attn_bwd(q, k, v, dout, window, causal, base, eps, round_qk=True, return_tol=True,
+                                         out_used=out_used, lse_used=lse_used)
+    _, _, _, tq0, tk0, tv0 = ob.attn_bwd(q, k, v, dout, window, causal, base, eps, round_qk=True, return_tol=True)
+    assert np.all(tq > tq0) and np.all(tk > tk0) and np.all(tv > tv0)
+    gq, gk, gv = _emulated_kernel_grads(q, k, v, dout, window, causal, base, eps, out_lse=(out_used, lse_used))
+    assert np.all(np.abs(gq - dq) <= tq / 2), np.max(np.abs(gq - dq) / tq)
+    assert np.all(np.abs(gk - dk) <= tk / 2), np.max(np.abs(gk - dk) / tk)
+    assert np.all(np.abs(gv - dv) <= tv / 2), np.max(np.abs(gv - dv) / tv)
+    # the plain bounds do not cover this input: the pin sees the move
+    assert (np.abs(gq - dq) > tq0 / 2).any() or (np.abs(gk - dk) > tk0 / 2).any()
