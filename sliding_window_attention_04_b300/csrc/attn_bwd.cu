@@ -9,6 +9,7 @@
 
 #include "attn.h"
 #include "attn_bwd.cuh"
+#include "attn_bwd_ws.cuh"
 #include "attn_internal.h"
 
 namespace {
@@ -17,21 +18,39 @@ constexpr size_t kAlign = 256;
 
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
-// Workspace layout: q^ bf16 [B, T, H, D] | k^ bf16 [B, T, Hkv, D] | delta fp32 [B, H, T] |
-// dq^ fp32 [B, T, H, D], each part starting on a 256-byte boundary.
+// Workspace layout: q^ bf16 [B, T, H, D] | k^ bf16 [B, T, Hkv, D] | delta fp32 [B, H, Tp] |
+// -lse log2(e) fp32 [B, H, Tp] | dq^ fp32 [B, T, H, D], each part starting on a 256-byte boundary;
+// Tp = T rounded up to a multiple of 128 (rows of whole query tiles, for 512-byte bulk copies).
 struct WsLayout {
-  size_t qh, kh, delta, dqh, total;
+  size_t qh, kh, delta, nlse, dqh, total;
 };
 
 WsLayout layout(int B, int H, int Hkv, int T, int D) {
   const size_t nq = static_cast<size_t>(B) * T * H * D, nk = static_cast<size_t>(B) * T * Hkv * D;
+  const size_t Tp = (static_cast<size_t>(T) + swa::kTile - 1) / swa::kTile * swa::kTile;
   WsLayout l;
   l.qh = 0;
   l.kh = round_up(l.qh + nq * 2);
   l.delta = round_up(l.kh + nk * 2);
-  l.dqh = round_up(l.delta + static_cast<size_t>(B) * H * T * 4);
+  l.nlse = round_up(l.delta + static_cast<size_t>(B) * H * Tp * 4);
+  l.dqh = round_up(l.nlse + static_cast<size_t>(B) * H * Tp * 4);
   l.total = round_up(l.dqh + nq * 4);
   return l;
+}
+
+// 4-D (d, h, t, b) view of an fp32 [B, T, H, D] tensor, boxes of 128 rows x 32 columns (128 bytes)
+// with the 128-byte swizzle; rows past T are dropped by stores and reductions.
+CUresult encode_f32_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* map, const void* base, int B, int H,
+                        int T, int D) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 4, static_cast<cuuint64_t>(H) * D * 4,
+                                 static_cast<cuuint64_t>(T) * H * D * 4};
+  const cuuint32_t box[4] = {32, 1, static_cast<cuuint32_t>(swa::kTile), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -46,8 +65,11 @@ int g_attr_device = -1;  // device whose kernel attributes have been set
 
 template <int D>
 cudaError_t set_bwd_attrs() {
-  return cudaFuncSetAttribute(swa::attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              swa::BwdCfg<D>::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(swa::attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       swa::BwdCfg<D>::kSmemBytes);
+  if (e != cudaSuccess || D == 128) return e;
+  return cudaFuncSetAttribute(swa::attn_bwd_ws_kernel<D == 128 ? 64 : D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              swa::BwdWsCfg<D == 128 ? 64 : D>::kSmemBytes);
 }
 
 template <int D>
@@ -56,19 +78,28 @@ int launch_bwd(const swa::BwdParams& p, const swa_host::LibCtx& ctx, cudaStream_
   if (swa_host::encode_bf16_tile_map(ctx.encode, &maps.qh, p.qh, p.B, p.H, p.T, D) != CUDA_SUCCESS ||
       swa_host::encode_bf16_tile_map(ctx.encode, &maps.kh, p.kh, p.B, p.Hkv, p.T, D) != CUDA_SUCCESS ||
       swa_host::encode_bf16_tile_map(ctx.encode, &maps.v, p.v, p.B, p.Hkv, p.T, D) != CUDA_SUCCESS ||
-      swa_host::encode_bf16_tile_map(ctx.encode, &maps.dout, p.dout, p.B, p.H, p.T, D) != CUDA_SUCCESS)
+      swa_host::encode_bf16_tile_map(ctx.encode, &maps.dout, p.dout, p.B, p.H, p.T, D) != CUDA_SUCCESS ||
+      encode_f32_map(ctx.encode, &maps.dqh, p.dqh, p.B, p.H, p.T, D) != CUDA_SUCCESS ||
+      encode_f32_map(ctx.encode, &maps.dk, p.dk, p.B, p.Hkv, p.T, D) != CUDA_SUCCESS ||
+      encode_f32_map(ctx.encode, &maps.dv, p.dv, p.B, p.Hkv, p.T, D) != CUDA_SUCCESS)
     return ATTN_ERR_CUDA;
   const long long rows = static_cast<long long>(p.B) * p.T * (p.H + p.Hkv);
-  const long long prep_blocks = (rows + 255) / 256;
+  const long long prep_blocks = (rows * 2 + 255) / 256;  // two lanes per row, 16 rows per warp
   const int prep_grid = static_cast<int>(prep_blocks < 8L * ctx.sm_count ? prep_blocks : 8L * ctx.sm_count);
   swa::attn_bwd_prep_kernel<D><<<prep_grid, 256, 0, st>>>(p);
   const long long ctas = static_cast<long long>(p.B) * p.Hkv * p.n_ktiles;
-  swa::attn_bwd_kernel<D><<<static_cast<unsigned>(ctas), swa::BwdCfg<D>::kThreads, swa::BwdCfg<D>::kSmemBytes, st>>>(
-      p, maps);
-  const long long qrows = static_cast<long long>(p.B) * p.T * p.H;
-  const long long dq_blocks = (qrows + 127) / 128;
+  if constexpr (D <= 64) {
+    // warp-specialised pipeline (producer, MMA issuer, two softmax warpgroups, dQ warpgroup)
+    swa::attn_bwd_ws_kernel<D><<<static_cast<unsigned>(ctas), swa::BwdWsCfg<D>::kThreads,
+                                 swa::BwdWsCfg<D>::kSmemBytes, st>>>(p, maps);
+  } else {
+    swa::attn_bwd_kernel<D><<<static_cast<unsigned>(ctas), swa::BwdCfg<D>::kThreads, swa::BwdCfg<D>::kSmemBytes,
+                              st>>>(p, maps);
+  }
+  const long long fin_rows = static_cast<long long>(p.B) * p.T * (p.H + p.Hkv);  // q rows, then k rows
+  const long long dq_blocks = (fin_rows * (D / 8) + 255) / 256;
   const int dq_grid = static_cast<int>(dq_blocks < 8L * ctx.sm_count ? dq_blocks : 8L * ctx.sm_count);
-  swa::attn_bwd_dq_kernel<D><<<dq_grid, 128, 0, st>>>(p);
+  swa::attn_bwd_dq_kernel<D><<<dq_grid, 256, 0, st>>>(p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -148,6 +179,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
     p.qh = reinterpret_cast<__nv_bfloat16*>(ws + l.qh);
     p.kh = reinterpret_cast<__nv_bfloat16*>(ws + l.kh);
     p.delta = reinterpret_cast<float*>(ws + l.delta);
+    p.nlse = reinterpret_cast<float*>(ws + l.nlse);
     p.dqh = reinterpret_cast<float*>(ws + l.dqh);
     p.rope = table;
     p.rope_T = table_T;
@@ -164,6 +196,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
     p.n_ktiles = (T + swa::kTile - 1) / swa::kTile;
+    p.Tp = p.n_ktiles * swa::kTile;
     if (static_cast<long long>(B) * H_kv * p.n_ktiles >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int rc = ATTN_OK;

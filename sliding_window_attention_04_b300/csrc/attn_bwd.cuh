@@ -23,9 +23,10 @@
 //      has read) and dS^T also into shared memory, and
 //        dV_j += P^T dO_i,  dK^_j += dS^T Q^_i                     (TS: A from TMEM)
 //        dQ^_i = dS K^_j                                           (SS: A = dS^T read M-major)
-//      dQ^_i is added to the fp32 workspace with vector reductions; dV_j and dK^_j stay in TMEM to
-//      the end, where dK^ goes through the norm and RoPE backward and both are written in fp32;
-//   3. dq: the norm and RoPE backward of the accumulated dq^.
+//      dQ^_i is added to the fp32 workspace; dV_j and dK^_j stay in TMEM to the end, where dv and
+//      dk^ / sqrt(D) are written in fp32 (attn_bwd_ws.cuh holds the warp-specialised form of this
+//      kernel used for D = 32 and 64; this synchronous form serves D = 128);
+//   3. finalize: the norm and RoPE backward of dq^ / sqrt(D) and, in place, of dk^ / sqrt(D).
 // dk and dv are deterministic; dq sums the key tiles' contributions in the order they arrive.
 #pragma once
 #include <cstdint>
@@ -48,7 +49,8 @@ struct BwdParams {
   float* dv;                  // [B, T, Hkv, D]
   __nv_bfloat16* qh;          // workspace: q^ [B, T, H, D]
   __nv_bfloat16* kh;          // workspace: k^ [B, T, Hkv, D]
-  float* delta;               // workspace: [B, H, T]
+  float* delta;               // workspace: delta = rowsum(dO * out), [B, H, Tp]
+  float* nlse;                // workspace: -lse log2(e), [B, H, Tp] (padding: -inf)
   float* dqh;                 // workspace: dq^ accumulator (unscaled) [B, T, H, D]
   const float4* rope;         // cos/sin table as in AttnParams, or nullptr
   int rope_T;
@@ -59,11 +61,39 @@ struct BwdParams {
   float scale_log2;  // log2(e) / sqrt(D)
   float scale;       // 1 / sqrt(D)
   int n_ktiles;      // ceil(T / 128)
+  int Tp;            // n_ktiles * 128: row length of delta / nlse (padded with -inf / 0 past T)
 };
 
 struct BwdMaps {
   CUtensorMap qh, kh, v, dout;  // 128-row tiles of one head, swizzled as the tensor core reads them
+  CUtensorMap dqh, dk, dv;      // fp32 [B, T, heads, D]: 128 rows x 32 columns per box, 128-byte swizzle
 };
+
+// 1-D bulk copy global -> shared (both 16-byte aligned, size a multiple of 16), counted on `bar`.
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Shared -> global element-wise fp32 add of one tensor-map box (rows past the tensor are dropped).
+__device__ __forceinline__ void tma_reduce_add_4d(const void* tmap, const void* src, int x, int y, int z, int w) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
+// 32 fp32 values of row `row` into a 128-row x 32-column box staged with the 128-byte swizzle
+// (16-byte unit u of row r at position u ^ (r & 7)).
+__device__ __forceinline__ void stage_row32(uint8_t* box, int row, const uint32_t (&a)[32]) {
+  uint8_t* rp = box + row * 128;
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    *reinterpret_cast<uint4*>(rp + ((u ^ (row & 7)) << 4)) = make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
+}
 
 // ------------------------------------------------------------------------------------------------
 // 1. prep
@@ -75,136 +105,200 @@ __device__ __forceinline__ void load_row_words(const __nv_bfloat16* src, uint32_
   for (int c = 0; c < D / 8; ++c) set_chunk<D>(w, c, __ldg(s4 + c));
 }
 
+// Two lanes per row, as the forward's prologue splits a row: lane e owns, in every 16-byte chunk c,
+// the 8 bytes at 8e (elements 8c + 4e .. 8c + 4e + 3). A RoPE pair (i, i + D/2) keeps i mod 8, so
+// both elements of a pair belong to one lane; the eight partial sums of squares P_m (m = d mod 8)
+// run over the chunks in increasing order, four per lane, and combine with one shuffle in the tree
+// ((P0 + P2) + (P4 + P6), (P1 + P3) + (P5 + P7)) of the forward's qk_row_transform_packed, so q^ and
+// k^ are bit-identical to the forward's.
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
+  constexpr int NC = D / 8;  // 16-byte chunks per row
+  const int e = threadIdx.x & 1;
   const long long nq = static_cast<long long>(p.B) * p.T * p.H;
   const long long nk = static_cast<long long>(p.B) * p.T * p.Hkv;
-  for (long long row = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; row < nq + nk;
-       row += static_cast<long long>(gridDim.x) * blockDim.x) {
+  // the loop runs per warp (16 rows a step) so that every lane takes part in the shuffles
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+  for (long long base = (static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * 16;
+       base < nq + nk; base += warps * 16) {
+    const long long row = base + (threadIdx.x & 31) / 2;
+    const bool valid = row < nq + nk;
     const bool isq = row < nq;
-    const long long r = isq ? row : row - nq;
+    const long long r = valid ? (isq ? row : row - nq) : 0;
     const int heads = isq ? p.H : p.Hkv;
     const int t = static_cast<int>((r / heads) % p.T);
-    uint32_t w[D / 2];
-    load_row_words<D>((isq ? p.q : p.k) + r * D, w);
-    // the forward's prologue arithmetic, operation for operation: the same bf16 q^, k^
-    qk_row_transform_packed<D>(w, t, p.rope, p.rope_T, p.use_norm, p.eps);
-    uint4* dst = reinterpret_cast<uint4*>((isq ? p.qh : p.kh) + r * D);
+    const uint2* src = reinterpret_cast<const uint2*>((isq ? p.q : p.k) + r * D) + e;
+    uint64_t x[2 * NC];  // x[2c], x[2c + 1]: elements 8c + 4e + {0, 1} and {2, 3}
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) dst[c] = get_chunk<D>(w, c);
-    if (isq) {
+    for (int c = 0; c < NC; ++c) {
+      const uint2 u = valid ? __ldg(src + 2 * c) : make_uint2(0, 0);
+      x[2 * c] = bf16x2_to_f2<D>(u.x);
+      x[2 * c + 1] = bf16x2_to_f2<D>(u.y);
+    }
+    float rs = 1.0f;
+    if (p.use_norm) {
+      uint64_t acc0 = 0, acc1 = 0;  // (P_4e, P_4e+1), (P_4e+2, P_4e+3)
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        acc0 = f2_fma(x[2 * c], x[2 * c], acc0);
+        acc1 = f2_fma(x[2 * c + 1], x[2 * c + 1], acc1);
+      }
+      const uint64_t mine = f2_add(acc0, acc1);  // e=0: (P0+P2, P1+P3); e=1: (P4+P6, P5+P7)
+      const uint64_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
+      const uint64_t tot = e == 0 ? f2_add(mine, other) : f2_add(other, mine);
+      const float ss = __fadd_rn(f2_lo(tot), f2_hi(tot));
+      const float ms = __fmul_rn(ss, 1.0f / D);
+      rs = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, p.eps)));
+    }
+    const uint64_t r2 = f2_pack(rs, rs);
+    uint2* dst = reinterpret_cast<uint2*>((isq ? p.qh : p.kh) + r * D) + e;
+    if (p.rope != nullptr) {
+      const uint64_t nr2 = f2_pack(-rs, -rs);
+      const float4* tab = p.rope + t;
+#pragma unroll
+      for (int c = 0; c < NC / 2; ++c) {
+        uint32_t wa[2], wb[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          // pairs 8c + 4e + 2q + {0, 1}: table entry 4c + 2e + q
+          const float4 tt = __ldg(tab + static_cast<size_t>(4 * c + 2 * e + q) * p.rope_T);
+          const uint64_t cos2 = f2_pack(tt.x, tt.y), sin2 = f2_pack(tt.z, tt.w);
+          const uint64_t c2 = f2_mul(cos2, r2), s2 = f2_mul(sin2, r2), sn2 = f2_mul(sin2, nr2);
+          const uint64_t x1 = x[2 * c + q], x2 = x[2 * (c + NC / 2) + q];
+          wa[q] = f2_to_bf16x2(f2_fma(x1, c2, f2_mul(x2, s2)));
+          wb[q] = f2_to_bf16x2(f2_fma(x2, c2, f2_mul(x1, sn2)));
+        }
+        if (valid) {
+          dst[2 * c] = make_uint2(wa[0], wa[1]);
+          dst[2 * (c + NC / 2)] = make_uint2(wb[0], wb[1]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+        if (valid) dst[2 * c] = make_uint2(f2_to_bf16x2(f2_mul(x[2 * c], r2)), f2_to_bf16x2(f2_mul(x[2 * c + 1], r2)));
+    }
+    // delta = rowsum(dO * out) (fp32, any order) and -lse log2(e) of q rows; the dq^ accumulator cleared
+    const bool qrow = valid && isq;
+    uint64_t acc = 0;
+    if (qrow) {
+      const uint2* o2 = reinterpret_cast<const uint2*>(p.out + r * D) + e;
+      const uint2* g2 = reinterpret_cast<const uint2*>(p.dout + r * D) + e;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        const uint2 uo = __ldg(o2 + 2 * c), ug = __ldg(g2 + 2 * c);
+        acc = f2_fma(bf16x2_to_f2<D>(ug.x), bf16x2_to_f2<D>(uo.x), acc);
+        acc = f2_fma(bf16x2_to_f2<D>(ug.y), bf16x2_to_f2<D>(uo.y), acc);
+      }
+      float4* z = reinterpret_cast<float4*>(p.dqh + r * D) + e;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) z[2 * c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float d = f2_lo(acc) + f2_hi(acc);
+    d += __shfl_xor_sync(0xffffffffu, d, 1);
+    if (qrow && e == 0) {
       const int h = static_cast<int>(r % p.H);
       const long long b = r / (static_cast<long long>(p.T) * p.H);
-      const uint4* o4 = reinterpret_cast<const uint4*>(p.out + r * D);
-      const uint4* g4 = reinterpret_cast<const uint4*>(p.dout + r * D);
-      float acc = 0.f;
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        float o[8], g[8];
-        bf16x8_to_f32(__ldg(o4 + c), o);
-        bf16x8_to_f32(__ldg(g4 + c), g);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc = fmaf(g[e], o[e], acc);
-      }
-      p.delta[(b * p.H + h) * p.T + t] = acc;
-      float4* z = reinterpret_cast<float4*>(p.dqh + r * D);
-#pragma unroll
-      for (int c = 0; c < D / 4; ++c) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      p.delta[(b * p.H + h) * p.Tp + t] = d;
+      p.nlse[(b * p.H + h) * p.Tp + t] = -__ldg(p.lse + (b * p.H + h) * p.T + t) * 1.4426950408889634f;
+    }
+  }
+  // padding of delta / nlse past T
+  const int pad = p.Tp - p.T;
+  if (pad > 0) {
+    const long long n_pad = static_cast<long long>(p.B) * p.H * pad;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n_pad;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+      const long long o = (i / pad) * p.Tp + p.T + i % pad;
+      p.delta[o] = 0.f;
+      p.nlse[o] = __int_as_float(0xff800000);
     }
   }
 }
 
 // ------------------------------------------------------------------------------------------------
-// Norm + RoPE backward of one row, in place: dy (fp32, D values, gradient of the rotated and
-// normalised row) -> dx, given the raw row x (bf16) at position pos.
+// 3. finalize: the norm and RoPE backward of dq^ / sqrt(D) (q rows, from the accumulator) and of
+//    dk^ / sqrt(D) (k rows, in place in dk)
 
+// Lanes per row as in the prep kernel (lane c: elements 8c .. 8c + 7), sums across a row's lanes by
+// shuffles, the rotation partner (chunk c xor D/16) by a shuffle.
 template <int D>
-__device__ __forceinline__ void prologue_backward_row(float (&g)[D], const __nv_bfloat16* xrow, int pos,
-                                                      const BwdParams& p) {
-  constexpr int H2 = D / 2;
-  uint32_t w[D / 2];  // the raw row, bf16 pairs (element 2k in the low half of w[k])
-  load_row_words<D>(xrow, w);
-  auto elem = [&](int d) {
-    return __uint_as_float((d & 1) ? (w[d >> 1] & 0xFFFF0000u) : (w[d >> 1] << 16));
-  };
-  const float4* tab = p.rope != nullptr ? p.rope + pos : nullptr;
-  // rotated (unnormalised) pair i: rx1 = x1 c + x2 s, rx2 = x2 c - x1 s; the table holds pairs 2m, 2m + 1
-  auto rotated = [&](int i, float cs, float sn, float& r1, float& r2) {
-    const float x1 = elem(i), x2 = elem(i + H2);
-    if (tab != nullptr) {
-      r1 = fmaf(x1, cs, x2 * sn);
-      r2 = fmaf(x2, cs, -(x1 * sn));
-    } else {
-      r1 = x1;
-      r2 = x2;
-    }
-  };
-  float r = 1.f, c3 = 0.f;
-  if (p.use_norm) {
-    float ss = 0.f, dot = 0.f;
-#pragma unroll
-    for (int m = 0; m < D / 4; ++m) {
-      const float4 t = tab != nullptr ? __ldg(tab + static_cast<size_t>(m) * p.rope_T) : make_float4(1.f, 1.f, 0.f, 0.f);
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int i = 2 * m + e;
-        float r1, r2;
-        rotated(i, e ? t.y : t.x, e ? t.w : t.z, r1, r2);
-        ss = fmaf(r1, r1, fmaf(r2, r2, ss));
-        dot = fmaf(r1, g[i], fmaf(r2, g[i + H2], dot));
-      }
-    }
-    r = 1.0f / sqrtf(ss * (1.0f / D) + p.eps);
-    c3 = r * r * r * (1.0f / D) * dot;
-  }
-#pragma unroll
-  for (int m = 0; m < D / 4; ++m) {
-    const float4 t = tab != nullptr ? __ldg(tab + static_cast<size_t>(m) * p.rope_T) : make_float4(1.f, 1.f, 0.f, 0.f);
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int i = 2 * m + e;
-      const float cs = e ? t.y : t.x, sn = e ? t.w : t.z;
-      float g1 = g[i], g2 = g[i + H2];
-      if (p.use_norm) {
-        float r1, r2;
-        rotated(i, cs, sn, r1, r2);
-        g1 = fmaf(r, g1, -(c3 * r1));
-        g2 = fmaf(r, g2, -(c3 * r2));
-      }
-      if (tab != nullptr) {
-        g[i] = fmaf(g1, cs, -(g2 * sn));
-        g[i + H2] = fmaf(g1, sn, g2 * cs);
-      } else {
-        g[i] = g1;
-        g[i + H2] = g2;
-      }
-    }
-  }
-}
-
-// ------------------------------------------------------------------------------------------------
-// 3. dq = norm/RoPE backward of dq^ / sqrt(D), one thread per (b, t, h) row
-
-template <int D>
-__global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const BwdParams p) {
+  constexpr int NC = D / 8, RPW = 32 / NC;
+  const int lane = threadIdx.x & 31;
+  const int c = lane % NC, sub = lane / NC;
   const long long nq = static_cast<long long>(p.B) * p.T * p.H;
-  for (long long r = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; r < nq;
-       r += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int t = static_cast<int>((r / p.H) % p.T);
-    float g[D];
-    const float4* a4 = reinterpret_cast<const float4*>(p.dqh + r * D);
+  const long long nk = static_cast<long long>(p.B) * p.T * p.Hkv;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+  for (long long base = (static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * RPW;
+       base < nq + nk; base += warps * RPW) {
+    const long long row = base + sub;
+    const bool valid = row < nq + nk;
+    const bool isq = row < nq;
+    const long long r = valid ? (isq ? row : row - nq) : 0;
+    const int t = valid ? static_cast<int>((r / (isq ? p.H : p.Hkv)) % p.T) : 0;
+    float* gsrc = isq ? p.dqh + r * D : p.dk + r * D;
+    float* gdst = isq ? p.dq + r * D : p.dk + r * D;
+    const float gscale = isq ? p.scale : 1.0f;  // dk^ arrives already divided by sqrt(D)
+    float g[8], x[8];
+    if (valid) {
+      const float4* a4 = reinterpret_cast<const float4*>(gsrc) + 2 * c;
+      const float4 u0 = a4[0], u1 = a4[1];
+      g[0] = u0.x; g[1] = u0.y; g[2] = u0.z; g[3] = u0.w; g[4] = u1.x; g[5] = u1.y; g[6] = u1.z; g[7] = u1.w;
+      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>((isq ? p.q : p.k) + r * D) + c), x);
+    } else {
 #pragma unroll
-    for (int c = 0; c < D / 4; ++c) {
-      const float4 u = a4[c];
-      g[4 * c] = u.x * p.scale;
-      g[4 * c + 1] = u.y * p.scale;
-      g[4 * c + 2] = u.z * p.scale;
-      g[4 * c + 3] = u.w * p.scale;
+      for (int e = 0; e < 8; ++e) g[e] = x[e] = 0.f;
     }
-    prologue_backward_row<D>(g, p.q + r * D, t, p);
-    float4* o4 = reinterpret_cast<float4*>(p.dq + r * D);
 #pragma unroll
-    for (int c = 0; c < D / 4; ++c) o4[c] = make_float4(g[4 * c], g[4 * c + 1], g[4 * c + 2], g[4 * c + 3]);
+    for (int e = 0; e < 8; ++e) g[e] *= gscale;
+    const bool first = c < NC / 2;
+    const int c1 = c % (NC / 2);
+    float cs[8], sn[8];
+    if (p.rope != nullptr) {
+      const float4* tab = p.rope + t;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 tt = __ldg(tab + static_cast<size_t>(4 * c1 + k) * p.rope_T);
+        cs[2 * k] = tt.x; cs[2 * k + 1] = tt.y; sn[2 * k] = tt.z; sn[2 * k + 1] = tt.w;
+      }
+      // x <- RoPE(x): first half x1 c + x2 s, second half x2 c - x1 s
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = __shfl_xor_sync(0xffffffffu, x[e], NC / 2);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = first ? fmaf(x[e], cs[e], o[e] * sn[e]) : fmaf(x[e], cs[e], -(o[e] * sn[e]));
+    }
+    if (p.use_norm) {
+      float ss = 0.f, dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        ss = fmaf(x[e], x[e], ss);
+        dot = fmaf(x[e], g[e], dot);
+      }
+#pragma unroll
+      for (int off = 1; off < NC; off <<= 1) {
+        ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        dot += __shfl_xor_sync(0xffffffffu, dot, off);
+      }
+      const float rr = 1.0f / sqrtf(ss * (1.0f / D) + p.eps);
+      const float c3 = rr * rr * rr * (1.0f / D) * dot;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) g[e] = fmaf(rr, g[e], -(c3 * x[e]));
+    }
+    if (p.rope != nullptr) {
+      // transpose of the rotation: dx1 = g1 c - g2 s, dx2 = g1 s + g2 c
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = __shfl_xor_sync(0xffffffffu, g[e], NC / 2);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) g[e] = first ? fmaf(g[e], cs[e], -(o[e] * sn[e])) : fmaf(o[e], sn[e], g[e] * cs[e]);
+    }
+    if (valid) {
+      float4* o4 = reinterpret_cast<float4*>(gdst) + 2 * c;
+      o4[0] = make_float4(g[0], g[1], g[2], g[3]);
+      o4[1] = make_float4(g[4], g[5], g[6], g[7]);
+    }
   }
 }
 
@@ -356,7 +450,7 @@ __global__ void __launch_bounds__(128, 1) attn_bwd_kernel(const BwdParams p, con
       const int i = i0 + tid;
       const size_t o = (static_cast<size_t>(b) * p.H + h) * p.T + i;
       s_lse[s * 128 + tid] = i < p.T ? __ldg(p.lse + o) * 1.4426950408889634f : __int_as_float(0x7f800000);
-      s_delta[s * 128 + tid] = i < p.T ? __ldg(p.delta + o) : 0.f;
+      s_delta[s * 128 + tid] = i < p.T ? __ldg(p.delta + (static_cast<size_t>(b) * p.H + h) * p.Tp + i) : 0.f;
     }
     if (n == 0 && !mbar_wait(bars + Cfg::kBarKV, 0)) ok = false;
     if (!mbar_wait(bars + Cfg::kBarLoad + s, (n / S) & 1)) ok = false;
@@ -545,7 +639,6 @@ __global__ void __launch_bounds__(128, 1) attn_bwd_kernel(const BwdParams p, con
       for (int e = 0; e < 32; ++e) g[32 * c + e] = __uint_as_float(a[e]) * p.scale;
     }
     if (j < p.T) {
-      prologue_backward_row<D>(g, p.k + row * D, j, p);
       float4* o4 = reinterpret_cast<float4*>(p.dk + row * D);
 #pragma unroll
       for (int c = 0; c < D / 4; ++c) o4[c] = make_float4(g[4 * c], g[4 * c + 1], g[4 * c + 2], g[4 * c + 3]);
