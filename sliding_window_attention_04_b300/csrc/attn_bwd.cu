@@ -19,10 +19,11 @@ constexpr size_t kAlign = 256;
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Workspace layout: q^ bf16 [B, T, H, D] | k^ bf16 [B, T, Hkv, D] | delta fp32 [B, H, Tp] |
-// -lse log2(e) fp32 [B, H, Tp] | dq^ fp32 [B, T, H, D], each part starting on a 256-byte boundary;
-// Tp = T rounded up to a multiple of 128 (rows of whole query tiles, for 512-byte bulk copies).
+// -lse log2(e) fp32 [B, H, Tp] | dq^ fp32 [B, T, H, D] | ticket counter (int), each part starting on
+// a 256-byte boundary; Tp = T rounded up to a multiple of 128 (rows of whole query tiles, for
+// 512-byte bulk copies).
 struct WsLayout {
-  size_t qh, kh, delta, nlse, dqh, total;
+  size_t qh, kh, delta, nlse, dqh, tickets, total;
 };
 
 WsLayout layout(int B, int H, int Hkv, int T, int D) {
@@ -34,7 +35,8 @@ WsLayout layout(int B, int H, int Hkv, int T, int D) {
   l.delta = round_up(l.kh + nk * 2);
   l.nlse = round_up(l.delta + static_cast<size_t>(B) * H * Tp * 4);
   l.dqh = round_up(l.nlse + static_cast<size_t>(B) * H * Tp * 4);
-  l.total = round_up(l.dqh + nq * 4);
+  l.tickets = round_up(l.dqh + nq * 4);
+  l.total = l.tickets + kAlign;
   return l;
 }
 
@@ -89,9 +91,11 @@ int launch_bwd(const swa::BwdParams& p, const swa_host::LibCtx& ctx, cudaStream_
   swa::attn_bwd_prep_kernel<D><<<prep_grid, 256, 0, st>>>(p);
   const long long ctas = static_cast<long long>(p.B) * p.Hkv * p.n_ktiles;
   if constexpr (D <= 64) {
-    // warp-specialised pipeline (producer, MMA issuer, two softmax warpgroups, dQ warpgroup)
-    swa::attn_bwd_ws_kernel<D><<<static_cast<unsigned>(ctas), swa::BwdWsCfg<D>::kThreads,
-                                 swa::BwdWsCfg<D>::kSmemBytes, st>>>(p, maps);
+    // persistent warp-specialised pipeline: one CTA per SM takes key tiles from the ticket counter
+    if (ctas >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+    const int grid = static_cast<int>(ctas < ctx.sm_count ? ctas : ctx.sm_count);
+    swa::attn_bwd_ws_kernel<D><<<grid, swa::BwdWsCfg<D>::kThreads, swa::BwdWsCfg<D>::kSmemBytes, st>>>(
+        p, maps, p.tickets, static_cast<int>(ctas));
   } else {
     swa::attn_bwd_kernel<D><<<static_cast<unsigned>(ctas), swa::BwdCfg<D>::kThreads, swa::BwdCfg<D>::kSmemBytes,
                               st>>>(p, maps);
@@ -180,6 +184,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
     p.kh = reinterpret_cast<__nv_bfloat16*>(ws + l.kh);
     p.delta = reinterpret_cast<float*>(ws + l.delta);
     p.nlse = reinterpret_cast<float*>(ws + l.nlse);
+    p.tickets = reinterpret_cast<int*>(ws + l.tickets);
     p.dqh = reinterpret_cast<float*>(ws + l.dqh);
     p.rope = table;
     p.rope_T = table_T;

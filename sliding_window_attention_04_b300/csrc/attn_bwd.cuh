@@ -52,6 +52,7 @@ struct BwdParams {
   float* delta;               // workspace: delta = rowsum(dO * out), [B, H, Tp]
   float* nlse;                // workspace: -lse log2(e), [B, H, Tp] (padding: -inf)
   float* dqh;                 // workspace: dq^ accumulator (unscaled) [B, T, H, D]
+  int* tickets;               // workspace: work counter of the persistent kernel (cleared by the prologue)
   const float4* rope;         // cos/sin table as in AttnParams, or nullptr
   int rope_T;
   int* err;
@@ -115,6 +116,7 @@ template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
   constexpr int NC = D / 8;  // 16-byte chunks per row
   const int e = threadIdx.x & 1;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.tickets = 0;
   const long long nq = static_cast<long long>(p.B) * p.T * p.H;
   const long long nk = static_cast<long long>(p.B) * p.T * p.Hkv;
   // the loop runs per warp (16 rows a step) so that every lane takes part in the shuffles
