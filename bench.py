@@ -239,6 +239,109 @@ def run_reference(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
+BWD_METRIC = "attention bwd TFLOP/s (2.5x the unmasked forward FLOPs, SSSL mix) and % of B300 dense-BF16 peak"
+
+
+def run_backward(args, w, rank, local_rank, world):
+    """The backward of every layer (dq, dk, dv from the forward's out, lse and a seeded dout), timed
+    like the forward: the K steps as CUDA-graph replays with device-resident inputs."""
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+    from sliding_window_attention_04_b300 import attn
+
+    attn.attn_init(local_rank)
+    host, dev = build_inputs(w, device)
+    douts, outs, lses, grads = [], [], [], []
+    for li, layer in enumerate(w.layers):
+        douts.append(make_qkv(w.B, w.T, w.H, w.D, seed=layer_seed(w.index, li) + 7919)[2].to(device))
+        o, l = attn.attn_fwd(dev[li][0], dev[li][1], dev[li][2], window=layer.window, causal=layer.causal,
+                             rope_base=w.rope_base, eps=w.eps)
+        outs.append(o)
+        lses.append(l)
+        grads.append(tuple(torch.empty(dev[li][0].shape, dtype=torch.float32, device=device) for _ in range(3)))
+    ws = torch.empty(attn.attn_bwd_workspace_bytes(w.B, w.H, w.H, w.T, w.D), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    step_flops = 2.5 * sum(configs.attn_flops(w.B, w.H, w.T, w.D, l.window, l.causal) for l in w.layers)
+
+    def step(strm):
+        for li, layer in enumerate(w.layers):
+            dq, dk, dv = grads[li]
+            attn.attn_bwd(dev[li][0], dev[li][1], dev[li][2], outs[li], lses[li], douts[li], window=layer.window,
+                          causal=layer.causal, rope_base=w.rope_base, eps=w.eps, workspace=ws, dq=dq, dk=dk, dv=dv,
+                          stream=strm)
+
+    for _ in range(args.warmup):
+        step(stream)
+    torch.cuda.synchronize(device)
+    st = attn.attn_device_status()
+    if st != 0:
+        raise SystemExit(f"device status after warm-up: {attn.status_string(st)}")
+    # inputs of a layer: q, k, v, out, dout (5 x B T H D bf16); the workspace is rewritten every call
+    step_in_bytes = len(w.layers) * 5 * 2 * w.B * w.T * w.H * w.D
+    flush = step_in_bytes < 2 * L2_BYTES
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(stream)
+    with torch.cuda.graph(graph, stream=cap):
+        for _ in range(1 if flush else args.steps):
+            step(cap)
+    stream.wait_stream(cap)
+    graph.replay()
+    scrub = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device) if flush else None
+    torch.cuda.synchronize(device)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps if flush else 1)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    for e0, e1 in evs:
+        if flush:
+            scrub.fill_(1)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
+    st = attn.attn_device_status()
+    if st != 0:
+        raise SystemExit(f"device status after the timed region: {attn.status_string(st)}")
+    (elapsed_ms,) = max_over_ranks([elapsed_ms], dist, device)
+    value = whole_job_tflops(step_flops, args.steps, world, elapsed_ms)
+    peak, peak_sustained, peak_kind = peaks()
+    if rank == 0:
+        cfg = config_dict(w)
+        cfg["pass"] = "backward: prologue pass, tcgen05 main kernel, finalize pass per layer"
+        cfg["l2"] = (f"flushed between steps ({step_in_bytes / 1e6:.0f} MB of inputs per step)" if flush else
+                     f"no flush: a step reads {step_in_bytes / 1e9:.2f} GB of inputs, each layer its own")
+        line = {
+            "metric": BWD_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+            "pct_of_peak": value / world / peak * 100.0,
+            "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak, "unit": "TFLOP/s",
+                         "frac": value / world / peak, "traffic": None,
+                         "peak_kind": f"{peak_kind} dense bf16 burst (sustained {peak_sustained})",
+                         "kernel": "attn_bwd (three launches per layer)",
+                         "achieved_basis": "2.5 x unmasked forward FLOPs per layer / the layer's three launches"},
+            "gpu_launches": 3 * args.steps * len(w.layers),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -253,6 +356,9 @@ def main():
     ap.add_argument("--workload", default="",
                     help="another workload by name prefix (extra measurements and captures; the bench "
                          "line is the ANDREA-120M workload)")
+    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
+                    help="bwd: time attn_bwd (dq, dk, dv from out, lse, dout) on the same layers instead of "
+                         "the forward (an extra measurement; the bench line is the forward)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -270,6 +376,9 @@ def main():
 
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    if args.which == "bwd":
+        run_backward(args, w, rank, local_rank, world)
+        return
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
     dist = None
