@@ -72,9 +72,9 @@ struct BwdWsCfg {
   static constexpr int kBarFinal = kBarDq + 1;           // [2] a tile's accumulators complete
   static constexpr int kBarAccFree = kBarFinal + 2;      // the accumulators have been read
   static constexpr int kNumBars = kBarAccFree + 1;
-  static constexpr int kTileConsumers = 1 + 8 + 4;      // issuer, softmax warps, dQ warps
-  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem address, abort flag, tile ids [2]
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  static constexpr int kTileConsumers = 1 + 8 + 1;      // issuer, softmax warps, dQ warpgroup
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem address, abort flag, tile ids [2], dQ-warps flag
+  static constexpr int kSmemBytes = kOffMisc + 32 + 1024;
   static constexpr uint32_t kColDV = 384;
   static constexpr uint32_t kColDK = 384 + D;
   static constexpr uint32_t kTmemCols = 512;
@@ -236,8 +236,9 @@ __global__ void __launch_bounds__(512, 1)
     *abort_flag = 1;
   };
   auto wait = [&](int i, uint32_t parity) { return mbar_wait_or_abort(bar(i), parity, abort_flag); };
-  // the next tile of the ticket ring (tl-th of this CTA); -1 when none is left or on timeout.
-  // Every consumer warp arrives once on the slot's empty barrier after reading it.
+  // the next tile of the ticket ring (tl-th of this CTA); -1 when none is left, -2 on timeout.
+  // The issuer and every softmax warp arrive once on the slot's empty barrier after reading it (the dQ
+  // warpgroup reads it through its leader).
   auto next_tile = [&](int tl, bool one_thread) -> int {
     const int slot = tl & 1;
     int t = -1;
@@ -443,16 +444,28 @@ __global__ void __launch_bounds__(512, 1)
     const int row = tid & 127;  // TMEM lane: query row for dQ^, key row for dV / dK^
     const bool leader = tid == 12 * 32;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    volatile int* wg_ok = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 16);
     bool ok = true;
     int N = 0;
+    volatile int* wg_tile = wg_ok + 1;
     for (int tl = 0; ok; ++tl) {
-      const int t = next_tile(tl, false);
+      if (leader) {
+        const int slot = tl & 1;
+        *wg_tile = wait(Cfg::kBarTileFull + slot, (tl >> 1) & 1) ? tile_id[slot] : -2;
+        mbar_arrive(bar(Cfg::kBarTileEmpty + slot));
+      }
+      named_barrier(1, 128);
+      const int t = *wg_tile;
       if (t == -2) { ok = false; break; }
       if (t < 0) break;
       BwdTile w;
       w.set(p, t);
       for (int n = 0; n < w.n_iter; ++n, ++N) {
-        if (!wait(Cfg::kBarDq, N & 1)) {
+        // one thread waits (bounded) and hands the outcome to the others through the warpgroup barrier,
+        // so that all four warps leave together on a timeout and no bar.sync is left waiting
+        if (leader) *wg_ok = wait(Cfg::kBarDq, N & 1) ? 1 : 0;
+        named_barrier(1, 128);
+        if (*wg_ok == 0) {
           ok = false;
           break;
         }
@@ -490,7 +503,9 @@ __global__ void __launch_bounds__(512, 1)
       // last reader, has completed with the accumulators), dK^ through registers; the accumulators
       // are released once both are read and dV's box copies have left the slots (the slots' next
       // writer is a softmax that starts after the next tile's first dV, dK^ product).
-      if (!wait(Cfg::kBarFinal + (tl & 1), (tl >> 1) & 1) || *abort_flag != 0) {
+      if (leader) *wg_ok = wait(Cfg::kBarFinal + (tl & 1), (tl >> 1) & 1) && *abort_flag == 0 ? 1 : 0;
+      named_barrier(1, 128);
+      if (*wg_ok == 0) {
         ok = false;
         break;
       }
