@@ -174,12 +174,28 @@ def attn_probs(q, k, v, b: int, h: int, window: int = -1, causal: bool = True, r
     return p
 
 
+def round_bf16_array(x) -> np.ndarray:
+    """round_bf16 for whole float64 arrays: the nearest bf16 value (ties to even), by adding the
+    rounding bias to the float64 bit pattern at the 8th significant bit. Values below the smallest
+    normal bf16 (2^-126, none in this package's data but zero) go through round_bf16."""
+    a = np.array(x, dtype=np.float64, copy=True)
+    bits = a.view(np.uint64)
+    keep = ~np.uint64((1 << 45) - 1)
+    lsb = (bits >> np.uint64(45)) & np.uint64(1)
+    out = ((bits + np.uint64((1 << 44) - 1) + lsb) & keep).view(np.float64)
+    tiny = (np.abs(a) < 2.0 ** -126) & (a != 0.0)
+    if tiny.any():
+        out[tiny] = round_bf16(a[tiny])
+    out[a == 0.0] = a[a == 0.0]
+    return out
+
+
 def _bf16_values(x) -> np.ndarray:
-    """bf16 tensor / uint16 bit patterns -> their values as float64 (exact)."""
-    return (_bits(x).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    b = _bits(x)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def value_gate(v, ve, x_gate, w_gate) -> np.ndarray:
+def value_gate(v, ve, x_gate, w_gate, return_amb: bool = False):
     """Value-embedding gate (habr "Autoresearch" deep dive, train.py listing, CausalSelfAttention.forward,
     "Value Residual (ResFormer)"): for every (b, t, K/V head h)
         gate = 2 * sigmoid(sum_c x_gate[b, t, c] * w_gate[h, c])      (c < 32 channels)
@@ -189,24 +205,53 @@ def value_gate(v, ve, x_gate, w_gate) -> np.ndarray:
     (rounded), the sum with v (rounded). Everything else is float64.
 
     v, ve: [B, T, Hkv, D]; x_gate: [B, T, C]; w_gate: [Hkv, C] (bf16 tensors or uint16 bit patterns).
-    Returns float64 [B, T, Hkv, D] holding bf16 values (the gated v the attention then reads)."""
-    import math
+    Returns float64 [B, T, Hkv, D] holding bf16 values (the gated v the attention then reads).
 
+    return_amb: also each element's ambiguity radius, the largest distance from v' to the v' of any
+    evaluation whose logit and sigmoid are single-precision evaluations within these budgets: the
+    logit accumulated over the 32 exact products in any order (each addition rounded: at most
+    32 * 2^-24 * sum |x w| from the exact sum); the sigmoid 1 / (1 + exp(-logit)) with exp within 2 ulp
+    and the addition and reciprocal correctly rounded (relative error at most 2^-21); the sum v + product
+    either exact or first rounded to single precision. Each of those values is rounded to bf16 as above;
+    the product gate * ve of two bf16 values is exact in single precision, so its rounding is unique."""
     vv, ee = _bf16_values(v), _bf16_values(ve)
     xx, ww = _bf16_values(x_gate), _bf16_values(w_gate)
     B, T, Hkv, D = vv.shape
     assert ee.shape == vv.shape and xx.shape[:2] == (B, T) and ww.shape == (Hkv, xx.shape[2])
     logit = np.empty((B, T, Hkv))
+    mag = np.empty((B, T, Hkv))
+    import math
+
     for b in range(B):
         for t in range(T):
             for h in range(Hkv):
                 # products of two bf16 values are exact in float64; fsum adds them with one rounding
-                logit[b, t, h] = math.fsum(float(a) * float(w) for a, w in zip(xx[b, t], ww[h]))
-    logit = round_bf16(logit)
-    sig = round_bf16(1.0 / (1.0 + np.exp(-logit)))
+                terms = [float(a) * float(w) for a, w in zip(xx[b, t], ww[h])]
+                logit[b, t, h] = math.fsum(terms)
+                mag[b, t, h] = math.fsum(abs(z) for z in terms)
+
+    def gated(lg):
+        sig = round_bf16_array(1.0 / (1.0 + np.exp(-lg)))
+        return sig
+
+    lb = round_bf16_array(logit)
+    sig = gated(lb)
     gate = 2.0 * sig
-    prod = round_bf16(gate[..., None] * ee)
-    return round_bf16(vv + prod)
+    prod = round_bf16_array(gate[..., None] * ee)
+    out = round_bf16_array(vv + prod)
+    if not return_amb:
+        return out
+    amb = np.zeros_like(out)
+    budget = 32.0 * 2.0 ** -24 * mag
+    for lg in (round_bf16_array(logit - budget), lb, round_bf16_array(logit + budget)):
+        s_exact = 1.0 / (1.0 + np.exp(-lg))
+        for sg in (round_bf16_array(s_exact * (1.0 - 2.0 ** -21)), round_bf16_array(s_exact),
+                   round_bf16_array(s_exact * (1.0 + 2.0 ** -21))):
+            pr = round_bf16_array((2.0 * sg)[..., None] * ee)
+            s64 = vv + pr
+            for cand in (round_bf16_array(s64), round_bf16_array(s64.astype(np.float32).astype(np.float64))):
+                amb = np.maximum(amb, np.abs(cand - out))
+    return out, amb
 
 
 from .attn_backward import attn_bwd, attn_fwd_f64  # noqa: E402  (backward oracle, NEXT-1)

@@ -597,3 +597,61 @@ def test_value_gate_matches_torch_bf16_evaluation():
     step = np.abs(logit_o - logit_t.to(torch.float64).numpy())[~same]
     assert (step <= np.abs(logit_o[~same]) * 2.0 ** -7 + 1e-30).all()  # one bf16 step at most
     np.testing.assert_array_equal(got[same], ref[same])
+
+
+def test_round_bf16_array_matches_the_scalar_routine():
+    """The vectorised rounding against the C routine: random values over many binades, exact bf16
+    values, midpoints (ties to even, both directions), values just either side of a midpoint."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal(4000) * np.exp2(rng.integers(-60, 60, 4000))
+    base = oracle.round_bf16_array(x)
+    mids = base + np.sign(base) * np.abs(base) * 2.0 ** -9 * (1 + rng.integers(0, 2, 4000))
+    cases = np.concatenate([x, base, mids, np.nextafter(mids, 0), np.nextafter(mids, np.inf), [0.0, -0.0, 1.0,
+                            1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8), 2.0 ** -126, 3e38]])
+    np.testing.assert_array_equal(oracle.round_bf16_array(cases), oracle.round_bf16(cases))
+
+
+def _f32_value_gate(v, ve, x, w, order):
+    """A single-precision evaluation of the gate: the logit summed in float32 in the given channel
+    order, sigmoid via float32 exp, every listed step rounded to bf16 (torch)."""
+    xx, ww = f64(x).astype(np.float32), f64(w).astype(np.float32)
+    logit = np.zeros(xx.shape[:2] + (ww.shape[0],), dtype=np.float32)
+    for c in order:
+        logit = (logit + xx[:, :, None, c] * ww[None, None, :, c]).astype(np.float32)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).to(torch.float32).numpy()
+    lg = bf(logit)
+    sig = bf((np.float32(1.0) / (np.float32(1.0) + np.exp(-lg).astype(np.float32))).astype(np.float32))
+    prod = bf((2.0 * sig)[..., None] * f64(ve).astype(np.float32))
+    return bf((f64(v).astype(np.float32) + prod).astype(np.float32)).astype(np.float64)
+
+
+def test_value_gate_ambiguity_radius_covers_single_precision_evaluations():
+    """Single-precision evaluations (channel orders forward, backward, random) land within the radius
+    of the exact-then-rounded gate; the radius is zero on most rows and one bf16 step where nonzero."""
+    v, ve, x, w = _gate_inputs(3, B=4, T=32, Hkv=4, D=16, w_scale=0.5)
+    got, amb = oracle.value_gate(v, ve, x, w, return_amb=True)
+    assert np.array_equal(got, oracle.value_gate(v, ve, x, w))
+    rng = np.random.default_rng(1)
+    for order in (range(32), range(31, -1, -1), rng.permutation(32)):
+        alt = _f32_value_gate(v, ve, x, w, order)
+        assert np.all(np.abs(alt - got) <= amb), np.max(np.abs(alt - got) - amb)
+    zero_rows = (amb.max(axis=-1) == 0).mean()
+    assert zero_rows > 0.8, zero_rows
+    # a one-step change of the bf16 sigmoid moves the gate by at most 2^-7 of 2 and the product by that
+    # much of |ve|, plus one bf16 step of v' for the roundings that follow
+    nz = amb > 0
+    assert np.all(amb[nz] <= np.abs(f64(ve))[nz] * 2.0 ** -6 + np.abs(got[nz]) * 2.0 ** -7)
+
+
+def test_value_gate_ambiguity_radius_catches_a_forced_tie():
+    """A row whose exact logit sits on a bf16 midpoint (1 + 2^-8, between 1 and 1 + 2^-7): the exact
+    value rounds to even (1.0) and any evaluation error may move it up; the radius must show it."""
+    B, T, Hkv, D, C = 1, 1, 1, 4, 32
+    x = torch.zeros(B, T, C, dtype=torch.bfloat16)
+    w = torch.zeros(Hkv, C, dtype=torch.bfloat16)
+    x[0, 0, 0], w[0, 0] = 1.0, 1.0                    # 1
+    x[0, 0, 1], w[0, 1] = 2.0 ** -8, 1.0              # + 2^-8: the midpoint
+    v = torch.zeros(B, T, Hkv, D, dtype=torch.bfloat16)
+    ve = torch.ones(B, T, Hkv, D, dtype=torch.bfloat16)
+    got, amb = oracle.value_gate(v, ve, x, w, return_amb=True)
+    assert (amb > 0).all()
