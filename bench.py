@@ -356,9 +356,10 @@ def main():
     ap.add_argument("--workload", default="",
                     help="another workload by name prefix (extra measurements and captures; the bench "
                          "line is the ANDREA-120M workload)")
-    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
+    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd", "fwd_ve"], default="fwd",
                     help="bwd: time attn_bwd (dq, dk, dv from out, lse, dout) on the same layers instead of "
-                         "the forward (an extra measurement; the bench line is the forward)")
+                         "the forward; fwd_ve: the forward with the value-embedding gate on every layer "
+                         "(attn_fwd_ve); extra measurements, the bench line is the forward")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -396,10 +397,28 @@ def main():
     stream = torch.cuda.current_stream(device)
     step_flops = sum(configs.attn_flops(w.B, w.H, w.T, w.D, l.window, l.causal) for l in w.layers)
 
+    gates = None
+    if args.which == "fwd_ve":
+        # per layer: value embeddings like v, the block input x [B, T, H*D] (the gate reads its first 32
+        # channels) and the gate weights [H, 32], all seeded
+        gates = []
+        for li, _ in enumerate(w.layers):
+            gen = torch.Generator().manual_seed(layer_seed(w.index, li) + 104729)
+            ve = make_qkv(w.B, w.T, w.H, w.D, seed=layer_seed(w.index, li) + 7907)[2].to(device)
+            xg = torch.randn(w.B, w.T, w.H * w.D, generator=gen).to(torch.bfloat16).to(device)
+            wg = (torch.randn(w.H, 32, generator=gen) * 0.3).to(torch.bfloat16).to(device)
+            gates.append((ve, xg, wg))
+
     def step(strm):
         for li, layer in enumerate(w.layers):
-            attn.attn_fwd(dev[li][0], dev[li][1], dev[li][2], window=layer.window, causal=layer.causal,
-                          rope_base=w.rope_base, eps=w.eps, out=outs[li], lse=lses[li], stream=strm)
+            if gates is None:
+                attn.attn_fwd(dev[li][0], dev[li][1], dev[li][2], window=layer.window, causal=layer.causal,
+                              rope_base=w.rope_base, eps=w.eps, out=outs[li], lse=lses[li], stream=strm)
+            else:
+                ve, xg, wg = gates[li]
+                attn.attn_fwd_ve(dev[li][0], dev[li][1], dev[li][2], ve, xg, wg, window=layer.window,
+                                 causal=layer.causal, rope_base=w.rope_base, eps=w.eps, out=outs[li], lse=lses[li],
+                                 stream=strm)
 
     for _ in range(args.warmup):
         step(stream)
@@ -513,11 +532,15 @@ def main():
                "sample": f"batch rows 0..{nb - 1} of every layer (all {w.H} heads, T={w.T}); "
                          f"{flops / 1e9:.2f} GFLOP in {cpu_s:.1f} s"}
 
+    cfg = config_dict(w)
+    if gates is not None:
+        cfg["pass"] = "forward with the value-embedding gate on every layer (attn_fwd_ve); e2e is the plain forward"
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if gates is None else METRIC + ", value-embedding gate on every layer",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_dict(w),
+        "config": cfg,
         "pct_of_peak": value / world / peak * 100.0,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic_per_launch(),

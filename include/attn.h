@@ -107,6 +107,29 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
 int attn_fwd_gqa(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int H_kv,
                  int T, int D, int window, int causal, float rope_base, float eps, void* stream);
 
+/* attn_fwd_ve — attn_fwd_gqa on a layer with value embeddings (habr "Autoresearch" deep dive,
+ * train.py listing, CausalSelfAttention.forward, value residual: layers with `has_ve` replace v by
+ *   v' = v + 2 * sigmoid(ve_gate(x[..., :32])) * ve
+ * where ve_gate is a bias-free linear map from the first 32 channels of the attention block's input
+ * x to one logit per K/V head). The gate is applied to every V tile in shared memory while it is
+ * staged, so v' never goes through HBM; v and ve are not modified. As in the listing every step is
+ * a bf16 value: the logit (a 32-term dot product accumulated in fp32), the sigmoid, the product with
+ * ve and the sum with v are each rounded to bf16 (a step whose exact value lies within the fp32
+ * evaluation's error of a bf16 midpoint may round either way).
+ *
+ *  ve        [in]  bf16 [B, T, H_kv, D], 16-byte aligned: the value embeddings of the layer.
+ *  x_gate    [in]  bf16, row (b, t) starts at x_gate + (b*T + t)*x_stride; its first 32 elements
+ *                  are the gate's input (e.g. x itself with x_stride = n_embd). 16-byte aligned.
+ *  x_stride        elements between consecutive rows: >= 32 and a multiple of 8.
+ *  w_gate    [in]  bf16 [H_kv, 32], 16-byte aligned: the gate's weights (ve_gate.weight).
+ *  everything else as attn_fwd_gqa. out and lse must not overlap ve.
+ * Returns ATTN_ERR_INVALID_ARG for a null ve / x_gate / w_gate or a bad stride, ATTN_ERR_UNSUPPORTED
+ * when the persistent kernel is not available for D (see attn_fwd_kernel), else as attn_fwd_gqa.
+ */
+int attn_fwd_ve(const void* q, const void* k, const void* v, const void* ve, const void* x_gate, int x_stride,
+                const void* w_gate, void* out, float* lse, int B, int H, int H_kv, int T, int D, int window, int causal,
+                float rope_base, float eps, void* stream);
+
 /* attn_fwd_kernel — which kernel attn_fwd launches for head dimension D on the initialised
  * device: 1 = the warp-specialised persistent kernel (TMA-fed K/V ring, tcgen05 MMAs into TMEM,
  * separate prologue, MMA and softmax warps; D = 32, 64 and 128), 0 = the single-warpgroup kernel

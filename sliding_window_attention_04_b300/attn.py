@@ -27,7 +27,8 @@ ATTN_ERR_SCRATCH_LIMIT = -7
 
 EXPORTED = ("attn_init", "attn_fwd", "attn_destroy", "attn_status_string", "attn_device_status",
             "attn_selftest_wait_timeout", "attn_fwd_noalloc", "attn_fwd_kernel", "attn_fwd_gqa",
-            "attn_noalloc_status", "attn_noalloc_selftest_wait_timeout", "attn_bwd_workspace_bytes", "attn_bwd")
+            "attn_noalloc_status", "attn_noalloc_selftest_wait_timeout", "attn_bwd_workspace_bytes", "attn_bwd",
+            "attn_fwd_ve")
 
 
 class AttnError(RuntimeError):
@@ -70,6 +71,8 @@ def _load() -> ctypes.CDLL:
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd.argtypes = [c_void_p] * 10 + [ctypes.c_size_t] + [c_int] * 7 + [c_float, c_float, c_void_p]
     lib.attn_bwd.restype = c_int
+    lib.attn_fwd_ve.argtypes = [c_void_p] * 5 + [c_int] + [c_void_p] * 3 + [c_int] * 7 + [c_float, c_float, c_void_p]
+    lib.attn_fwd_ve.restype = c_int
     return lib
 
 
@@ -269,3 +272,42 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tenso
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd")
     return dq, dk, dv
+
+
+def attn_fwd_ve(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ve: torch.Tensor, x_gate: torch.Tensor,
+                w_gate: torch.Tensor, window: int = -1, causal: bool = True, rope_base: float = 10000.0,
+                eps: float = 1e-6, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """attn_fwd on a layer with value embeddings: v' = v + 2 sigmoid(x_gate[..., :32] @ w_gate.T) ve applied
+    inside the kernel. ve like v ([B, T, H_kv, D] bf16); x_gate [B, T, C] bf16 with C >= 32 whose rows may be
+    strided (a slice of x), last dimension contiguous; w_gate [H_kv, 32] bf16."""
+    _check_input("q", q)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, D]")
+    B, T, H, D = q.shape
+    _check_input("k", k)
+    H_kv = k.shape[2]
+    if k.dim() != 4 or tuple(k.shape) != (B, T, H_kv, D) or H % H_kv != 0:
+        raise ValueError(f"k has shape {tuple(k.shape)}, expected [B, T, H_kv, D] with H a multiple of H_kv")
+    _check_input("v", v, k.shape)
+    _check_input("ve", ve, k.shape)
+    if not isinstance(x_gate, torch.Tensor) or x_gate.device.type != "cuda" or x_gate.dtype != torch.bfloat16:
+        raise ValueError("x_gate must be a bf16 CUDA tensor")
+    if x_gate.dim() != 3 or tuple(x_gate.shape[:2]) != (B, T) or x_gate.shape[2] < 32 or x_gate.stride(2) != 1 \
+            or x_gate.stride(0) != T * x_gate.stride(1):
+        raise ValueError("x_gate must be [B, T, C >= 32] with contiguous rows of a common stride")
+    _check_input("w_gate", w_gate, (H_kv, 32))
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check_input("out", out, q.shape)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    rc = lib.attn_fwd_ve(q.data_ptr(), k.data_ptr(), v.data_ptr(), ve.data_ptr(), x_gate.data_ptr(),
+                         x_gate.stride(1), w_gate.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, H_kv, T, D,
+                         int(window), int(bool(causal)), float(rope_base), float(eps),
+                         ctypes.c_void_p(s.cuda_stream or None))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_ve")
+    return out, lse

@@ -425,7 +425,8 @@ int attn_init(int device) {
 
 // attn_fwd and attn_fwd_gqa: q, out [B, T, H, D]; k, v [B, T, Hkv, D]; lse [B, H, T].
 static int fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int Hkv, int T,
-             int D, int window, int causal, float rope_base, float eps, void* stream) {
+             int D, int window, int causal, float rope_base, float eps, void* stream, const void* ve = nullptr,
+             const void* x_gate = nullptr, int x_stride = 0, const void* w_gate = nullptr) {
   // ---- argument checks (host only, nothing launched) ----
   if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
@@ -447,6 +448,12 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
               overlaps(lse, lse_bytes, v, kv_bytes) || overlaps(lse, lse_bytes, out, tensor_bytes)))
     return ATTN_ERR_INVALID_ARG;
   if (D != 32 && D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (ve) {
+    if (!x_gate || !w_gate || !aligned16(ve) || !aligned16(x_gate) || !aligned16(w_gate)) return ATTN_ERR_INVALID_ARG;
+    if (x_stride < 32 || x_stride % 8 != 0) return ATTN_ERR_INVALID_ARG;
+    if (overlaps(out, tensor_bytes, ve, kv_bytes)) return ATTN_ERR_INVALID_ARG;
+    if (lse && overlaps(lse, lse_bytes, ve, kv_bytes)) return ATTN_ERR_INVALID_ARG;
+  }
 
   State& s = state();
   // Held until the launch is enqueued: the ticket slot is chosen, ordered after its previous user
@@ -454,6 +461,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
   std::lock_guard<std::mutex> lock(s.mu);
   if (!s.inited) return ATTN_ERR_NOT_INITIALIZED;
   const bool use_ws = (D == 32 && s.ws_ok[0]) || (D == 64 && s.ws_ok[1]) || (D == 128 && s.ws_ok[2]);
+  if (ve && !use_ws) return ATTN_ERR_UNSUPPORTED;  // the gate lives in the persistent kernel's prologue
   const float4* table = nullptr;
   int table_T = 0;
   if (rope_base > 0.f && swa_host::rope_table_locked(D, rope_base, T, &table, &table_T) != ATTN_OK) return ATTN_ERR_CUDA;
@@ -483,6 +491,10 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
   p.ref_log2 = eps >= 0.f ? static_cast<float>(std::sqrt(static_cast<double>(D)) * 1.4426950408889634 * 1.01) : 0.f;
   p.n_qtiles = (T + swa::kTile - 1) / swa::kTile;
   if (static_cast<long long>(B) * H * p.n_qtiles >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+  p.ve = static_cast<const __nv_bfloat16*>(ve);
+  p.xg = static_cast<const __nv_bfloat16*>(x_gate);
+  p.wg = static_cast<const __nv_bfloat16*>(w_gate);
+  p.xg_stride = x_stride;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (use_ws) {
@@ -539,6 +551,14 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
 int attn_fwd_gqa(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int H_kv,
                  int T, int D, int window, int causal, float rope_base, float eps, void* stream) {
   return fwd_impl(q, k, v, out, lse, B, H, H_kv, T, D, window, causal, rope_base, eps, stream);
+}
+
+int attn_fwd_ve(const void* q, const void* k, const void* v, const void* ve, const void* x_gate, int x_stride,
+                const void* w_gate, void* out, float* lse, int B, int H, int H_kv, int T, int D, int window, int causal,
+                float rope_base, float eps, void* stream) {
+  if (!ve) return ATTN_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, out, lse, B, H, H_kv, T, D, window, causal, rope_base, eps, stream, ve, x_gate, x_stride,
+                  w_gate);
 }
 
 int attn_fwd_kernel(int D) {

@@ -98,7 +98,8 @@ struct WsCfg {
   static constexpr int kBarPVDone = kBarPFull + 4;        // [2 tiles][2] P.V job n of tile t done -> softmax, S issuer
   static constexpr int kBarFinal = kBarPVDone + 4;        // [3] MMA drain at exit (S issuer, P.V issuers)
   static constexpr int kBarEpi = kBarFinal + 3;           // [2] tile t's four softmax warps are done with the unit
-  static constexpr int kNumBars = kBarEpi + 2;
+  static constexpr int kBarVReady = kBarEpi + 2;          // [kStages] gated calls: prologue gated V -> P.V issuers
+  static constexpr int kNumBars = kBarVReady + kStages;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, unit ids, unit geometry
   static constexpr int kSmemBytes = kOffMisc + 128 + 1024;  // + alignment slack
   // TMEM columns
@@ -327,6 +328,50 @@ __device__ __forceinline__ void transform_half_row_inplace(uint8_t* tile, int ro
   }
 }
 
+// Value-embedding gate of one V row in place, split over two threads like the prologue's K rows
+// (thread h owns the 8 bytes at 8 h of every 16-byte chunk). The habr "Autoresearch" listing
+// (CausalSelfAttention.forward, value residual) computes, on bf16 tensors,
+//   v' = v + 2 * sigmoid(ve_gate(x[..., :32])) * ve
+// so every step rounds to bf16: the logit (a 32-term dot product accumulated in fp32), the sigmoid
+// (1 / (1 + exp(-logit)) with the accurate exp, a correctly rounded add and reciprocal), the product
+// with ve (exact in fp32 before its rounding), the sum with v.
+template <int D>
+__device__ __forceinline__ void gate_half_row_inplace(uint8_t* tile, int row, int h, int pos, int b, int hk,
+                                                      const AttnParams& p) {
+  const uint4* xr = reinterpret_cast<const uint4*>(p.xg + (static_cast<size_t>(b) * p.T + pos) * p.xg_stride);
+  const uint4* wr = reinterpret_cast<const uint4*>(p.wg + static_cast<size_t>(hk) * 32);
+  float acc = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float xv[8], wv[8];
+    bf16x8_to_f32(__ldg(xr + c), xv);
+    bf16x8_to_f32(__ldg(wr + c), wv);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc = fmaf(xv[e], wv[e], acc);
+  }
+  const float lg = __bfloat162float(__float2bfloat16_rn(acc));
+  const float sg = __bfloat162float(__float2bfloat16_rn(__frcp_rn(__fadd_rn(1.0f, expf(-lg)))));
+  const float gate = 2.0f * sg;
+  const uint2* er = reinterpret_cast<const uint2*>(p.ve + ((static_cast<size_t>(b) * p.T + pos) * p.Hkv + hk) * D) + h;
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) {
+    uint2* w = reinterpret_cast<uint2*>(tile + tile_off<D>(row, c) + 8 * h);
+    const uint2 u = *w;
+    const uint2 ev = __ldg(er + 2 * c);
+    const uint32_t in[2] = {u.x, u.y}, ew[2] = {ev.x, ev.y};
+    uint32_t o[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float v0 = __uint_as_float(in[k] << 16), v1 = __uint_as_float(in[k] & 0xFFFF0000u);
+      const float e0 = __uint_as_float(ew[k] << 16), e1 = __uint_as_float(ew[k] & 0xFFFF0000u);
+      const float p0 = __bfloat162float(__float2bfloat16_rn(gate * e0));
+      const float p1 = __bfloat162float(__float2bfloat16_rn(gate * e1));
+      o[k] = pack_bf16x2(__fadd_rn(v0, p0), __fadd_rn(v1, p1));
+    }
+    *w = make_uint2(o[0], o[1]);
+  }
+}
+
 struct WsMaps {
   CUtensorMap q, k, v, out;  // 4-D (D, H, T, B) views, box (D, 1, 128, 1), swizzled
 };
@@ -545,6 +590,7 @@ __global__ void __launch_bounds__(640, 1)
     for (int i = 0; i < NB; ++i) mbar_init(bar(Cfg::kBarBufFree + i), 1);
     for (int i = 0; i < 3; ++i) mbar_init(bar(Cfg::kBarFinal + i), 1);
     for (int i = 0; i < 2; ++i) mbar_init(bar(Cfg::kBarEpi + i), 4);
+    for (int i = 0; i < S; ++i) mbar_init(bar(Cfg::kBarVReady + i), 8);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -768,7 +814,12 @@ __global__ void __launch_bounds__(640, 1)
           const bool release = i < n_st - g.r_out;  // not kept for the next unit
           // Every load's V phase is observed (and released, at its last use) by both issuers, active
           // or not, so the stage's barriers never run two phases ahead of either of them.
-          if (!mbar_wait_or_abort(bar(Cfg::kBarVFull + st), (pos / S) & 1, abort_flag)) { ok = false; break; }
+          // a gated call's V tile is read once the prologue has applied the gate to it
+          if (!mbar_wait_or_abort(bar((p.ve != nullptr ? Cfg::kBarVReady : Cfg::kBarVFull) + st), (pos / S) & 1,
+                                  abort_flag)) {
+            ok = false;
+            break;
+          }
           if (!(t == 0 ? h0 : h1)) {
             if (release) mbar_arrive(bar(Cfg::kBarVFree + st));
             continue;
@@ -842,6 +893,15 @@ __global__ void __launch_bounds__(640, 1)
           if (jb == 1 && lane == 0) mbar_arrive(bar(Cfg::kBarQReady + slot));
         } else {
           if (lane == 0) mbar_arrive(bar(Cfg::kBarKReady + st));
+          if (p.ve != nullptr) {
+            // the value-embedding gate on the same step's V tile, in place
+            ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarVFull + st), (kcnt / S) & 1, abort_flag));
+            if (!ok) break;
+            if (pos < p.T) gate_half_row_inplace<D>(v_tile(st), r, h, pos, g.b, g.hk, p);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(Cfg::kBarVReady + st));
+          }
           ++kcnt;
         }
       }
