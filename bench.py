@@ -407,7 +407,8 @@ def main():
             ve = make_qkv(w.B, w.T, w.H, w.D, seed=layer_seed(w.index, li) + 7907)[2].to(device)
             xg = torch.randn(w.B, w.T, w.H * w.D, generator=gen).to(torch.bfloat16).to(device)
             wg = (torch.randn(w.H, 32, generator=gen) * 0.3).to(torch.bfloat16).to(device)
-            gates.append((ve, xg, wg))
+            gws = torch.empty(attn.attn_fwd_ve_workspace_bytes(w.B, w.H, w.T), dtype=torch.uint8, device=device)
+            gates.append((ve, xg, wg, gws))
 
     def step(strm):
         for li, layer in enumerate(w.layers):
@@ -415,10 +416,10 @@ def main():
                 attn.attn_fwd(dev[li][0], dev[li][1], dev[li][2], window=layer.window, causal=layer.causal,
                               rope_base=w.rope_base, eps=w.eps, out=outs[li], lse=lses[li], stream=strm)
             else:
-                ve, xg, wg = gates[li]
+                ve, xg, wg, gws = gates[li]
                 attn.attn_fwd_ve(dev[li][0], dev[li][1], dev[li][2], ve, xg, wg, window=layer.window,
                                  causal=layer.causal, rope_base=w.rope_base, eps=w.eps, out=outs[li], lse=lses[li],
-                                 stream=strm)
+                                 workspace=gws, stream=strm)
 
     for _ in range(args.warmup):
         step(stream)
@@ -470,7 +471,7 @@ def main():
         raise SystemExit(f"device status after the timed region: {attn.status_string(st)}")
     elapsed_ms, kernel_ms = max_over_ranks([elapsed_ms, kernel_ms], dist, device)
 
-    n_launch = args.steps * len(w.layers)
+    n_launch = args.steps * len(w.layers) * (2 if gates is not None else 1)
     value = whole_job_tflops(step_flops, args.steps, world, elapsed_ms)
     achieved = step_flops * args.steps / (kernel_ms / 1e3) / 1e12  # per GPU, kernel time only
     peak, peak_sustained, peak_kind = peaks()
@@ -534,7 +535,8 @@ def main():
 
     cfg = config_dict(w)
     if gates is not None:
-        cfg["pass"] = "forward with the value-embedding gate on every layer (attn_fwd_ve); e2e is the plain forward"
+        cfg["pass"] = ("forward with the value-embedding gate on every layer (attn_fwd_ve: gate-factor pass + "
+                       "attention kernel, two launches per layer); e2e is the plain forward")
     line = {
         "metric": METRIC if gates is None else METRIC + ", value-embedding gate on every layer",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

@@ -111,8 +111,9 @@ int attn_fwd_gqa(const void* q, const void* k, const void* v, void* out, float* 
  * train.py listing, CausalSelfAttention.forward, value residual: layers with `has_ve` replace v by
  *   v' = v + 2 * sigmoid(ve_gate(x[..., :32])) * ve
  * where ve_gate is a bias-free linear map from the first 32 channels of the attention block's input
- * x to one logit per K/V head). The gate is applied to every V tile in shared memory while it is
- * staged, so v' never goes through HBM; v and ve are not modified. As in the listing every step is
+ * x to one logit per K/V head). A short pass first writes the gate factor 2 * sigmoid(...) of every
+ * (b, t, K/V head) to `workspace`; the attention kernel then applies v + factor * ve to every V tile
+ * in shared memory while it is staged, so v' never goes through HBM; v and ve are not modified. As in the listing every step is
  * a bf16 value: the logit (a 32-term dot product accumulated in fp32), the sigmoid, the product with
  * ve and the sum with v are each rounded to bf16 (a step whose exact value lies within the fp32
  * evaluation's error of a bf16 midpoint may round either way).
@@ -122,13 +123,19 @@ int attn_fwd_gqa(const void* q, const void* k, const void* v, void* out, float* 
  *                  are the gate's input (e.g. x itself with x_stride = n_embd). 16-byte aligned.
  *  x_stride        elements between consecutive rows: >= 32 and a multiple of 8.
  *  w_gate    [in]  bf16 [H_kv, 32], 16-byte aligned: the gate's weights (ve_gate.weight).
- *  everything else as attn_fwd_gqa. out and lse must not overlap ve.
+ *  workspace [tmp] device buffer of at least attn_fwd_ve_workspace_bytes(B, H_kv, T) bytes, 16-byte
+ *                  aligned, caller-owned, not used by other work until the stream reaches the end of
+ *                  this call; its contents on entry do not matter.
+ *  everything else as attn_fwd_gqa. out, lse and workspace must not overlap ve or each other.
  * Returns ATTN_ERR_INVALID_ARG for a null ve / x_gate / w_gate or a bad stride, ATTN_ERR_UNSUPPORTED
  * when the persistent kernel is not available for D (see attn_fwd_kernel), else as attn_fwd_gqa.
  */
 int attn_fwd_ve(const void* q, const void* k, const void* v, const void* ve, const void* x_gate, int x_stride,
-                const void* w_gate, void* out, float* lse, int B, int H, int H_kv, int T, int D, int window, int causal,
-                float rope_base, float eps, void* stream);
+                const void* w_gate, void* out, float* lse, void* workspace, size_t workspace_bytes, int B, int H,
+                int H_kv, int T, int D, int window, int causal, float rope_base, float eps, void* stream);
+
+/* attn_fwd_ve_workspace_bytes — size of attn_fwd_ve's workspace (0 for a non-positive size). */
+size_t attn_fwd_ve_workspace_bytes(int B, int H_kv, int T);
 
 /* attn_fwd_kernel — which kernel attn_fwd launches for head dimension D on the initialised
  * device: 1 = the warp-specialised persistent kernel (TMA-fed K/V ring, tcgen05 MMAs into TMEM,

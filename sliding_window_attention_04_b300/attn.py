@@ -28,7 +28,7 @@ ATTN_ERR_SCRATCH_LIMIT = -7
 EXPORTED = ("attn_init", "attn_fwd", "attn_destroy", "attn_status_string", "attn_device_status",
             "attn_selftest_wait_timeout", "attn_fwd_noalloc", "attn_fwd_kernel", "attn_fwd_gqa",
             "attn_noalloc_status", "attn_noalloc_selftest_wait_timeout", "attn_bwd_workspace_bytes", "attn_bwd",
-            "attn_fwd_ve")
+            "attn_fwd_ve", "attn_fwd_ve_workspace_bytes")
 
 
 class AttnError(RuntimeError):
@@ -71,8 +71,11 @@ def _load() -> ctypes.CDLL:
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd.argtypes = [c_void_p] * 10 + [ctypes.c_size_t] + [c_int] * 7 + [c_float, c_float, c_void_p]
     lib.attn_bwd.restype = c_int
-    lib.attn_fwd_ve.argtypes = [c_void_p] * 5 + [c_int] + [c_void_p] * 3 + [c_int] * 7 + [c_float, c_float, c_void_p]
+    lib.attn_fwd_ve.argtypes = ([c_void_p] * 5 + [c_int] + [c_void_p] * 4 + [ctypes.c_size_t] + [c_int] * 7 +
+                                [c_float, c_float, c_void_p])
     lib.attn_fwd_ve.restype = c_int
+    lib.attn_fwd_ve_workspace_bytes.argtypes = [c_int, c_int, c_int]
+    lib.attn_fwd_ve_workspace_bytes.restype = ctypes.c_size_t
     return lib
 
 
@@ -277,6 +280,7 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tenso
 def attn_fwd_ve(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ve: torch.Tensor, x_gate: torch.Tensor,
                 w_gate: torch.Tensor, window: int = -1, causal: bool = True, rope_base: float = 10000.0,
                 eps: float = 1e-6, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                workspace: Optional[torch.Tensor] = None,
                 stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """attn_fwd on a layer with value embeddings: v' = v + 2 sigmoid(x_gate[..., :32] @ w_gate.T) ve applied
     inside the kernel. ve like v ([B, T, H_kv, D] bf16); x_gate [B, T, C] bf16 with C >= 32 whose rows may be
@@ -303,11 +307,21 @@ def attn_fwd_ve(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ve: torch.Ten
         _check_input("out", out, q.shape)
     if lse is None:
         lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    nbytes = int(lib.attn_fwd_ve_workspace_bytes(B, H_kv, T))
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    elif workspace.dtype != torch.uint8 or not workspace.is_contiguous() or workspace.numel() < nbytes:
+        raise ValueError(f"workspace must be a contiguous uint8 tensor of at least {nbytes} bytes")
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     rc = lib.attn_fwd_ve(q.data_ptr(), k.data_ptr(), v.data_ptr(), ve.data_ptr(), x_gate.data_ptr(),
-                         x_gate.stride(1), w_gate.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, H_kv, T, D,
+                         x_gate.stride(1), w_gate.data_ptr(), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+                         workspace.numel(), B, H, H_kv, T, D,
                          int(window), int(bool(causal)), float(rope_base), float(eps),
                          ctypes.c_void_p(s.cuda_stream or None))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_ve")
     return out, lse
+
+
+def attn_fwd_ve_workspace_bytes(B: int, H_kv: int, T: int) -> int:
+    return int(lib.attn_fwd_ve_workspace_bytes(B, H_kv, T))

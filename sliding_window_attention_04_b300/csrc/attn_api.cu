@@ -426,7 +426,8 @@ int attn_init(int device) {
 // attn_fwd and attn_fwd_gqa: q, out [B, T, H, D]; k, v [B, T, Hkv, D]; lse [B, H, T].
 static int fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int Hkv, int T,
              int D, int window, int causal, float rope_base, float eps, void* stream, const void* ve = nullptr,
-             const void* x_gate = nullptr, int x_stride = 0, const void* w_gate = nullptr) {
+             const void* x_gate = nullptr, int x_stride = 0, const void* w_gate = nullptr, float* gate_ws = nullptr,
+             size_t gate_ws_bytes = 0) {
   // ---- argument checks (host only, nothing launched) ----
   if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
@@ -452,6 +453,11 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
     if (!x_gate || !w_gate || !aligned16(ve) || !aligned16(x_gate) || !aligned16(w_gate)) return ATTN_ERR_INVALID_ARG;
     if (x_stride < 32 || x_stride % 8 != 0) return ATTN_ERR_INVALID_ARG;
     if (overlaps(out, tensor_bytes, ve, kv_bytes)) return ATTN_ERR_INVALID_ARG;
+    const size_t gate_bytes = static_cast<size_t>(B) * T * Hkv * 4;
+    if (!gate_ws || (reinterpret_cast<uintptr_t>(gate_ws) & 15u) || gate_ws_bytes < gate_bytes)
+      return ATTN_ERR_INVALID_ARG;
+    if (overlaps(gate_ws, gate_bytes, out, tensor_bytes) || (lse && overlaps(gate_ws, gate_bytes, lse, lse_bytes)))
+      return ATTN_ERR_INVALID_ARG;
     if (lse && overlaps(lse, lse_bytes, ve, kv_bytes)) return ATTN_ERR_INVALID_ARG;
   }
 
@@ -495,8 +501,17 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
   p.xg = static_cast<const __nv_bfloat16*>(x_gate);
   p.wg = static_cast<const __nv_bfloat16*>(w_gate);
   p.xg_stride = x_stride;
+  p.gate = gate_ws;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (ve) {
+    // the gate factors of every (b, t, K/V head), once, before the attention kernel reads them
+    const long long rows = static_cast<long long>(B) * T;
+    const long long blocks = (rows + 255) / 256;
+    const int grid = static_cast<int>(blocks < 8LL * s.sm_count ? blocks : 8LL * s.sm_count);
+    swa::ve_gate_kernel<<<grid, 256, 0, st>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  }
   if (use_ws) {
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) {
@@ -553,12 +568,17 @@ int attn_fwd_gqa(const void* q, const void* k, const void* v, void* out, float* 
   return fwd_impl(q, k, v, out, lse, B, H, H_kv, T, D, window, causal, rope_base, eps, stream);
 }
 
+size_t attn_fwd_ve_workspace_bytes(int B, int H_kv, int T) {
+  if (B < 1 || H_kv < 1 || T < 1) return 0;
+  return (static_cast<size_t>(B) * T * H_kv * 4 + 255) / 256 * 256;
+}
+
 int attn_fwd_ve(const void* q, const void* k, const void* v, const void* ve, const void* x_gate, int x_stride,
-                const void* w_gate, void* out, float* lse, int B, int H, int H_kv, int T, int D, int window, int causal,
-                float rope_base, float eps, void* stream) {
+                const void* w_gate, void* out, float* lse, void* workspace, size_t workspace_bytes, int B, int H,
+                int H_kv, int T, int D, int window, int causal, float rope_base, float eps, void* stream) {
   if (!ve) return ATTN_ERR_INVALID_ARG;
   return fwd_impl(q, k, v, out, lse, B, H, H_kv, T, D, window, causal, rope_base, eps, stream, ve, x_gate, x_stride,
-                  w_gate);
+                  w_gate, static_cast<float*>(workspace), workspace_bytes);
 }
 
 int attn_fwd_kernel(int D) {

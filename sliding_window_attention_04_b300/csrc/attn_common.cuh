@@ -34,12 +34,15 @@ struct AttnParams {
                            // reference; 0: no bound known (QK-norm off), running maximum instead
   int n_qtiles;            // ceil(T / 128)
   int head_group;          // persistent kernel: heads per ticket group (their K/V fit in L2 together)
-  // value-embedding gate (nullptr ve: none): v <- v + 2 sigmoid(xg[b, t, 0:32] . wg[hk, 0:32]) ve
+  // value-embedding gate (nullptr ve: none): v <- v + gate[b, t, hk] ve, where the gate factor
+  // 2 sigmoid(xg[b, t, 0:32] . wg[hk, 0:32]) is computed once per (b, t, hk) by ve_gate_kernel
   const __nv_bfloat16* ve;  // [B, T, Hkv, D]
   const __nv_bfloat16* xg;  // rows of xg_stride elements, [B, T, xg_stride]; the first 32 are used
   const __nv_bfloat16* wg;  // [Hkv, 32]
   int xg_stride;
+  float* gate;              // [B, T, Hkv] gate factors (caller's workspace)
 };
+
 
 // Byte offset of 16-byte chunk `chunk` (8 bf16 along D) of row `row` inside a 128-row operand
 // tile stored the way the tensor core reads a K-major (row = M or N index, D contiguous) bf16

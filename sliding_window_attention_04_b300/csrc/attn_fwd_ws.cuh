@@ -328,37 +328,55 @@ __device__ __forceinline__ void transform_half_row_inplace(uint8_t* tile, int ro
   }
 }
 
+// The gate factor of the value-embedding gate for every (b, t, K/V head), one thread per (b, t):
+// 2 * bf16(sigmoid(bf16(x[b, t, 0:32] . w[hk, 0:32]))). The habr "Autoresearch" listing computes it on
+// bf16 tensors (CausalSelfAttention.forward, value residual), so the logit (a 32-term dot product
+// accumulated in fp32) and the sigmoid (1 / (1 + exp(-logit)) with the accurate exp and a correctly
+// rounded add and reciprocal) are each rounded to bf16; the factor 2 is exact.
+__global__ void __launch_bounds__(256) ve_gate_kernel(AttnParams p) {
+  const long long n = static_cast<long long>(p.B) * p.T;
+  for (long long r = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; r < n;
+       r += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const uint4* xr = reinterpret_cast<const uint4*>(p.xg + r * p.xg_stride);
+    float xv[32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) bf16x8_to_f32(__ldg(xr + c), xv + 8 * c);
+    for (int hk = 0; hk < p.Hkv; ++hk) {
+      const uint4* wr = reinterpret_cast<const uint4*>(p.wg + static_cast<size_t>(hk) * 32);
+      float acc = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float wv[8];
+        bf16x8_to_f32(__ldg(wr + c), wv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(xv[8 * c + e], wv[e], acc);
+      }
+      const float lg = __bfloat162float(__float2bfloat16_rn(acc));
+      const float sg = __bfloat162float(__float2bfloat16_rn(__frcp_rn(__fadd_rn(1.0f, expf(-lg)))));
+      p.gate[r * p.Hkv + hk] = 2.0f * sg;
+    }
+  }
+}
+
+
 // Value-embedding gate of one V row in place, split over two threads like the prologue's K rows
-// (thread h owns the 8 bytes at 8 h of every 16-byte chunk). The habr "Autoresearch" listing
-// (CausalSelfAttention.forward, value residual) computes, on bf16 tensors,
-//   v' = v + 2 * sigmoid(ve_gate(x[..., :32])) * ve
-// so every step rounds to bf16: the logit (a 32-term dot product accumulated in fp32), the sigmoid
-// (1 / (1 + exp(-logit)) with the accurate exp, a correctly rounded add and reciprocal), the product
-// with ve (exact in fp32 before its rounding), the sum with v.
+// (thread h owns the 8 bytes at 8 h of every 16-byte chunk): v' = bf16(v + bf16(gate * ve)), with the
+// row's gate factor from ve_gate_kernel (attn_common.cuh). gate * ve is exact in fp32 (a bf16 value
+// times twice a bf16 value), so only its rounding and the sum's are steps of their own.
 template <int D>
 __device__ __forceinline__ void gate_half_row_inplace(uint8_t* tile, int row, int h, int pos, int b, int hk,
                                                       const AttnParams& p) {
-  const uint4* xr = reinterpret_cast<const uint4*>(p.xg + (static_cast<size_t>(b) * p.T + pos) * p.xg_stride);
-  const uint4* wr = reinterpret_cast<const uint4*>(p.wg + static_cast<size_t>(hk) * 32);
-  float acc = 0.f;
+  const size_t r = (static_cast<size_t>(b) * p.T + pos) * p.Hkv + hk;
+  const float gate = __ldg(p.gate + r);
+  const uint2* er = reinterpret_cast<const uint2*>(p.ve + r * D) + h;
+  uint2 ev[D / 8];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    float xv[8], wv[8];
-    bf16x8_to_f32(__ldg(xr + c), xv);
-    bf16x8_to_f32(__ldg(wr + c), wv);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc = fmaf(xv[e], wv[e], acc);
-  }
-  const float lg = __bfloat162float(__float2bfloat16_rn(acc));
-  const float sg = __bfloat162float(__float2bfloat16_rn(__frcp_rn(__fadd_rn(1.0f, expf(-lg)))));
-  const float gate = 2.0f * sg;
-  const uint2* er = reinterpret_cast<const uint2*>(p.ve + ((static_cast<size_t>(b) * p.T + pos) * p.Hkv + hk) * D) + h;
+  for (int c = 0; c < D / 8; ++c) ev[c] = __ldg(er + 2 * c);
 #pragma unroll
   for (int c = 0; c < D / 8; ++c) {
     uint2* w = reinterpret_cast<uint2*>(tile + tile_off<D>(row, c) + 8 * h);
     const uint2 u = *w;
-    const uint2 ev = __ldg(er + 2 * c);
-    const uint32_t in[2] = {u.x, u.y}, ew[2] = {ev.x, ev.y};
+    const uint32_t in[2] = {u.x, u.y}, ew[2] = {ev[c].x, ev[c].y};
     uint32_t o[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {

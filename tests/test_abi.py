@@ -175,12 +175,15 @@ def test_value_gate_host_validation_codes(binding):
     lib = binding.lib
     q, k, v, ve = FAKE, FAKE + (1 << 24), FAKE + (2 << 24), FAKE + (3 << 24)
     x, w, out, lse = FAKE + (4 << 24), FAKE + (5 << 24), FAKE + (6 << 24), FAKE + (7 << 24)
+    ws = FAKE + (8 << 24)
+    assert binding.attn_fwd_ve_workspace_bytes(1, 2, 64) == 512  # 1 * 64 * 2 fp32 factors
+    assert binding.attn_fwd_ve_workspace_bytes(0, 2, 64) == 0
 
     def call(**kw):
-        a = dict(q=q, k=k, v=v, ve=ve, x=x, xs=64, w=w, out=out, lse=lse, B=1, H=4, Hkv=2, T=64, D=64)
+        a = dict(q=q, k=k, v=v, ve=ve, x=x, xs=64, w=w, out=out, lse=lse, ws=ws, wsb=512, B=1, H=4, Hkv=2, T=64, D=64)
         a.update(kw)
-        return lib.attn_fwd_ve(a["q"], a["k"], a["v"], a["ve"], a["x"], a["xs"], a["w"], a["out"], a["lse"], a["B"],
-                               a["H"], a["Hkv"], a["T"], a["D"], -1, 1, 10000.0, 1e-6, None)
+        return lib.attn_fwd_ve(a["q"], a["k"], a["v"], a["ve"], a["x"], a["xs"], a["w"], a["out"], a["lse"], a["ws"],
+                               a["wsb"], a["B"], a["H"], a["Hkv"], a["T"], a["D"], -1, 1, 10000.0, 1e-6, None)
 
     assert call(ve=0) == E.ATTN_ERR_INVALID_ARG
     assert call(x=0) == E.ATTN_ERR_INVALID_ARG
@@ -189,6 +192,9 @@ def test_value_gate_host_validation_codes(binding):
     assert call(xs=16) == E.ATTN_ERR_INVALID_ARG       # fewer than 32 channels per row
     assert call(xs=36) == E.ATTN_ERR_INVALID_ARG       # rows not 16-byte aligned
     assert call(out=ve + 256) == E.ATTN_ERR_INVALID_ARG  # out overlaps ve
+    assert call(ws=0) == E.ATTN_ERR_INVALID_ARG
+    assert call(wsb=256) == E.ATTN_ERR_INVALID_ARG     # workspace too small
+    assert call(ws=out + 64) == E.ATTN_ERR_INVALID_ARG  # workspace overlaps out
     assert call(D=48) == E.ATTN_ERR_UNSUPPORTED
     assert call() == E.ATTN_ERR_NOT_INITIALIZED
     assert call(xs=32) == E.ATTN_ERR_NOT_INITIALIZED
