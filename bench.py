@@ -342,6 +342,97 @@ def run_backward(args, w, rank, local_rank, world):
         dist.destroy_process_group()
 
 
+POLAR_METRIC = "Polar Express TFLOP/s (5 steps, Muon matrix groups of the ANDREA-120M shape) and % of B300 dense-BF16 peak"
+
+
+def run_polar(args, rank, local_rank, world):
+    """Muon's orthogonalisation of one optimiser step on the ANDREA-120M shape (12 layers, n_embd 768):
+    the attention projections (48 matrices of 768 x 768), the MLP input (12 x 3072 x 768, tall) and output
+    (12 x 768 x 3072, wide) matrices, each group one batched polar_express call (5 steps), bf16."""
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+    from sliding_window_attention_04_b300 import attn, polar
+
+    attn.attn_init(local_rank)
+    groups = [(48, 768, 768), (12, 3072, 768), (12, 768, 3072)]
+    bufs = []
+    flops = 0
+    for gi, (bt, m, n) in enumerate(groups):
+        g = torch.randn(bt, m, n, generator=torch.Generator().manual_seed(555 + gi)).to(torch.bfloat16).to(device)
+        out = torch.empty_like(g)
+        ws = torch.empty(polar.workspace_bytes(bt, m, n), dtype=torch.uint8, device=device)
+        bufs.append((g, out, ws))
+        s, l = min(m, n), max(m, n)
+        flops += bt * 5 * (4 * s * s * l + 2 * s ** 3)
+    stream = torch.cuda.current_stream(device)
+
+    def step(strm):
+        for g, out, ws in bufs:
+            polar.polar_express(g, out=out, workspace=ws, stream=strm)
+
+    for _ in range(args.warmup):
+        step(stream)
+    torch.cuda.synchronize(device)
+    if attn.attn_device_status() != 0:
+        raise SystemExit("device status after warm-up")
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(stream)
+    with torch.cuda.graph(graph, stream=cap):
+        for _ in range(args.steps):
+            step(cap)
+    stream.wait_stream(cap)
+    graph.replay()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = e0.elapsed_time(e1)
+    if attn.attn_device_status() != 0:
+        raise SystemExit("device status after the timed region")
+    (elapsed_ms,) = max_over_ranks([elapsed_ms], dist, device)
+    value = whole_job_tflops(flops, args.steps, world, elapsed_ms)
+    peak, peak_sustained, peak_kind = peaks()
+    n_launch = args.steps * sum(1 + 5 * 3 for _ in groups)
+    if rank == 0:
+        line = {
+            "metric": POLAR_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "Muon groups of the ANDREA-120M shape: 48 x 768x768, 12 x 3072x768, "
+                                   "12 x 768x3072, 5 Polar Express steps each",
+                       "flops": "per step 4 s^2 l + 2 s^3 per matrix (s, l = min, max of its sides)",
+                       "l2": "no flush: a step reads 141 MB of matrices plus their products",
+                       "launch": "the K timed steps as one CUDA graph (captured, replayed once untimed, then timed)"},
+            "pct_of_peak": value / world / peak * 100.0,
+            "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak, "unit": "TFLOP/s",
+                         "frac": value / world / peak, "traffic": None,
+                         "peak_kind": f"{peak_kind} dense bf16 burst (sustained {peak_sustained})",
+                         "kernel": "gemm_kernel (three per step) + frob_normalize_kernel"},
+            "gpu_launches": n_launch,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -356,7 +447,7 @@ def main():
     ap.add_argument("--workload", default="",
                     help="another workload by name prefix (extra measurements and captures; the bench "
                          "line is the ANDREA-120M workload)")
-    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd", "fwd_ve"], default="fwd",
+    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd", "fwd_ve", "polar"], default="fwd",
                     help="bwd: time attn_bwd (dq, dk, dv from out, lse, dout) on the same layers instead of "
                          "the forward; fwd_ve: the forward with the value-embedding gate on every layer "
                          "(attn_fwd_ve); extra measurements, the bench line is the forward")
@@ -379,6 +470,9 @@ def main():
         raise SystemExit("--warmup must be >= 3")
     if args.which == "bwd":
         run_backward(args, w, rank, local_rank, world)
+        return
+    if args.which == "polar":
+        run_polar(args, rank, local_rank, world)
         return
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)

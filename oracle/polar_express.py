@@ -16,7 +16,9 @@ The five coefficient triples are the listing's table, kept as data (they define 
 
 Pinned by tests/test_oracle_polar.py: the iteration equals the polynomial applied to the singular
 values from numpy's SVD, the wide form on G^T equals the transpose of the tall form on G, and for
-well-conditioned G the result is close to U V^T.
+well-conditioned G the result is close to U V^T. The rounding-point functions below (gemm_rounded,
+normalize_rounded) are pinned by exact integer cases, by float32 evaluations landing inside their radii,
+and by the rounded chain staying close to the float64 iteration.
 """
 from __future__ import annotations
 
@@ -48,3 +50,74 @@ def polar_express(g, steps: int = 5) -> np.ndarray:
             A = x @ np.swapaxes(x, -1, -2)
             x = a * x + (b * A + c * (A @ A)) @ x
     return x
+
+
+# ---------------------------------------------------------------------------------------------
+# The same steps at bf16 rounding points, one operation at a time (for checking a bf16 GPU
+# evaluation step by step). Every result is the exact value rounded once to bf16; each carries an
+# ambiguity radius: the largest distance to the bf16 value any single-precision evaluation within
+# the stated budget can round to.
+
+
+def _as_f64(x) -> np.ndarray:
+    if not isinstance(x, np.ndarray):
+        return x.detach().cpu().double().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def _round_with_radius(exact: np.ndarray, budget: np.ndarray):
+    from . import round_bf16_array
+
+    y = round_bf16_array(exact)
+    lo, hi = round_bf16_array(exact - budget), round_bf16_array(exact + budget)
+    return y, np.maximum(np.abs(hi - y), np.abs(y - lo))
+
+
+def gemm_rounded(p, q, alpha: float = 1.0, beta: float = 0.0, r=None):
+    """D = bf16(alpha * P Q + beta * R) for batched P [.., M, K], Q [.., K, N] (bf16 values), with the
+    radius of a single-precision evaluation: the K products accumulated in fp32 in any order with any
+    rounding of the partial sums (at most 2 K 2^-24 sum |P| |Q|, twice the round-to-nearest bound), then
+    alpha times that plus beta R in fp32 (2 * 2^-24 of |alpha P Q| + |beta R|). alpha and beta are
+    taken as the fp32 values they are passed as."""
+    pp, qq = _as_f64(p), _as_f64(q)
+    a = float(np.float32(alpha))
+    b = float(np.float32(beta))
+    prod = pp @ qq
+    mag = np.abs(pp) @ np.abs(qq)
+    K = pp.shape[-1]
+    rr = _as_f64(r) if r is not None else np.zeros_like(prod)
+    exact = a * prod + b * rr
+    budget = abs(a) * 2.0 * K * 2.0 ** -24 * mag + 2.0 * 2.0 ** -24 * (np.abs(a * prod) + np.abs(b * rr))
+    return _round_with_radius(exact, budget)
+
+
+def normalize_rounded(g):
+    """X = G / (||G||_F * 1.02 + 1e-6) at the listing's bf16 rounding points, per matrix of [.., m, n]:
+    nrm = bf16(||G||_F), t = bf16(nrm * fp32(1.02)), den = bf16(t + fp32(1e-6)), X = bf16(G / den).
+    Radius: the sum of squares accumulated in fp32 in any order (relative 2 mn 2^-24), its square root
+    correctly rounded (2^-24 more), every later value within one fp32 rounding of its exact form; each
+    candidate chain of bf16 values is followed to the end and the radius is the largest distance from
+    the exact-then-rounded X."""
+    from . import round_bf16_array
+
+    gg = _as_f64(g)
+    ss = np.sum(gg * gg, axis=(-2, -1), keepdims=True)
+    mn = gg.shape[-2] * gg.shape[-1]
+    f102 = float(np.float32(1.02))
+    f1e6 = float(np.float32(1e-6))
+
+    def chain(rel, e1, e2, e3):
+        nrm = round_bf16_array(np.sqrt(ss * (1.0 + rel)))
+        t = round_bf16_array(nrm * f102 * (1.0 + e1 * 2.0 ** -23))
+        den = round_bf16_array((t + f1e6) * (1.0 + e2 * 2.0 ** -23))
+        return round_bf16_array(gg / den * (1.0 + e3 * 2.0 ** -23))
+
+    base = chain(0.0, 0, 0, 0)
+    radius = np.zeros_like(gg)
+    d = (2.0 * mn + 2.0) * 2.0 ** -24
+    for rel in (-d, 0.0, d):
+        for e1 in (-1, 0, 1):
+            for e2 in (-1, 0, 1):
+                for e3 in (-1, 0, 1):
+                    radius = np.maximum(radius, np.abs(chain(rel, e1, e2, e3) - base))
+    return base, radius

@@ -17,7 +17,7 @@ LIB_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIB_DIR, "libswa_attn.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 
-SOURCES = [os.path.join(CSRC, "attn_api.cu"), os.path.join(CSRC, "attn_bwd.cu")]
+SOURCES = [os.path.join(CSRC, "attn_api.cu"), os.path.join(CSRC, "attn_bwd.cu"), os.path.join(CSRC, "polar.cu")]
 FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",
@@ -28,7 +28,7 @@ FLAGS = [
 
 
 def _deps():
-    return SOURCES + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + [os.path.join(INCLUDE, "attn.h")]
+    return SOURCES + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
 def up_to_date() -> bool:

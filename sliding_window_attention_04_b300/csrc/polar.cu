@@ -1,0 +1,226 @@
+// Host side of include/polar.h: argument checks, tensor maps and the launches of the normalisation
+// and of the three GEMMs of every Polar Express step.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "attn.h"
+#include "attn_internal.h"
+#include "polar.cuh"
+#include "polar.h"
+
+namespace {
+
+// The listing's polar_express_coeffs (a, b, c) per step: the method's definition, kept as data.
+constexpr float kCoeffs[5][3] = {
+    {8.156554524902461f, -22.48329292557795f, 15.878769915207462f},
+    {4.042929935166739f, -2.808917465908714f, 0.5000178451051316f},
+    {3.8916678022926607f, -2.772484153217685f, 0.5060648178503393f},
+    {3.285753657755655f, -2.3681294933425376f, 0.46449024233003106f},
+    {2.3465413258596377f, -1.7097828382687081f, 0.42323551169305323f},
+};
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct PeLayout {
+  size_t a, b, x, total;
+};
+
+PeLayout pe_layout(int batch, int m, int n) {
+  const size_t s = static_cast<size_t>(m < n ? m : n);
+  PeLayout l;
+  l.a = 0;
+  l.b = round256(static_cast<size_t>(batch) * s * s * 2);
+  l.x = l.b + round256(static_cast<size_t>(batch) * s * s * 2);
+  l.total = l.x + round256(static_cast<size_t>(batch) * m * n * 2);
+  return l;
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+int check_shape(int batch, int m, int n) {
+  if (batch < 1 || m < 8 || n < 8 || m % 8 != 0 || n % 8 != 0) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(batch) * m * n >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+// A row-major [batch, rows, inner] bf16 matrix as a 3-D tensor map. K-major operand views take
+// 128 rows x 64 inner elements per box; MN-major views 64 K rows x 64 inner (M / N) elements.
+CUresult encode3d(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* map, const void* base, int batch, int rows,
+                  int inner, bool mn_box) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2, static_cast<cuuint64_t>(rows) * inner * 2};
+  const cuuint32_t box[3] = {64, mn_box ? 64u : 128u, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+std::mutex g_pe_mu;
+int g_pe_device = -1;
+
+cudaError_t set_attrs() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(swa::gemm_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                swa::GemmCfg::kSmemBytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(swa::gemm_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                swa::GemmCfg::kSmemBytes)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(swa::gemm_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              swa::GemmCfg::kSmemBytes);
+}
+
+// D = alpha * P Q + beta * R over a batch; P is M x K, Q is K x N. p_mn: P stored as [K, M] (read
+// MN-major), else [M, K]; q_mn: Q stored as [K, N], else as [N, K] (Q^T, read K-major).
+int gemm(const swa_host::LibCtx& ctx, cudaStream_t st, int batch, int M, int N, int K, const void* P, bool p_mn,
+         const void* Q, bool q_mn, float alpha, float beta, const void* R, void* D) {
+  swa::GemmMaps maps;
+  if (encode3d(ctx.encode, &maps.p, P, batch, p_mn ? K : M, p_mn ? M : K, p_mn) != CUDA_SUCCESS ||
+      encode3d(ctx.encode, &maps.q, Q, batch, q_mn ? K : N, q_mn ? N : K, q_mn) != CUDA_SUCCESS)
+    return ATTN_ERR_CUDA;
+  swa::GemmParams gp{};
+  gp.M = M;
+  gp.N = N;
+  gp.K = K;
+  gp.alpha = alpha;
+  gp.beta = beta;
+  gp.R = static_cast<const __nv_bfloat16*>(R);
+  gp.D = static_cast<__nv_bfloat16*>(D);
+  gp.err = ctx.d_err;
+  const dim3 grid((N + 127) / 128, (M + 127) / 128, batch);
+  if (!p_mn && !q_mn) swa::gemm_kernel<false, false><<<grid, 128, swa::GemmCfg::kSmemBytes, st>>>(gp, maps);
+  else if (!p_mn && q_mn) swa::gemm_kernel<false, true><<<grid, 128, swa::GemmCfg::kSmemBytes, st>>>(gp, maps);
+  else if (p_mn && q_mn) swa::gemm_kernel<true, true><<<grid, 128, swa::GemmCfg::kSmemBytes, st>>>(gp, maps);
+  else return ATTN_ERR_UNSUPPORTED;
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int ensure_attrs(const swa_host::LibCtx& ctx) {
+  std::lock_guard<std::mutex> g(g_pe_mu);
+  if (g_pe_device == ctx.device) return ATTN_OK;
+  if (swa_host::on_device(ctx.device, [] { return set_attrs(); }) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  g_pe_device = ctx.device;
+  return ATTN_OK;
+}
+
+// One step inside the library lock.
+int step_locked(const swa_host::LibCtx& ctx, cudaStream_t st, const void* X, void* Y, int batch, int m, int n,
+                int step, uint8_t* ws) {
+  const PeLayout l = pe_layout(batch, m, n);
+  void* A = ws + l.a;
+  void* B = ws + l.b;
+  const float a = kCoeffs[step][0], b = kCoeffs[step][1], c = kCoeffs[step][2];
+  int rc;
+  if (m <= n) {
+    // wide: A = X X^T (m x m, K = n); B = c A A + b A; Y = a X + B X
+    if ((rc = gemm(ctx, st, batch, m, m, n, X, false, X, false, 1.f, 0.f, nullptr, A)) != ATTN_OK) return rc;
+    if ((rc = gemm(ctx, st, batch, m, m, m, A, false, A, true, c, b, A, B)) != ATTN_OK) return rc;
+    return gemm(ctx, st, batch, m, n, m, B, false, X, true, 1.f, a, X, Y);
+  }
+  // tall: A = X^T X (n x n, K = m); B = c A A + b A; Y = a X + X B
+  if ((rc = gemm(ctx, st, batch, n, n, m, X, true, X, true, 1.f, 0.f, nullptr, A)) != ATTN_OK) return rc;
+  if ((rc = gemm(ctx, st, batch, n, n, n, A, false, A, true, c, b, A, B)) != ATTN_OK) return rc;
+  return gemm(ctx, st, batch, m, n, n, X, false, B, true, 1.f, a, X, Y);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pe_workspace_bytes(int batch, int m, int n) {
+  if (batch < 1 || m < 1 || n < 1) return 0;
+  return pe_layout(batch, m, n).total;
+}
+
+int pe_normalize(const void* G, void* X, int batch, int m, int n, void* stream) {
+  int rc;
+  if ((rc = check_shape(batch, m, n)) != ATTN_OK) return rc;
+  if (!G || !X || !al16(G) || !al16(X)) return ATTN_ERR_INVALID_ARG;
+  return swa_host::locked([&](const swa_host::LibCtx& ctx) -> int {
+    int r = ATTN_OK;
+    const cudaError_t e = swa_host::on_device(ctx.device, [&]() -> cudaError_t {
+      swa::frob_normalize_kernel<<<batch, 512, 0, static_cast<cudaStream_t>(stream)>>>(
+          static_cast<const __nv_bfloat16*>(G), static_cast<__nv_bfloat16*>(X), static_cast<long long>(m) * n);
+      return cudaGetLastError();
+    });
+    if (e != cudaSuccess) r = ATTN_ERR_CUDA;
+    return r;
+  });
+}
+
+int pe_step(const void* X, void* Y, int batch, int m, int n, int step, void* workspace, size_t workspace_bytes,
+            void* stream) {
+  int rc;
+  if ((rc = check_shape(batch, m, n)) != ATTN_OK) return rc;
+  if (step < 0 || step > 4) return ATTN_ERR_INVALID_ARG;
+  if (!X || !Y || !workspace || !al16(X) || !al16(Y) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_ERR_INVALID_ARG;
+  const PeLayout l = pe_layout(batch, m, n);
+  if (workspace_bytes < l.total) return ATTN_ERR_INVALID_ARG;
+  const size_t xb = static_cast<size_t>(batch) * m * n * 2;
+  if (overlap(X, xb, Y, xb) || overlap(X, xb, workspace, l.total) || overlap(Y, xb, workspace, l.total))
+    return ATTN_ERR_INVALID_ARG;
+  return swa_host::locked([&](const swa_host::LibCtx& ctx) -> int {
+    int r = ensure_attrs(ctx);
+    if (r != ATTN_OK) return r;
+    const cudaError_t e = swa_host::on_device(ctx.device, [&]() -> cudaError_t {
+      r = step_locked(ctx, static_cast<cudaStream_t>(stream), X, Y, batch, m, n, step,
+                      static_cast<uint8_t*>(workspace));
+      return cudaSuccess;
+    });
+    return e != cudaSuccess ? ATTN_ERR_CUDA : r;
+  });
+}
+
+int polar_express(const void* G, void* X, int batch, int m, int n, int steps, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  int rc;
+  if ((rc = check_shape(batch, m, n)) != ATTN_OK) return rc;
+  if (steps < 0 || steps > 5) return ATTN_ERR_INVALID_ARG;
+  if (!G || !X || !workspace || !al16(G) || !al16(X) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_ERR_INVALID_ARG;
+  const PeLayout l = pe_layout(batch, m, n);
+  if (workspace_bytes < l.total) return ATTN_ERR_INVALID_ARG;
+  const size_t xb = static_cast<size_t>(batch) * m * n * 2;
+  if (overlap(G, xb, X, xb) || overlap(X, xb, workspace, l.total) || overlap(G, xb, workspace, l.total))
+    return ATTN_ERR_INVALID_ARG;
+  return swa_host::locked([&](const swa_host::LibCtx& ctx) -> int {
+    int r = ensure_attrs(ctx);
+    if (r != ATTN_OK) return r;
+    const cudaError_t e = swa_host::on_device(ctx.device, [&]() -> cudaError_t {
+      cudaStream_t st = static_cast<cudaStream_t>(stream);
+      uint8_t* ws = static_cast<uint8_t*>(workspace);
+      // the step sequence ping-pongs between X and the workspace's matrix so that it ends in X
+      void* bufs[2] = {X, ws + l.x};
+      int cur = steps % 2 == 0 ? 0 : 1;
+      swa::frob_normalize_kernel<<<batch, 512, 0, st>>>(static_cast<const __nv_bfloat16*>(G),
+                                                        static_cast<__nv_bfloat16*>(bufs[cur]),
+                                                        static_cast<long long>(m) * n);
+      if (cudaGetLastError() != cudaSuccess) {
+        r = ATTN_ERR_CUDA;
+        return cudaSuccess;
+      }
+      for (int s = 0; s < steps && r == ATTN_OK; ++s) {
+        r = step_locked(ctx, st, bufs[cur], bufs[cur ^ 1], batch, m, n, s, ws);
+        cur ^= 1;
+      }
+      return cudaSuccess;
+    });
+    return e != cudaSuccess ? ATTN_ERR_CUDA : r;
+  });
+}
+
+}  // extern "C"

@@ -198,3 +198,34 @@ def test_value_gate_host_validation_codes(binding):
     assert call(D=48) == E.ATTN_ERR_UNSUPPORTED
     assert call() == E.ATTN_ERR_NOT_INITIALIZED
     assert call(xs=32) == E.ATTN_ERR_NOT_INITIALIZED
+
+
+def test_polar_header_and_exports(binding):
+    """include/polar.h declares exactly the pe_* / polar_express symbols the library exports."""
+    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "polar.h")).read(), flags=re.S)
+    declared = set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*((?:pe_|polar_)\w+)\s*\(", text, flags=re.M))
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T ((?:pe_|polar_)\w+)", out))
+    assert declared == exported == {"pe_workspace_bytes", "pe_normalize", "pe_step", "polar_express"}
+    from sliding_window_attention_04_b300 import polar
+
+    assert set(polar.EXPORTED) == exported
+
+
+def test_polar_host_validation_codes(binding):
+    from sliding_window_attention_04_b300 import polar
+
+    E, lib = binding, binding.lib
+    x, y, ws = FAKE, FAKE + (1 << 24), FAKE + (2 << 24)
+    nb = polar.workspace_bytes(2, 64, 96)
+    assert nb >= 2 * 64 * 64 * 2 * 2 + 2 * 64 * 96 * 2 and nb % 256 == 0
+    assert polar.workspace_bytes(0, 64, 96) == 0
+    assert lib.pe_step(x, y, 2, 64, 96, 0, ws, nb, None) == E.ATTN_ERR_NOT_INITIALIZED
+    assert lib.pe_step(x, y, 2, 64, 100, 0, ws, nb, None) == E.ATTN_ERR_INVALID_ARG   # n not a multiple of 8
+    assert lib.pe_step(x, y, 2, 64, 96, 5, ws, nb, None) == E.ATTN_ERR_INVALID_ARG    # no sixth triple
+    assert lib.pe_step(x, y, 2, 64, 96, 0, ws, nb - 256, None) == E.ATTN_ERR_INVALID_ARG
+    assert lib.pe_step(x, x + 64, 2, 64, 96, 0, ws, nb, None) == E.ATTN_ERR_INVALID_ARG  # X and Y overlap
+    assert lib.pe_step(x, y, 2, 64, 96, 0, ws + 16, nb, None) == E.ATTN_ERR_INVALID_ARG  # workspace alignment
+    assert lib.polar_express(x, y, 2, 64, 96, 6, ws, nb, None) == E.ATTN_ERR_INVALID_ARG
+    assert lib.polar_express(x, y, 2, 64, 96, 5, ws, nb, None) == E.ATTN_ERR_NOT_INITIALIZED
+    assert lib.pe_normalize(x, y, 0, 64, 96, None) == E.ATTN_ERR_INVALID_ARG

@@ -1,0 +1,89 @@
+"""GPU parity of the Polar Express orthogonalisation (include/polar.h) against the oracle.
+
+Each product of every step is checked on its own: given the GPU's own input of that product (the
+previous product's bf16 output), the GPU result must be the exact value rounded to bf16, except where
+an fp32 evaluation may round the other way (oracle.polar_express.gemm_rounded reports that radius per
+element). The normalisation likewise (normalize_rounded). The full call must equal the chain of its
+steps bit for bit, and stay within the rounded chain's measured distance of the float64 iteration.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import polar_express as pe
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def polar():
+    from sliding_window_attention_04_b300 import attn
+    from sliding_window_attention_04_b300 import polar as p
+
+    attn.attn_init(0)
+    return p
+
+
+def _f64(t):
+    return t.detach().cpu().double().numpy()
+
+
+def _within(name, got, ref, rad):
+    bad = np.abs(got - ref) > rad
+    assert not bad.any(), f"{name}: {int(bad.sum())} elements outside the radius, e.g. {np.argwhere(bad)[:3].tolist()}"
+
+
+SHAPES = [(2, 64, 96), (1, 96, 64), (3, 128, 128), (1, 72, 200), (1, 200, 72), (2, 256, 384), (1, 384, 256)]
+
+
+@pytest.mark.parametrize("batch,m,n", SHAPES)
+def test_every_product_matches_the_rounded_oracle(polar, batch, m, n):
+    g = torch.randn(batch, m, n, generator=torch.Generator().manual_seed(m * 1000 + n)).to(torch.bfloat16)
+    x = polar.normalize(g.cuda())
+    torch.cuda.synchronize()
+    ref, rad = pe.normalize_rounded(g)
+    _within("normalize", _f64(x), ref, rad)
+    tall = m > n
+    for k, (a, b, c) in enumerate(pe.POLAR_EXPRESS_COEFFS):
+        y, A, B = polar.step(x, k)
+        torch.cuda.synchronize()
+        xh, Ah, Bh, yh = _f64(x), _f64(A), _f64(B), _f64(y)
+        xt = np.swapaxes(xh, -1, -2)
+        Aref, ra = pe.gemm_rounded(xt, xh) if tall else pe.gemm_rounded(xh, xt)
+        _within(f"step {k} A", Ah, Aref, ra)
+        Bref, rb = pe.gemm_rounded(Ah, Ah, c, b, Ah)
+        _within(f"step {k} B", Bh, Bref, rb)
+        Yref, ry = pe.gemm_rounded(xh, Bh, 1.0, a, xh) if tall else pe.gemm_rounded(Bh, xh, 1.0, a, xh)
+        _within(f"step {k} X", yh, Yref, ry)
+        x = y.clone()
+    full = polar.polar_express(g.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(full, x)
+    f64 = pe.polar_express(_f64(g))
+    rel = np.linalg.norm(_f64(full) - f64) / np.linalg.norm(f64)
+    assert rel < 5e-2, rel
+
+
+def test_model_shaped_batches(polar):
+    """Muon's groups of the ANDREA-120M shape (768 x 768, 768 x 3072 wide, 3072 x 768 tall), a few matrices
+    each: the full call against the float64 iteration, and the last step's products against the rounded
+    oracle."""
+    for batch, m, n in ((4, 768, 768), (1, 768, 3072), (1, 3072, 768)):
+        g = torch.randn(batch, m, n, generator=torch.Generator().manual_seed(m + n)).to(torch.bfloat16)
+        gc = g.cuda()
+        full = polar.polar_express(gc)
+        x4 = polar.normalize(gc)
+        for k in range(4):
+            x4, _, _ = polar.step(x4, k)
+            x4 = x4.clone()
+        y, A, B = polar.step(x4, 4)
+        torch.cuda.synchronize()
+        assert torch.equal(y, full)
+        a, b, c = pe.POLAR_EXPRESS_COEFFS[4]
+        xh, Ah, Bh = _f64(x4), _f64(A), _f64(B)
+        tall = m > n
+        Yref, ry = pe.gemm_rounded(xh, Bh, 1.0, a, xh) if tall else pe.gemm_rounded(Bh, xh, 1.0, a, xh)
+        _within(f"{m}x{n} last step", _f64(y), Yref, ry)
+        f64 = pe.polar_express(_f64(g))
+        rel = np.linalg.norm(_f64(full) - f64) / np.linalg.norm(f64)
+        assert rel < 5e-2, (m, n, rel)
