@@ -97,6 +97,14 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def wait_ready(self, timeout: float = 10.0):
+        """Block until the sampler has printed its first sample, so that its start-up (which can stall the
+        GPU for milliseconds) lies before the timed region, then let one more interval pass."""
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.02)
+        time.sleep(0.25)
+
     def stop(self):
         if self.proc is None:
             return None
@@ -298,7 +306,7 @@ def run_backward(args, w, rank, local_rank, world):
            for _ in range(args.steps if flush else 1)]
     sampler = ClockSampler(local_rank)
     sampler.start()
-    time.sleep(0.3)
+    sampler.wait_ready()
     if dist:
         dist.barrier()
     torch.cuda.synchronize(device)
@@ -392,7 +400,7 @@ def run_polar(args, rank, local_rank, world):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local_rank)
     sampler.start()
-    time.sleep(0.3)
+    sampler.wait_ready()
     if dist:
         dist.barrier()
     torch.cuda.synchronize(device)
@@ -409,7 +417,7 @@ def run_polar(args, rank, local_rank, world):
     (elapsed_ms,) = max_over_ranks([elapsed_ms], dist, device)
     value = whole_job_tflops(flops, args.steps, world, elapsed_ms)
     peak, peak_sustained, peak_kind = peaks()
-    n_launch = args.steps * sum(1 + 5 * 3 for _ in groups)
+    n_launch = args.steps * sum(2 + 5 * 3 for _ in groups)  # two normalisation passes, three GEMMs a step
     if rank == 0:
         line = {
             "metric": POLAR_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -424,7 +432,8 @@ def run_polar(args, rank, local_rank, world):
             "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak, "unit": "TFLOP/s",
                          "frac": value / world / peak, "traffic": None,
                          "peak_kind": f"{peak_kind} dense bf16 burst (sustained {peak_sustained})",
-                         "kernel": "gemm_kernel (three per step) + frob_normalize_kernel"},
+                         "kernel": "gemm_kernel (three per step; achieved over the whole step, normalisation "
+                                   "passes and gaps included)"},
             "gpu_launches": n_launch,
             "clocks": clocks,
         }
@@ -544,7 +553,7 @@ def main():
            for _ in range(args.steps if flush else 1)]
     sampler = ClockSampler(local_rank)
     sampler.start()
-    time.sleep(0.3)
+    sampler.wait_ready()
     if dist:
         dist.barrier()
     torch.cuda.synchronize(device)

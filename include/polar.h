@@ -29,12 +29,17 @@
 extern "C" {
 #endif
 
-/* pe_workspace_bytes — scratch pe_step / polar_express need: A and B ([batch, s, s], s = min(m, n))
- * and one more [batch, m, n] matrix, each on a 256-byte boundary. 0 for a non-positive size. */
+/* pe_workspace_bytes — scratch pe_normalize / pe_step / polar_express need: A and B ([batch, s, s],
+ * s = min(m, n)), one more [batch, m, n] matrix and the normalisation's fp32 partial sums (at most
+ * 1024 per matrix), each on a 256-byte boundary. 0 for a non-positive size. */
 size_t pe_workspace_bytes(int batch, int m, int n);
 
-/* pe_normalize — X = G / (||G||_F * 1.02 + 1e-6) per matrix (bf16 steps as above). X may equal G. */
-int pe_normalize(const void* G, void* X, int batch, int m, int n, void* stream);
+/* pe_normalize — X = G / (||G||_F * 1.02 + 1e-6) per matrix (bf16 steps as above). X may equal G
+ * (in place); otherwise G and X must not overlap, and neither may overlap the workspace (at least
+ * pe_workspace_bytes(batch, m, n) bytes, 256-byte aligned). The sum of squares is taken in fp32 over
+ * chunks whose partial sums are added in one fixed order: the result is deterministic. */
+int pe_normalize(const void* G, void* X, int batch, int m, int n, void* workspace, size_t workspace_bytes,
+                 void* stream);
 
 /* pe_step — one step with the listing's coefficient triple number `step` (0..4): Y from X. X and Y
  * must not overlap each other or the workspace. After the call (when the stream reaches it) the

@@ -24,18 +24,43 @@ constexpr float kCoeffs[5][3] = {
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
+// The normalisation's chunk: 16384 elements, or more so that a matrix has at most 1024 chunks (the
+// second pass sums a matrix's partial sums in every CTA).
+int norm_chunk(long long mn) {
+  long long c = 16384;
+  while ((mn + c - 1) / c > 1024) c *= 2;
+  return static_cast<int>(c);
+}
+
 struct PeLayout {
-  size_t a, b, x, total;
+  size_t a, b, x, part, total;
+  int chunk, nchunks;
 };
 
 PeLayout pe_layout(int batch, int m, int n) {
   const size_t s = static_cast<size_t>(m < n ? m : n);
+  const long long mn = static_cast<long long>(m) * n;
   PeLayout l;
+  l.chunk = norm_chunk(mn);
+  l.nchunks = static_cast<int>((mn + l.chunk - 1) / l.chunk);
   l.a = 0;
   l.b = round256(static_cast<size_t>(batch) * s * s * 2);
   l.x = l.b + round256(static_cast<size_t>(batch) * s * s * 2);
-  l.total = l.x + round256(static_cast<size_t>(batch) * m * n * 2);
+  l.part = l.x + round256(static_cast<size_t>(batch) * m * n * 2);
+  l.total = l.part + round256(static_cast<size_t>(batch) * l.nchunks * 4);
   return l;
+}
+
+// Both passes of the normalisation; `part` is the workspace's partial-sum region.
+cudaError_t launch_normalize(cudaStream_t st, const void* G, void* X, int batch, int m, int n, uint8_t* ws) {
+  const PeLayout l = pe_layout(batch, m, n);
+  const long long mn = static_cast<long long>(m) * n;
+  float* part = reinterpret_cast<float*>(ws + l.part);
+  const dim3 grid(l.nchunks, batch);
+  swa::frob_partial_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(G), part, mn, l.chunk);
+  swa::frob_scale_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(G), static_cast<__nv_bfloat16*>(X),
+                                               part, mn, l.chunk);
+  return cudaGetLastError();
 }
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -68,16 +93,39 @@ CUresult encode3d(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* map, co
 std::mutex g_pe_mu;
 int g_pe_device = -1;
 
+template <bool A_MN, bool B_MN, int BN>
+cudaError_t set_attr_one() {
+  return cudaFuncSetAttribute(swa::gemm_kernel<A_MN, B_MN, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              swa::GemmCfg<BN>::kSmemBytes);
+}
+
 cudaError_t set_attrs() {
-  cudaError_t e;
-  if ((e = cudaFuncSetAttribute(swa::gemm_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                swa::GemmCfg::kSmemBytes)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(swa::gemm_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                swa::GemmCfg::kSmemBytes)) != cudaSuccess)
-    return e;
-  return cudaFuncSetAttribute(swa::gemm_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              swa::GemmCfg::kSmemBytes);
+  const cudaError_t e[6] = {set_attr_one<false, false, 128>(), set_attr_one<false, false, 256>(),
+                            set_attr_one<false, true, 128>(),  set_attr_one<false, true, 256>(),
+                            set_attr_one<true, true, 128>(),   set_attr_one<true, true, 256>()};
+  for (cudaError_t x : e)
+    if (x != cudaSuccess) return x;
+  return cudaSuccess;
+}
+
+template <bool A_MN, bool B_MN>
+void launch_gemm(int bn, int grid, cudaStream_t st, const swa::GemmParams& gp, const swa::GemmMaps& maps) {
+  if (bn == 256)
+    swa::gemm_kernel<A_MN, B_MN, 256><<<grid, 192, swa::GemmCfg<256>::kSmemBytes, st>>>(gp, maps);
+  else
+    swa::gemm_kernel<A_MN, B_MN, 128><<<grid, 192, swa::GemmCfg<128>::kSmemBytes, st>>>(gp, maps);
+}
+
+// Output tile width: the one whose tiles finish in fewer rounds of the grid, counted in 128-column
+// units of MMA work; 256 on a tie (it reads fewer operand bytes per product).
+int choose_bn(int batch, int M, int N, int sms, int* grid) {
+  const long long tm = (M + 127) / 128;
+  const long long t128 = tm * ((N + 127) / 128) * batch, t256 = tm * ((N + 255) / 256) * batch;
+  const long long c128 = (t128 + sms - 1) / sms, c256 = 2 * ((t256 + sms - 1) / sms);
+  const bool wide = c256 <= c128;
+  const long long tiles = wide ? t256 : t128;
+  *grid = static_cast<int>(tiles < sms ? tiles : sms);
+  return wide ? 256 : 128;
 }
 
 // D = alpha * P Q + beta * R over a batch; P is M x K, Q is K x N. p_mn: P stored as [K, M] (read
@@ -86,21 +134,23 @@ int gemm(const swa_host::LibCtx& ctx, cudaStream_t st, int batch, int M, int N, 
          const void* Q, bool q_mn, float alpha, float beta, const void* R, void* D) {
   swa::GemmMaps maps;
   if (encode3d(ctx.encode, &maps.p, P, batch, p_mn ? K : M, p_mn ? M : K, p_mn) != CUDA_SUCCESS ||
-      encode3d(ctx.encode, &maps.q, Q, batch, q_mn ? K : N, q_mn ? N : K, q_mn) != CUDA_SUCCESS)
+      encode3d(ctx.encode, &maps.q, Q, batch, q_mn ? K : N, q_mn ? N : K, q_mn) != CUDA_SUCCESS ||
+      encode3d(ctx.encode, &maps.d, D, batch, M, N, false) != CUDA_SUCCESS)
     return ATTN_ERR_CUDA;
   swa::GemmParams gp{};
+  gp.batch = batch;
   gp.M = M;
   gp.N = N;
   gp.K = K;
   gp.alpha = alpha;
   gp.beta = beta;
   gp.R = static_cast<const __nv_bfloat16*>(R);
-  gp.D = static_cast<__nv_bfloat16*>(D);
   gp.err = ctx.d_err;
-  const dim3 grid((N + 127) / 128, (M + 127) / 128, batch);
-  if (!p_mn && !q_mn) swa::gemm_kernel<false, false><<<grid, 128, swa::GemmCfg::kSmemBytes, st>>>(gp, maps);
-  else if (!p_mn && q_mn) swa::gemm_kernel<false, true><<<grid, 128, swa::GemmCfg::kSmemBytes, st>>>(gp, maps);
-  else if (p_mn && q_mn) swa::gemm_kernel<true, true><<<grid, 128, swa::GemmCfg::kSmemBytes, st>>>(gp, maps);
+  int grid = 0;
+  const int bn = choose_bn(batch, M, N, ctx.sm_count, &grid);
+  if (!p_mn && !q_mn) launch_gemm<false, false>(bn, grid, st, gp, maps);
+  else if (!p_mn && q_mn) launch_gemm<false, true>(bn, grid, st, gp, maps);
+  else if (p_mn && q_mn) launch_gemm<true, true>(bn, grid, st, gp, maps);
   else return ATTN_ERR_UNSUPPORTED;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -145,19 +195,22 @@ size_t pe_workspace_bytes(int batch, int m, int n) {
   return pe_layout(batch, m, n).total;
 }
 
-int pe_normalize(const void* G, void* X, int batch, int m, int n, void* stream) {
+int pe_normalize(const void* G, void* X, int batch, int m, int n, void* workspace, size_t workspace_bytes,
+                 void* stream) {
   int rc;
   if ((rc = check_shape(batch, m, n)) != ATTN_OK) return rc;
-  if (!G || !X || !al16(G) || !al16(X)) return ATTN_ERR_INVALID_ARG;
+  if (!G || !X || !workspace || !al16(G) || !al16(X) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_ERR_INVALID_ARG;
+  const PeLayout l = pe_layout(batch, m, n);
+  if (workspace_bytes < l.total) return ATTN_ERR_INVALID_ARG;
+  const size_t xb = static_cast<size_t>(batch) * m * n * 2;
+  if ((G != X && overlap(G, xb, X, xb)) || overlap(X, xb, workspace, l.total) || overlap(G, xb, workspace, l.total))
+    return ATTN_ERR_INVALID_ARG;
   return swa_host::locked([&](const swa_host::LibCtx& ctx) -> int {
-    int r = ATTN_OK;
     const cudaError_t e = swa_host::on_device(ctx.device, [&]() -> cudaError_t {
-      swa::frob_normalize_kernel<<<batch, 512, 0, static_cast<cudaStream_t>(stream)>>>(
-          static_cast<const __nv_bfloat16*>(G), static_cast<__nv_bfloat16*>(X), static_cast<long long>(m) * n);
-      return cudaGetLastError();
+      return launch_normalize(static_cast<cudaStream_t>(stream), G, X, batch, m, n, static_cast<uint8_t*>(workspace));
     });
-    if (e != cudaSuccess) r = ATTN_ERR_CUDA;
-    return r;
+    return e != cudaSuccess ? ATTN_ERR_CUDA : ATTN_OK;
   });
 }
 
@@ -206,10 +259,7 @@ int polar_express(const void* G, void* X, int batch, int m, int n, int steps, vo
       // the step sequence ping-pongs between X and the workspace's matrix so that it ends in X
       void* bufs[2] = {X, ws + l.x};
       int cur = steps % 2 == 0 ? 0 : 1;
-      swa::frob_normalize_kernel<<<batch, 512, 0, st>>>(static_cast<const __nv_bfloat16*>(G),
-                                                        static_cast<__nv_bfloat16*>(bufs[cur]),
-                                                        static_cast<long long>(m) * n);
-      if (cudaGetLastError() != cudaSuccess) {
+      if (launch_normalize(st, G, bufs[cur], batch, m, n, ws) != cudaSuccess) {
         r = ATTN_ERR_CUDA;
         return cudaSuccess;
       }

@@ -6,14 +6,18 @@
 //   per step (a, b, c):  wide (rows <= cols): A = X X^T, B = b A + c A A, X = a X + B X
 //                        tall (rows > cols):  A = X^T X, B = b A + c A A, X = a X + X B
 //
-// gemm_kernel<A_MN, B_MN> computes, for every matrix z of a batch,
+// gemm_kernel<A_MN, B_MN, BN> computes, for every matrix z of a batch,
 //   D[z] = alpha * P[z] Q[z] + beta * R[z]      (bf16 in, fp32 accumulation in TMEM, bf16 out)
 // with P (M x K) and Q (K x N) read through TMA tensor maps either K-major (rows of K contiguous
 // elements) or MN-major (rows of M / N contiguous elements), so X X^T, X^T X, A A and B X all take
-// their operands straight from the row-major matrices without a transpose. One 128 x 128 output
-// tile per CTA: a TMA producer thread streams 64-deep K slices of P and Q through a 6-stage
-// shared-memory ring, one thread issues the tcgen05 MMAs (M = 128, N = 128, K = 16 each), and the
-// four warps read the accumulator from TMEM (thread = output row) for the epilogue.
+// their operands straight from the row-major matrices without a transpose.
+//
+// Persistent and warp-specialised: each CTA (one per SM) walks the 128 x BN output tiles of the
+// whole batch with a stride of the grid. Warp 0 streams 64-deep K slices of P and Q through a
+// shared-memory ring by TMA; one thread of warp 1 issues the tcgen05 MMAs (M = 128, N = BN, K = 16)
+// into one of two TMEM accumulators; warps 2-5 drain the other accumulator (thread = output row,
+// 64 columns at a time: alpha * acc + beta * R, rounded to bf16, staged swizzled in shared memory and
+// written by TMA stores), so a tile's epilogue overlaps the next tile's products.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -24,39 +28,68 @@
 namespace swa {
 
 struct GemmParams {
-  int M, N, K;
+  int batch, M, N, K;
   float alpha, beta;
   const __nv_bfloat16* R;  // [batch, M, N] or nullptr (no beta term)
-  __nv_bfloat16* D;        // [batch, M, N]
   int* err;
 };
 
 struct GemmMaps {
-  CUtensorMap p, q;  // 3-D (inner, rows, batch) views; see the host side for the box of each form
+  CUtensorMap p, q, d;  // 3-D (inner, rows, batch) views; see the host side for the box of each form
 };
 
+template <int BN>
 struct GemmCfg {
-  static constexpr int BM = 128, BN = 128, BK = 64, kStages = 6;
+  static constexpr int BM = 128, BK = 64, kThreads = 192;
+  static constexpr int kStages = BN == 256 ? 4 : 6;
   static constexpr int kTileP = BM * BK * 2;  // 16 KB
-  static constexpr int kTileQ = BN * BK * 2;  // 16 KB
+  static constexpr int kTileQ = BN * BK * 2;  // 16 or 32 KB
   static constexpr int kStageBytes = kTileP + kTileQ;
-  static constexpr int kOffBar = kStages * kStageBytes;
-  static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarDone = 2 * kStages, kNumBars = 2 * kStages + 1;
+  static constexpr int kOut = BM * 64 * 2;  // one 128 x 64 bf16 output chunk, 16 KB
+  static constexpr int kOffOut = kStages * kStageBytes;
+  static constexpr int kOffBar = kOffOut + 2 * kOut;
+  static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarAccFull = 2 * kStages, kBarAccEmpty = 2 * kStages + 2,
+                       kBarDone = 2 * kStages + 4, kNumBars = 2 * kStages + 5;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  static constexpr uint32_t kTmemCols = 2 * BN;
+  static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
-// Shared-memory descriptor of K step ks (16 deep) of a 128 x 64 operand tile: K-major (128 rows of
-// 128 bytes, 128-byte swizzle) or MN-major (two 64-wide M / N chunks of 64 K rows, 8 KB apart).
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+// Wait until the shared-memory sources of all but the newest committed bulk group have been read.
+__device__ __forceinline__ void bulk_wait_group_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+// Shared-memory descriptor of K step ks (16 deep) of an operand tile of `rows` M / N rows x 64 K:
+// K-major (rows of 128 bytes, 128-byte swizzle, 8-row groups 1 KB apart) or MN-major (64-wide M / N
+// chunks of 64 K rows, 8 KB apart).
 template <bool MN>
 __device__ __forceinline__ uint64_t gemm_desc(uint32_t tile, int ks) {
   if constexpr (MN) return make_sdesc(tile + ks * 16 * 128, 8192, 1024, 2);
   else return make_sdesc(tile + ks * 32, 16, 1024, 2);
 }
 
-template <bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(128, 1) gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
-  using Cfg = GemmCfg;
+// Eight 16-byte pieces of row `row` of R from column c0 (zero past the row's end or the matrix).
+__device__ __forceinline__ void gemm_load_r(uint4 (&v)[8], const __nv_bfloat16* rrow, int c0, int N) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    v[u] = (rrow != nullptr && c0 + 8 * u < N) ? __ldg(reinterpret_cast<const uint4*>(rrow + c0 + 8 * u))
+                                               : make_uint4(0, 0, 0, 0);
+}
+
+template <bool A_MN, bool B_MN, int BN>
+__global__ void __launch_bounds__(192, 1) gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
+  using Cfg = GemmCfg<BN>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -64,155 +97,287 @@ __global__ void __launch_bounds__(128, 1) gemm_kernel(const GemmParams p, const 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
+  volatile int* epi_ok = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n0 = blockIdx.x * Cfg::BN, m0 = blockIdx.y * Cfg::BM, z = blockIdx.z;
+  const int tiles_n = (p.N + BN - 1) / BN, tiles_m = (p.M + Cfg::BM - 1) / Cfg::BM;
+  const int per_mat = tiles_m * tiles_n, total = per_mat * p.batch;
   const int nk = (p.K + Cfg::BK - 1) / Cfg::BK;
+  auto decode = [&](int t, int& z, int& m0, int& n0) {
+    z = t / per_mat;
+    const int r = t - z * per_mat;
+    const int mt = r / tiles_n;
+    m0 = mt * Cfg::BM;
+    n0 = (r - mt * tiles_n) * BN;
+  };
 
   if (tid == 0) {
-    for (int i = 0; i < Cfg::kNumBars; ++i) mbar_init(bars + i, 1);
+    for (int i = 0; i < 2 * S + 2; ++i) mbar_init(bars + i, 1);
+    mbar_init(bars + Cfg::kBarAccEmpty, 4);
+    mbar_init(bars + Cfg::kBarAccEmpty + 1, 4);
+    mbar_init(bars + Cfg::kBarDone, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 128);
+    tmem_alloc(tmem_slot, Cfg::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  auto stage_p = [&](int s) { return smem + s * Cfg::kStageBytes; };
-  auto stage_q = [&](int s) { return smem + s * Cfg::kStageBytes + Cfg::kTileP; };
 
-  if (warp == 0 && lane == 0) {
-    // ---- producer: K slices of P and Q ----
-    prefetch_tmap(&maps.p);
-    prefetch_tmap(&maps.q);
-    for (int kt = 0; kt < nk; ++kt) {
-      const int s = kt % S, k0 = kt * Cfg::BK;
-      if (kt >= S && !mbar_wait_or_abort(bars + Cfg::kBarEmpty + s, ((kt / S) - 1) & 1, abort_flag)) {
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- producer: K slices of P and Q for every tile of this CTA ----
+      prefetch_tmap(&maps.p);
+      prefetch_tmap(&maps.q);
+      prefetch_tmap(&maps.d);
+      uint32_t g = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int z, m0, n0;
+        decode(t, z, m0, n0);
+        for (int kt = 0; kt < nk; ++kt, ++g) {
+          const int s = g % S, k0 = kt * Cfg::BK;
+          if (g >= S && !mbar_wait_or_abort(bars + Cfg::kBarEmpty + s, ((g / S) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint64_t* full = bars + Cfg::kBarFull + s;
+          uint8_t* sp = smem + s * Cfg::kStageBytes;
+          uint8_t* sq = sp + Cfg::kTileP;
+          mbar_arrive_expect_tx(full, Cfg::kStageBytes);
+          if constexpr (A_MN) {
+            tma_load_3d(sp, &maps.p, full, m0, k0, z);
+            tma_load_3d(sp + 8192, &maps.p, full, m0 + 64, k0, z);
+          } else {
+            tma_load_3d(sp, &maps.p, full, k0, m0, z);
+          }
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j) {
+            if constexpr (B_MN) tma_load_3d(sq + 8192 * j, &maps.q, full, n0 + 64 * j, k0, z);
+            else if (j % 2 == 0) tma_load_3d(sq + 8192 * j, &maps.q, full, k0, n0 + 64 * j, z);
+          }
+        }
+      }
+      if (!ok) {
         report_error(p.err, kDevErrTimeout);
         *abort_flag = 1;
-        break;
       }
-      uint64_t* full = bars + Cfg::kBarFull + s;
-      mbar_arrive_expect_tx(full, Cfg::kStageBytes);
-      if constexpr (A_MN) {
-        tma_load_3d(stage_p(s), &maps.p, full, m0, k0, z);
-        tma_load_3d(stage_p(s) + 8192, &maps.p, full, m0 + 64, k0, z);
-      } else {
-        tma_load_3d(stage_p(s), &maps.p, full, k0, m0, z);
-      }
-      if constexpr (B_MN) {
-        tma_load_3d(stage_q(s), &maps.q, full, n0, k0, z);
-        tma_load_3d(stage_q(s) + 8192, &maps.q, full, n0 + 64, k0, z);
-      } else {
-        tma_load_3d(stage_q(s), &maps.q, full, k0, n0, z);
-      }
+      // The loads this thread issued must land before the CTA may exit: wait for the last phase armed
+      // on every stage (already complete unless the consumer side gave up).
+      for (uint32_t j = g > static_cast<uint32_t>(S) ? g - S : 0u; j < g; ++j)
+        mbar_wait(bars + Cfg::kBarFull + j % S, (j / S) & 1);
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer ----
-    constexpr uint32_t idesc = make_idesc_bf16(128, 128, B_MN) | (A_MN ? (1u << 15) : 0u);
-    bool ok = true;
-    for (int kt = 0; kt < nk; ++kt) {
-      const int s = kt % S;
-      if (!mbar_wait_or_abort(bars + Cfg::kBarFull + s, (kt / S) & 1, abort_flag)) {
-        ok = false;
-        break;
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer ----
+      constexpr uint32_t idesc = make_idesc_bf16(128, BN, B_MN) | (A_MN ? (1u << 15) : 0u);
+      uint32_t g = 0;
+      bool ok = true;
+      int i = 0;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++i) {
+        const int buf = i & 1;
+        if (i >= 2 && !mbar_wait_or_abort(bars + Cfg::kBarAccEmpty + buf, ((i >> 1) - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc = tmem + static_cast<uint32_t>(buf * BN);
+        for (int kt = 0; kt < nk; ++kt, ++g) {
+          const int s = g % S;
+          if (!mbar_wait_or_abort(bars + Cfg::kBarFull + s, (g / S) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sp = smem_u32(smem + s * Cfg::kStageBytes), sq = sp + Cfg::kTileP;
+#pragma unroll
+          for (int ks = 0; ks < Cfg::BK / 16; ++ks)
+            umma_ss(acc, gemm_desc<A_MN>(sp, ks), gemm_desc<B_MN>(sq, ks), idesc, (kt > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(bars + Cfg::kBarEmpty + s);
+        }
+        if (ok) umma_commit(bars + Cfg::kBarAccFull + buf);
       }
+      if (!ok) {
+        report_error(p.err, kDevErrTimeout);
+        *abort_flag = 1;
+      }
+      // every product issued has completed before TMEM is released
+      umma_commit(bars + Cfg::kBarDone);
+      mbar_wait(bars + Cfg::kBarDone, 0);
+    }
+  } else {
+    // ---- epilogue: warps 2-5, thread = tile row (TMEM lane quarter = warp % 4) ----
+    const int et = tid - 64;
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint8_t* out = smem + Cfg::kOffOut;
+    int i = 0, cc = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
+      int z, m0, n0;
+      decode(t, z, m0, n0);
+      const int buf = i & 1;
+      const int grow = m0 + row;
+      const __nv_bfloat16* rrow =
+          (p.R != nullptr && grow < p.M) ? p.R + (static_cast<size_t>(z) * p.M + grow) * p.N : nullptr;
+      const int nvc = min(BN / 64, (p.N - n0 + 63) / 64);  // 64-column chunks inside the matrix
+      uint4 rv[8];
+      gemm_load_r(rv, rrow, n0, p.N);
+      if (et == 0) {
+        const bool ok = mbar_wait_or_abort(bars + Cfg::kBarAccFull + buf, (i >> 1) & 1, abort_flag);
+        if (!ok) {
+          report_error(p.err, kDevErrTimeout);
+          *abort_flag = 1;
+        }
+        *epi_ok = ok ? 1 : 0;
+      }
+      epi_bar_sync();
+      if (*epi_ok == 0) break;
       tc_fence_after();
-      const uint32_t sp = smem_u32(stage_p(s)), sq = smem_u32(stage_q(s));
+      for (int c = 0; c < nvc; ++c, ++cc) {
+        uint32_t a[64];
+        const uint32_t col = lane_base + static_cast<uint32_t>(buf * BN + 64 * c);
+        tmem_ld32(tmem + col, a);
+        tmem_ld32(tmem + col + 32, a + 32);
+        tmem_ld_wait();
+        reg_fence<32>(a);
+        reg_fence<32>(a + 32);
+        if (c == nvc - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars + Cfg::kBarAccEmpty + buf);
+        }
+        uint4 rn[8];
+        if (c + 1 < nvc) gemm_load_r(rn, rrow, n0 + 64 * (c + 1), p.N);
+        uint32_t o[32];
 #pragma unroll
-      for (int ks = 0; ks < Cfg::BK / 16; ++ks)
-        umma_ss(tmem, gemm_desc<A_MN>(sp, ks), gemm_desc<B_MN>(sq, ks), idesc, (kt > 0 || ks > 0) ? 1u : 0u);
-      umma_commit(bars + Cfg::kBarEmpty + s);
-    }
-    if (!ok) {
-      report_error(p.err, kDevErrTimeout);
-      *abort_flag = 1;
-    }
-    umma_commit(bars + Cfg::kBarDone);
-  }
-
-  // ---- epilogue: thread = output row m0 + tid; 32 columns per TMEM load ----
-  const bool ok = mbar_wait_or_abort(bars + Cfg::kBarDone, 0, abort_flag) && *abort_flag == 0;
-  tc_fence_after();
-  const int row = m0 + tid;
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-  const size_t rbase = (static_cast<size_t>(z) * p.M + row) * p.N;
-#pragma unroll 1
-  for (int c = 0; c < Cfg::BN / 32; ++c) {
-    uint32_t a[32];
-    __syncwarp();
-    tmem_ld32(tmem + lane_base + 32 * c, a);
-    tmem_ld_wait();
-    reg_fence<32>(a);
-    const int nc = n0 + 32 * c;
-    if (!ok || row >= p.M || nc >= p.N) continue;
-    float r[32];
-    const bool full_cols = nc + 32 <= p.N;
-    if (p.R != nullptr) {
-      if (full_cols) {
-        const uint4* r4 = reinterpret_cast<const uint4*>(p.R + rbase + nc);
+        for (int u = 0; u < 8; ++u) {
+          float r[8];
+          bf16x8_to_f32(rv[u], r);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) bf16x8_to_f32(__ldg(r4 + u), r + 8 * u);
-      } else {
-        for (int e = 0; e < 32; ++e) r[e] = nc + e < p.N ? __bfloat162float(p.R[rbase + nc + e]) : 0.f;
+          for (int e = 0; e < 4; ++e) {
+            const float d0 = fmaf(p.alpha, __uint_as_float(a[8 * u + 2 * e]), p.beta * r[2 * e]);
+            const float d1 = fmaf(p.alpha, __uint_as_float(a[8 * u + 2 * e + 1]), p.beta * r[2 * e + 1]);
+            o[4 * u + e] = pack_bf16x2(d0, d1);
+          }
+        }
+        uint8_t* sb = out + (cc & 1) * Cfg::kOut;
+        if (et == 0) bulk_wait_group_read1();  // the store that last used this buffer has read it
+        epi_bar_sync();
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(sb + row * 128 + ((j ^ (row & 7)) << 4)) =
+              make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        fence_proxy_async_smem();
+        epi_bar_sync();
+        if (et == 0) {
+          tma_store_3d(&maps.d, sb, n0 + 64 * c, m0, z);
+          bulk_commit_group();
+        }
+        if (c + 1 < nvc) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) rv[u] = rn[u];
+        }
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 32; ++e) r[e] = 0.f;
     }
-    uint32_t o[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const float d0 = fmaf(p.alpha, __uint_as_float(a[2 * e]), p.beta * r[2 * e]);
-      const float d1 = fmaf(p.alpha, __uint_as_float(a[2 * e + 1]), p.beta * r[2 * e + 1]);
-      o[e] = pack_bf16x2(d0, d1);
-    }
-    if (full_cols) {
-      uint4* d4 = reinterpret_cast<uint4*>(p.D + rbase + nc);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) d4[u] = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
-    } else {
-      const __nv_bfloat16* ob = reinterpret_cast<const __nv_bfloat16*>(o);
-      for (int e = 0; e < 32 && nc + e < p.N; ++e) p.D[rbase + nc + e] = ob[e];
-    }
+    if (et == 0) bulk_wait_group0();
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, Cfg::kTmemCols);
   }
 }
 
-// Frobenius normalisation, one CTA per matrix, as the listing's bf16 tensor operations round:
-//   nrm = bf16(sqrt(sum x^2)) (fp32 sum), t = bf16(nrm * 1.02), den = bf16(t + 1e-6), X = bf16(G / den).
-__global__ void __launch_bounds__(512) frob_normalize_kernel(const __nv_bfloat16* G, __nv_bfloat16* X, long long mn) {
-  __shared__ float part[16];
-  __shared__ float s_den;
-  const __nv_bfloat16* g = G + blockIdx.x * mn;
-  __nv_bfloat16* x = X + blockIdx.x * mn;
-  float ss = 0.f;
-  for (long long i = threadIdx.x; i < mn; i += blockDim.x) {
-    const float v = __bfloat162float(g[i]);
-    ss = fmaf(v, v, ss);
-  }
+// Frobenius normalisation in two passes over chunks of `chunk` elements (a multiple of 2048; 256
+// threads, eight 16-byte vectors each per 2048 elements), grid (chunks, batch):
+//   frob_partial_kernel: part[z][c] = fp32 sum of x^2 over chunk c of matrix z;
+//   frob_scale_kernel:   every CTA sums part[z][*] in one fixed order (so all chunks of a matrix see the
+//                        same norm), then rounds as the listing's bf16 operations do:
+//                        nrm = bf16(sqrt(sum)), t = bf16(nrm * 1.02), den = bf16(t + 1e-6),
+//                        X = bf16(G / den).
+// X may alias G: each element is read and then written by the same thread of the second pass.
+__device__ __forceinline__ float block_sum_256(float v, float* red) {
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
-  if (threadIdx.x == 0) {
+  float t = 0.f;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < 8; ++w) t += red[w];
+  return t;
+}
+
+__global__ void __launch_bounds__(256) frob_partial_kernel(const __nv_bfloat16* G, float* part, long long mn,
+                                                           int chunk) {
+  __shared__ float red[8];
+  const long long base = static_cast<long long>(blockIdx.y) * mn;
+  const long long c0 = static_cast<long long>(blockIdx.x) * chunk;
+  const long long c1 = c0 + chunk < mn ? c0 + chunk : mn;
+  float ss = 0.f;
+  for (long long i0 = c0 + 8 * threadIdx.x; i0 < c1; i0 += 8 * 256 * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const long long i = i0 + static_cast<long long>(u) * 8 * 256;
+      v[u] = i < c1 ? __ldg(reinterpret_cast<const uint4*>(G + base + i)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      float f[8];
+      bf16x8_to_f32(v[u], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+    }
+  }
+  const float t = block_sum_256(ss, red);
+  if (threadIdx.x == 0) part[static_cast<long long>(blockIdx.y) * gridDim.x + blockIdx.x] = t;
+}
+
+__global__ void __launch_bounds__(256) frob_scale_kernel(const __nv_bfloat16* G, __nv_bfloat16* X,
+                                                         const float* part, long long mn, int chunk) {
+  __shared__ float s_den;
+  if (threadIdx.x < 32) {
+    const float* pz = part + static_cast<long long>(blockIdx.y) * gridDim.x;
     float t = 0.f;
-    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += part[w];
-    const float nrm = __bfloat162float(__float2bfloat16_rn(__fsqrt_rn(t)));
-    const float t1 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(nrm, 1.02f)));
-    s_den = __bfloat162float(__float2bfloat16_rn(__fadd_rn(t1, 1e-6f)));
+    for (int c = threadIdx.x; c < static_cast<int>(gridDim.x); c += 32) t += pz[c];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    if (threadIdx.x == 0) {
+      const float nrm = __bfloat162float(__float2bfloat16_rn(__fsqrt_rn(t)));
+      const float t1 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(nrm, 1.02f)));
+      s_den = __bfloat162float(__float2bfloat16_rn(__fadd_rn(t1, 1e-6f)));
+    }
   }
   __syncthreads();
   const float den = s_den;
-  for (long long i = threadIdx.x; i < mn; i += blockDim.x) x[i] = __float2bfloat16_rn(__fdiv_rn(__bfloat162float(g[i]), den));
+  const long long base = static_cast<long long>(blockIdx.y) * mn;
+  const long long c0 = static_cast<long long>(blockIdx.x) * chunk;
+  const long long c1 = c0 + chunk < mn ? c0 + chunk : mn;
+  for (long long i0 = c0 + 8 * threadIdx.x; i0 < c1; i0 += 8 * 256 * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const long long i = i0 + static_cast<long long>(u) * 8 * 256;
+      if (i < c1) v[u] = *reinterpret_cast<const uint4*>(G + base + i);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const long long i = i0 + static_cast<long long>(u) * 8 * 256;
+      if (i >= c1) continue;
+      float f[8];
+      bf16x8_to_f32(v[u], f);
+      uint4 o;
+      o.x = pack_bf16x2(__fdiv_rn(f[0], den), __fdiv_rn(f[1], den));
+      o.y = pack_bf16x2(__fdiv_rn(f[2], den), __fdiv_rn(f[3], den));
+      o.z = pack_bf16x2(__fdiv_rn(f[4], den), __fdiv_rn(f[5], den));
+      o.w = pack_bf16x2(__fdiv_rn(f[6], den), __fdiv_rn(f[7], den));
+      *reinterpret_cast<uint4*>(X + base + i) = o;
+    }
+  }
 }
 
 }  // namespace swa

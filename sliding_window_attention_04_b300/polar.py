@@ -18,7 +18,7 @@ EXPORTED = ("pe_workspace_bytes", "pe_normalize", "pe_step", "polar_express")
 _c = ctypes
 lib.pe_workspace_bytes.argtypes = [_c.c_int, _c.c_int, _c.c_int]
 lib.pe_workspace_bytes.restype = _c.c_size_t
-lib.pe_normalize.argtypes = [_c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int, _c.c_int, _c.c_void_p]
+lib.pe_normalize.argtypes = [_c.c_void_p, _c.c_void_p] + [_c.c_int] * 3 + [_c.c_void_p, _c.c_size_t, _c.c_void_p]
 lib.pe_normalize.restype = _c.c_int
 lib.pe_step.argtypes = [_c.c_void_p, _c.c_void_p] + [_c.c_int] * 4 + [_c.c_void_p, _c.c_size_t, _c.c_void_p]
 lib.pe_step.restype = _c.c_int
@@ -58,12 +58,16 @@ def _stream(s, device):
     return _c.c_void_p(s.cuda_stream or None)
 
 
-def normalize(g: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+def normalize(g: torch.Tensor, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+              stream=None) -> torch.Tensor:
     _check("g", g)
     batch, m, n = _dims(g)
     out = torch.empty_like(g) if out is None else out
     _check("out", out, g.shape)
-    rc = lib.pe_normalize(g.data_ptr(), out.data_ptr(), batch, m, n, _stream(stream, g.device))
+    nbytes = workspace_bytes(batch, m, n)
+    ws = _workspace(workspace, nbytes, g.device)
+    rc = lib.pe_normalize(g.data_ptr(), out.data_ptr(), batch, m, n, ws.data_ptr(), ws.numel(),
+                          _stream(stream, g.device))
     if rc != ATTN_OK:
         raise AttnError(rc, "pe_normalize")
     return out

@@ -228,4 +228,10 @@ def test_polar_host_validation_codes(binding):
     assert lib.pe_step(x, y, 2, 64, 96, 0, ws + 16, nb, None) == E.ATTN_ERR_INVALID_ARG  # workspace alignment
     assert lib.polar_express(x, y, 2, 64, 96, 6, ws, nb, None) == E.ATTN_ERR_INVALID_ARG
     assert lib.polar_express(x, y, 2, 64, 96, 5, ws, nb, None) == E.ATTN_ERR_NOT_INITIALIZED
-    assert lib.pe_normalize(x, y, 0, 64, 96, None) == E.ATTN_ERR_INVALID_ARG
+    assert lib.pe_normalize(x, y, 0, 64, 96, ws, nb, None) == E.ATTN_ERR_INVALID_ARG
+    assert lib.pe_normalize(x, y, 2, 64, 96, ws, nb - 256, None) == E.ATTN_ERR_INVALID_ARG  # no room for the partials
+    assert lib.pe_normalize(x, x + 64, 2, 64, 96, ws, nb, None) == E.ATTN_ERR_INVALID_ARG  # partial overlap
+    assert lib.pe_normalize(x, x, 2, 64, 96, ws, nb, None) == E.ATTN_ERR_NOT_INITIALIZED   # in place is allowed
+    # the partial sums: at most 1024 per matrix, 16384 elements per chunk for small matrices
+    big = polar.workspace_bytes(1, 4096, 8192)
+    assert big >= 2 * 4096 * 4096 * 2 + 4096 * 8192 * 2 + 1024 * 4

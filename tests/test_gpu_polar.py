@@ -87,3 +87,21 @@ def test_model_shaped_batches(polar):
         f64 = pe.polar_express(_f64(g))
         rel = np.linalg.norm(_f64(full) - f64) / np.linalg.norm(f64)
         assert rel < 5e-2, (m, n, rel)
+
+
+def test_normalize_in_place_and_many_chunks(polar):
+    """In place equals out of place; a 2048 x 8192 matrix spans 1024 chunks of the two-pass sum and still
+    lies within the rounded oracle's radius; two calls agree bit for bit."""
+    g = torch.randn(3, 200, 72, generator=torch.Generator().manual_seed(9)).to(torch.bfloat16).cuda()
+    ref = polar.normalize(g)
+    h = g.clone()
+    polar.normalize(h, out=h)
+    torch.cuda.synchronize()
+    assert torch.equal(h, ref)
+    big = (torch.randn(1, 2048, 8192, generator=torch.Generator().manual_seed(10)) * 3.0).to(torch.bfloat16)
+    x1 = polar.normalize(big.cuda())
+    x2 = polar.normalize(big.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(x1, x2)
+    r, rad = pe.normalize_rounded(big)
+    _within("normalize 2048x8192", _f64(x1), r, rad)
