@@ -46,13 +46,14 @@ struct SchedSlot {
 // on the same buffers skip the encoding.
 struct MapKey {
   const void* base;
-  int B, H, T, D;
+  int B, H, T, D, rows;
   bool operator<(const MapKey& o) const {
     if (base != o.base) return base < o.base;
     if (B != o.B) return B < o.B;
     if (H != o.H) return H < o.H;
     if (T != o.T) return T < o.T;
-    return D < o.D;
+    if (D != o.D) return D < o.D;
+    return rows < o.rows;
   }
 };
 constexpr size_t kMapCacheMax = 1024;
@@ -121,17 +122,18 @@ cudaError_t set_ws_attrs(bool* usable) {
   return cudaSuccess;
 }
 
-// 4-D view (d, h, t, b) of a [B, T, H, D] bf16 tensor; one box is one 128-row tile of one head,
-// written to shared memory in the tensor core's swizzled layout (128-byte rows: 128-byte swizzle,
-// 64-byte rows: 64-byte swizzle). Rows past T read as zero and are not written by stores.
+// 4-D view (d, h, t, b) of a [B, T, H, D] bf16 tensor; one box is `rows` rows (a 128-row tile, or
+// the 32 rows of one warp for the forward's output) of one head, in shared memory in the tensor
+// core's swizzled layout (128-byte rows: 128-byte swizzle, 64-byte rows: 64-byte swizzle). Rows past
+// T read as zero and are not written by stores.
 CUresult encode_tile_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* map, const void* base, int B,
-                         int H, int T, int D) {
+                         int H, int T, int D, int rows = swa::kTile) {
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T),
                               static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
                                  static_cast<cuuint64_t>(T) * H * D * 2};
   // D = 128 rows are 256 bytes: a box covers 64 columns (the 128-byte swizzle span), two per tile
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(D > 64 ? 64 : D), 1, static_cast<cuuint32_t>(swa::kTile), 1};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(D > 64 ? 64 : D), 1, static_cast<cuuint32_t>(rows), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
@@ -187,12 +189,12 @@ cudaError_t launch_simple(const swa::AttnParams& p, cudaStream_t stream) {
 
 // The cached tensor map of a [B, T, H, D] bf16 tensor at `base` (encoded on first use).
 const CUtensorMap* cached_map(std::map<MapKey, CUtensorMap>& cache, PFN_cuTensorMapEncodeTiled_v12000 encode,
-                              const void* base, int B, int H, int T, int D) {
-  const MapKey key{base, B, H, T, D};
+                              const void* base, int B, int H, int T, int D, int rows = swa::kTile) {
+  const MapKey key{base, B, H, T, D, rows};
   auto it = cache.find(key);
   if (it != cache.end()) return &it->second;
   CUtensorMap m;
-  if (encode_tile_map(encode, &m, base, B, H, T, D) != CUDA_SUCCESS) return nullptr;
+  if (encode_tile_map(encode, &m, base, B, H, T, D, rows) != CUDA_SUCCESS) return nullptr;
   if (cache.size() >= kMapCacheMax) cache.clear();
   return &cache.emplace(key, m).first->second;
 }
@@ -204,7 +206,7 @@ int launch_ws(const swa::AttnParams& p, std::map<MapKey, CUtensorMap>& cache,
   const CUtensorMap* mq = cached_map(cache, encode, p.q, p.B, p.H, p.T, D);
   const CUtensorMap* mk = cached_map(cache, encode, p.k, p.B, p.Hkv, p.T, D);
   const CUtensorMap* mv = cached_map(cache, encode, p.v, p.B, p.Hkv, p.T, D);
-  const CUtensorMap* mo = cached_map(cache, encode, p.out, p.B, p.H, p.T, D);
+  const CUtensorMap* mo = cached_map(cache, encode, p.out, p.B, p.H, p.T, D, swa::kOutRows);
   if (!mq || !mk || !mv || !mo) return ATTN_ERR_CUDA;
   maps.q = *mq;
   maps.k = *mk;

@@ -49,8 +49,10 @@
 // gets zero P without exponentials, and only a block that the mask edge cuts is masked element
 // by element; tiles without any masked entry skip the mask tests. The running max is updated lazily:
 // O and l are rescaled only when the tile max exceeds the current reference by more than
-// kRescaleLog2. At the end of a unit the softmax warps normalise O_t, stage it as bf16 in the (now
-// free) Q tile buffer, store it by TMA (one box; two at D = 128), and write the per-row log-sum-exp.
+// kRescaleLog2. At the end of a unit the softmax warps normalise O_t and store it as bf16, each
+// thread its own row, and write the per-row log-sum-exp. A Q slot is freed as soon as the unit's last
+// S job has read its Q^ tiles (and every role has read the slot's unit id and geometry), so the
+// producer loads the Q tiles of the unit after next while the current unit still runs.
 //
 // Registers: the kernel is compiled to 96 per thread (640 x 96 = 61440); at start the warpgroups
 // re-divide them with setmaxnreg: softmax 128, prologue 80, producer/MMA group 64, i.e.
@@ -67,25 +69,45 @@
 
 namespace swa {
 
+// Arrivals that free a Q slot for the unit two ahead: the S issuer's commit after the unit's last S
+// job (its Q^ tiles are no longer read), both P.V issuers and the eight softmax warps once they have
+// read the slot's unit id and geometry.
+constexpr int kQEmptyArrivals = 1 + 2 + 8;
+
+// Rows of the output box one softmax warp stages and stores (its 32 rows of the query tile).
+constexpr int kOutRows = 32;
+
+// Byte offset of 16-byte chunk `ch` of row `row` in a staged output box (the tensor map's swizzle:
+// 128-byte rows with the 128-byte pattern, 64-byte rows at D = 32 with the 64-byte pattern).
+template <int D>
+__device__ __forceinline__ uint32_t out_stage_off(int row, int ch) {
+  if constexpr (D >= 64) return static_cast<uint32_t>(row * 128 + ((ch ^ (row & 7)) << 4));
+  else return static_cast<uint32_t>(row * 64 + ((ch ^ ((row >> 1) & 3)) << 4));
+}
+
 template <int D>
 struct WsCfg {
   using G = TileGeom<D>;
   static constexpr int kThreads = 640;
   static constexpr int kLaunchRegs = 96;  // per thread at launch; the run-time split adds up to it
   // D = 128: 32 KB tiles and 128-column O accumulators; one Q slot (the next unit's Q is loaded
-  // after the current unit's epilogues), a 2-stage ring and two S/P buffers fit shared memory and TMEM.
+  // once the current unit's S jobs are done), a 2-stage ring and two S/P buffers fit shared memory
+  // and TMEM.
   static constexpr int kQSlots = D == 128 ? 1 : 2;       // units whose Q tiles are resident at once
   static constexpr int kStages = D == 128 ? 2 : 4;       // K/V ring depth
   static constexpr int kSBufs = D == 128 ? 2 : 3;        // S/P buffers in TMEM
   static constexpr int kTileBytes = G::kBytes;           // one 128 x D bf16 tile
-  static constexpr int kOffQ = 0;                        // [kQSlots][2 tiles] Q^ / output staging
+  static constexpr int kOffQ = 0;                        // [kQSlots][2 tiles] Q^
   static constexpr int kOffK = kOffQ + 2 * kQSlots * kTileBytes;  // [kStages] K^ (transformed in place)
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  // output staging: one box of kOutRows rows x min(D, 64) columns per softmax warp
+  static constexpr int kOutBytes = kOutRows * (D > 64 ? 64 : D) * 2;
+  static constexpr int kOffOut = kOffV + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffOut + 8 * kOutBytes;
   // barrier indices
   static constexpr int kBarQFull = 0;                     // [2] TMA -> prologue
   static constexpr int kBarQReady = 2;                    // [2] prologue -> MMA
-  static constexpr int kBarQEmpty = 4;                    // [2] slot free (epilogue stores, P.V issuers) -> producer
+  static constexpr int kBarQEmpty = 4;                    // [2] slot free (S issuer, P.V issuers, softmax warps) -> producer
   static constexpr int kBarUnit = 6;                      // [2] producer -> MMA, softmax (unit id)
   static constexpr int kBarKFull = 8;                     // [kStages] TMA -> prologue
   static constexpr int kBarKReady = kBarKFull + kStages;  // [kStages] prologue -> S issuer
@@ -97,11 +119,11 @@ struct WsCfg {
   static constexpr int kBarPFull = kBarBufFree + kSBufs;  // [2 tiles][2] softmax t wrote P of job n -> P.V issuer t
   static constexpr int kBarPVDone = kBarPFull + 4;        // [2 tiles][2] P.V job n of tile t done -> softmax, S issuer
   static constexpr int kBarFinal = kBarPVDone + 4;        // [3] MMA drain at exit (S issuer, P.V issuers)
-  static constexpr int kBarEpi = kBarFinal + 3;           // [2] tile t's four softmax warps are done with the unit
-  static constexpr int kBarVReady = kBarEpi + 2;          // [kStages] gated calls: prologue gated V -> P.V issuers
+  static constexpr int kBarVReady = kBarFinal + 3;        // [kStages] gated calls: prologue gated V -> P.V issuers
   static constexpr int kNumBars = kBarVReady + kStages;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, unit ids, unit geometry
   static constexpr int kSmemBytes = kOffMisc + 128 + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   // TMEM columns
   static constexpr uint32_t kTmemCols = 512;
   static __device__ __forceinline__ uint32_t col_buf(int b) { return static_cast<uint32_t>(128 * b); }
@@ -391,7 +413,8 @@ __device__ __forceinline__ void gate_half_row_inplace(uint8_t* tile, int row, in
 }
 
 struct WsMaps {
-  CUtensorMap q, k, v, out;  // 4-D (D, H, T, B) views, box (D, 1, 128, 1), swizzled
+  CUtensorMap q, k, v;  // 4-D (D, H, T, B) views, box (min(D, 64), 1, 128, 1), swizzled
+  CUtensorMap out;      // the same view of the output, box (min(D, 64), 1, kOutRows, 1)
 };
 
 // Visible columns of one 32-column block as a bit mask (bit c set: column c visible), for the
@@ -590,7 +613,7 @@ __global__ void __launch_bounds__(640, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(Cfg::kBarQFull + i), 1);
       mbar_init(bar(Cfg::kBarQReady + i), 8);
-      mbar_init(bar(Cfg::kBarQEmpty + i), 4);
+      mbar_init(bar(Cfg::kBarQEmpty + i), kQEmptyArrivals);
       mbar_init(bar(Cfg::kBarUnit + i), 1);
     }
     for (int i = 0; i < 4; ++i) {
@@ -607,7 +630,6 @@ __global__ void __launch_bounds__(640, 1)
     }
     for (int i = 0; i < NB; ++i) mbar_init(bar(Cfg::kBarBufFree + i), 1);
     for (int i = 0; i < 3; ++i) mbar_init(bar(Cfg::kBarFinal + i), 1);
-    for (int i = 0; i < 2; ++i) mbar_init(bar(Cfg::kBarEpi + i), 4);
     for (int i = 0; i < S; ++i) mbar_init(bar(Cfg::kBarVReady + i), 8);
     *abort_flag = 0;
     fence_mbar_init();
@@ -635,7 +657,6 @@ __global__ void __launch_bounds__(640, 1)
       prefetch_tmap(&maps.q);
       prefetch_tmap(&maps.k);
       prefetch_tmap(&maps.v);
-      prefetch_tmap(&maps.out);
       const uint64_t pol_stream = policy_evict_first();
       const uint64_t pol_keep = policy_evict_last();
       int q_armed[2] = {-1, -1};  // parity of the last armed phase of each Q barrier (for draining)
@@ -797,6 +818,8 @@ __global__ void __launch_bounds__(640, 1)
           // K^ of this stage no longer read (unless the next unit reuses it)
           if (ok && i < n_st - g.r_out) umma_commit(bar(Cfg::kBarKFree + st));
         }
+        // the unit's Q^ tiles are no longer read once its last S job completes
+        if (ok) umma_commit(bar(Cfg::kBarQEmpty + slot));
       }
       if (!ok) fail();
       umma_commit(bar(Cfg::kBarFinal + 0));
@@ -817,9 +840,7 @@ __global__ void __launch_bounds__(640, 1)
         const int unit = unit_id[slot];
         if (unit < 0) break;
         const UnitGeom g = unit_geo[slot];
-        // The slot's unit id and geometry have been read: the producer may reuse the slot once the
-        // epilogues are done too. (An issuer whose query tile lies past T has no P.V job in the
-        // unit, so without this arrival the epilogues alone would not order its read.)
+        // The slot's unit id and geometry have been read (one of the arrivals that free the slot).
         mbar_arrive(bar(Cfg::kBarQEmpty + slot));
         const int n_st = g.n_steps();
         for (int i = 0; i < n_st; ++i) {
@@ -947,6 +968,9 @@ __global__ void __launch_bounds__(640, 1)
       const int unit = unit_id[slot];
       if (unit < 0) break;
       const UnitGeom g = unit_geo[slot];
+      // the slot's unit id and geometry have been read (the arrival releases the reads)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Cfg::kBarQEmpty + slot));
       const int qs = g.qs0 + kTile * t;
       const int i_row = qs + r;
       float m_used = fixed_ref ? p.ref_log2 : -INFINITY;  // reference max of this row (log2 units)
@@ -1004,60 +1028,52 @@ __global__ void __launch_bounds__(640, 1)
         ++n;
       }
       if (!ok) break;
-      // The tile's four warps meet on the epilogue barrier once per unit (after staging their rows of
-      // the output): each arrives, then waits for the phase, with the bounded wait. Every warp waits,
-      // so none can arrive for a later unit before all four have arrived for this one.
-      const bool stores = (warp & 3) == 0;
-      if (!g.valid(t)) {  // this query tile lies past T
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(Cfg::kBarEpi + t));
-        ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarEpi + t), ul & 1, abort_flag));
-        if (ok && stores && r == 0) mbar_arrive(bar(Cfg::kBarQEmpty + slot));
-        if (!ok) break;
-        continue;
-      }
-      // ---- epilogue: O / l -> bf16 staged in this tile's Q buffer, one TMA store; LSE ----
+      if (!g.valid(t)) continue;  // this query tile lies past T
+      // ---- epilogue: O / l -> bf16; each warp stages its 32 rows and stores them by TMA; LSE ----
       ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarPVDone + 2 * t + ((n - 1) & 1)),
                                                       ((n - 1) >> 1) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
       const float inv_l = l_run > 0.f ? __frcp_rn(l_run) : 0.f;  // = 1 / l_run, correctly rounded
-      uint8_t* stage = q_tile(slot, t);
+      const bool row_in = i_row < p.T;
+      const int row0 = qs + kOutRows * (warp & 3);  // first row of this warp's box
+      uint8_t* stg = smem + Cfg::kOffOut + warp * Cfg::kOutBytes;
+      constexpr int kBoxCols = D > 64 ? 64 : D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + 32 * c, o);
-        tmem_ld_wait();
-        reg_fence<32>(o);
+      for (int x = 0; x < kBoxes; ++x) {
+        // the buffer is free once this warp's previous store from it has been read
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+#pragma unroll 1
+        for (int cc = 0; cc < kBoxCols / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tO + kBoxCols * x + 32 * cc, o);
+          tmem_ld_wait();
+          reg_fence<32>(o);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 u;
-          u.x = pack_bf16x2(__uint_as_float(o[q * 8 + 0]) * inv_l, __uint_as_float(o[q * 8 + 1]) * inv_l);
-          u.y = pack_bf16x2(__uint_as_float(o[q * 8 + 2]) * inv_l, __uint_as_float(o[q * 8 + 3]) * inv_l);
-          u.z = pack_bf16x2(__uint_as_float(o[q * 8 + 4]) * inv_l, __uint_as_float(o[q * 8 + 5]) * inv_l);
-          u.w = pack_bf16x2(__uint_as_float(o[q * 8 + 6]) * inv_l, __uint_as_float(o[q * 8 + 7]) * inv_l);
-          *reinterpret_cast<uint4*>(stage + tile_off<D>(r, 4 * c + q)) = u;
+          for (int q = 0; q < 4; ++q) {
+            uint4 u;
+            u.x = pack_bf16x2(__uint_as_float(o[q * 8 + 0]) * inv_l, __uint_as_float(o[q * 8 + 1]) * inv_l);
+            u.y = pack_bf16x2(__uint_as_float(o[q * 8 + 2]) * inv_l, __uint_as_float(o[q * 8 + 3]) * inv_l);
+            u.z = pack_bf16x2(__uint_as_float(o[q * 8 + 4]) * inv_l, __uint_as_float(o[q * 8 + 5]) * inv_l);
+            u.w = pack_bf16x2(__uint_as_float(o[q * 8 + 6]) * inv_l, __uint_as_float(o[q * 8 + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(stg + out_stage_off<D>(lane, 4 * cc + q)) = u;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && row0 < p.T) {
+          tma_store_4d(&maps.out, stg, kBoxCols * x, g.h, row0, g.b);
+          bulk_commit_group();
         }
       }
-      if (p.lse != nullptr && i_row < p.T) {
+      if (p.lse != nullptr && row_in) {
         const float m_fin = m_used == -INFINITY ? 0.f : m_used;
         p.lse[(static_cast<size_t>(g.b) * p.H + g.h) * p.T + i_row] = (m_fin + __log2f(l_run)) * 0.69314718055994531f;
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(Cfg::kBarEpi + t));
-      ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarEpi + t), ul & 1, abort_flag));
-      if (ok && stores && r == 0) {
-#pragma unroll
-        for (int x = 0; x < kBoxes; ++x) tma_store_4d(&maps.out, stage + x * kTile * 128, 64 * x, g.h, qs, g.b);
-        bulk_commit_group();
-        bulk_wait_group_read0();
-        mbar_arrive(bar(Cfg::kBarQEmpty + slot));
-      }
-      if (!ok) break;
     }
     if (!ok && lane == 0) fail();
-    if (r == 0) bulk_wait_group0();
+    if (lane == 0) bulk_wait_group0();  // this warp's output stores are complete
   }
 
   tc_fence_before();

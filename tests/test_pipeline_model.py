@@ -90,7 +90,7 @@ def valid(g, t):
 
 
 class CTA:
-    def __init__(self, units, S, NB, QS, rng, rescale_prob=0.3):
+    def __init__(self, units, S, NB, QS, rng, rescale_prob=0.3, q_release=True, softmax_release=True):
         self.units, self.S, self.NB, self.QS, self.rng = units, S, NB, QS, rng
         self.rescale_prob = rescale_prob
         b = {}
@@ -98,23 +98,27 @@ class CTA:
         def mk(name, count, n=1):
             b[name] = [Bar(f"{name}[{i}]", count) for i in range(n)]
 
-        mk("QFull", 1, 2); mk("QReady", 8, 2); mk("QEmpty", 4, 2); mk("Unit", 1, 2)
+        # a Q slot is freed by the S issuer's commit after the unit's last S job, both P.V issuers and
+        # the eight softmax warps (after reading the slot's unit id and geometry)
+        mk("QFull", 1, 2); mk("QReady", 8, 2); mk("Unit", 1, 2)
+        mk("QEmpty", (1 if q_release else 0) + 2 + (8 if softmax_release else 0), 2)
+        self.q_release, self.softmax_release = q_release, softmax_release
         mk("KFull", 1, S); mk("KReady", 8, S); mk("VFull", 1, S); mk("KFree", 1, S); mk("VFree", 2, S)
         mk("SFull", 1, 4); mk("BufFree", 1, NB); mk("PFull", 4, 4); mk("PVDone", 1, 4); mk("Final", 1, 3)
-        mk("Epi", 4, 2)
         self.b = b
         # shared state of the CTA
         self.unit_id = [None, None]
         self.unit_geo = [None, None]
-        self.qtile = {}      # (slot, t) -> ("raw"|"hat"|"out", unit index)
+        self.qtile = {}      # (slot, t) -> ("raw"|"hat"|"free", unit index)
+        self.q_left = {}     # (slot, t) -> S jobs of the slot's unit still to read the Q^ tile
         self.kstage = {}     # stage -> ("raw"|"hat", (bh, j)) ; K
         self.vstage = {}     # stage -> (bh, j) ; V
         self.buf = {}        # (buffer, warp) -> ("S"|"P"|"Pread", global job): the warp's 32 TMEM lanes
-        self.o = [None, None]  # O_t: (unit index, job index in tile of the last P.V), or ("read", unit)
+        self.o = [None, None]  # O_t: (unit index, job index in tile of the last P.V)
+        self.o_read = [{}, {}]  # tile t: softmax warp -> the unit whose O rows it has read
         self.pipe = []       # tensor pipe queue
         self.tma = []        # loads in flight
         self.jobs = {}       # global S job -> dict(t, unit, j, slot, pos, n)
-        self.done_epi = []
 
     # ---- helpers used by the roles ----
     def wait(self, bar, k):
@@ -138,7 +142,7 @@ def producer(c):
         two = valid(g, 1)
         c.b["QFull"][slot].arrive(tx=2 if two else 1)
         for t in range(2 if two else 1):
-            assert c.qtile.get((slot, t), ("free",))[0] in ("free", "stored"), "Q slot reloaded while in use"
+            assert c.qtile.get((slot, t), ("free",))[0] == "free", "Q slot reloaded while in use"
             c.tma.append(("Q", (slot, t), ul, c.b["QFull"][slot]))
         for i in range(g["r_in"], g["n"]):
             j = g["ke_all"] - i
@@ -204,6 +208,8 @@ def s_issuer(c, pv_lag=True, buf_free=True):
         yield c.wait(c.b["QReady"][slot], ph)
         g = dict(c.unit_geo[slot])
         n_st = g["n"]
+        for t in range(2):
+            c.q_left[(slot, t)] = sum(has(g, t, g["ke_all"] - i) for i in range(n_st))
         for i in range(n_st):
             j = g["ke_all"] - i
             if i < g["r_in"]:
@@ -231,6 +237,8 @@ def s_issuer(c, pv_lag=True, buf_free=True):
                 gS += 1
             if i < n_st - g["r_out"]:
                 c.pipe.append(("commit", c.b["KFree"][st]))
+        if c.q_release:
+            c.pipe.append(("commit", c.b["QEmpty"][slot]))
     c.pipe.append(("commit", c.b["Final"][0]))
     yield c.wait(c.b["Final"][0], 0)
 
@@ -278,7 +286,7 @@ def pv_issuer(c, t):
     yield c.wait(c.b["Final"][1 + t], 0)
 
 
-def softmax(c, t, w, all_wait=True):
+def softmax(c, t, w):
     QS, NB = c.QS, c.NB
     n = 0
     gS = 0
@@ -289,6 +297,8 @@ def softmax(c, t, w, all_wait=True):
             return
         u = c.unit_id[slot]
         g = dict(c.unit_geo[slot])
+        if c.softmax_release:
+            c.b["QEmpty"][slot].arrive()
         for j in range(g["ke_all"], g["kb_all"] - 1, -1):
             h0, h1 = has(g, 0, j), has(g, 1, j)
             gj = gS + (1 if (t == 1 and h0) else 0)
@@ -308,26 +318,14 @@ def softmax(c, t, w, all_wait=True):
             c.buf[(b, w)] = ("P", gj)
             c.b["PFull"][2 * t + (n & 1)].arrive()
             n += 1
-        stores = w == 0
         if not valid(g, t):
-            c.b["Epi"][t].arrive()
-            if all_wait or stores:
-                yield c.wait(c.b["Epi"][t], ul)
-            if stores:
-                c.b["QEmpty"][slot].arrive()
             continue
+        # epilogue: every warp reads its own rows of O_t and stores them
         yield c.wait(c.b["PVDone"][2 * t + ((n - 1) & 1)], (n - 1) >> 1)
         assert c.o[t] == (u, n - 1), f"epilogue of O_{t} unit {u} sees {c.o[t]}"
-        cur = c.qtile[(slot, t)]
-        assert cur == ("hat", u), f"epilogue stages over Q {cur}"
         yield ("work",)
-        c.b["Epi"][t].arrive()
-        if all_wait or stores:
-            yield c.wait(c.b["Epi"][t], ul)
-        if stores:
-            c.qtile[(slot, t)] = ("stored", u)
-            c.o[t] = ("read", u)
-            c.b["QEmpty"][slot].arrive()
+        assert c.o[t] == (u, n - 1), f"O_{t} overwritten while warp {w} reads it"
+        c.o_read[t][w] = u
 
 
 def tensor_pipe(c):
@@ -349,6 +347,10 @@ def tensor_pipe(c):
             assert c.kstage[J["pos"] % c.S] == ("hat", (J["bh"], J["j"])), "S reads the wrong K stage"
             for w in range(4):
                 c.buf[(b, w)] = ("S", op[1])
+            key = (J["slot"], J["t"])
+            c.q_left[key] -= 1
+            if c.q_left[key] == 0:  # the unit's last reader of this Q^ tile
+                c.qtile[key] = ("free", J["unit"])
         else:  # P.V
             J = c.jobs[op[1]]
             t, n = J["t"], J["n"]
@@ -357,7 +359,10 @@ def tensor_pipe(c):
                 assert got == ("P", op[1]), f"P.V {op[1]} reads buffer {J['buf']} lanes of warp {w}: {got}"
             assert c.vstage[J["pos"] % c.S] == (J["bh"], J["j"]), "P.V reads the wrong V stage"
             if J["first"]:
-                assert c.o[t] is None or c.o[t][0] == "read", f"O_{t} restarted before its epilogue: {c.o[t]}"
+                if c.o[t] is not None:
+                    prev = c.o[t][0]
+                    assert all(c.o_read[t].get(w) == prev for w in range(4)), \
+                        f"O_{t} restarted before every warp read unit {prev}: {c.o_read[t]}"
             else:
                 assert c.o[t] == (J["unit"], n - 1), f"O_{t} accumulation out of order: {c.o[t]}, job {n}"
             c.o[t] = (J["unit"], n)
@@ -384,16 +389,16 @@ def tma_engine(c):
         yield ("work",)
 
 
-def run_cta(units, S, NB, QS, seed, max_steps=2_000_000, all_wait=True, **issuer_flags):
+def run_cta(units, S, NB, QS, seed, max_steps=2_000_000, q_release=True, softmax_release=True, **issuer_flags):
     rng = random.Random(seed)
-    c = CTA(units, S, NB, QS, rng)
+    c = CTA(units, S, NB, QS, rng, q_release=q_release, softmax_release=softmax_release)
     procs = {"producer": producer(c), "s_issuer": s_issuer(c, **issuer_flags), "pv0": pv_issuer(c, 0),
              "pv1": pv_issuer(c, 1)}
     for w in range(8):
         procs[f"prologue{w}"] = prologue(c, w)
     for t in range(2):
         for w in range(4):
-            procs[f"softmax{t}.{w}"] = softmax(c, t, w, all_wait)
+            procs[f"softmax{t}.{w}"] = softmax(c, t, w)
     engines = {"tensor": tensor_pipe(c), "tma": tma_engine(c)}
     pending = {k: None for k in procs}  # the action each process is blocked on
     steps = 0
@@ -449,13 +454,14 @@ def test_protocol_has_no_deadlock_and_exact_waits(D, T, window, causal):
         assert all(b.completed == 1 for b in c.b["Final"])
 
 
-@pytest.mark.parametrize("flag", ["all_wait", "pv_lag", "buf_free"])
+@pytest.mark.parametrize("flag", ["pv_lag", "buf_free", "q_release", "softmax_release"])
 def test_model_catches_removed_rules(flag):
-    """Removing any one rule breaks the protocol somewhere: every softmax warp waiting on the epilogue
-    barrier (else a warp that runs through a following unit whose tile lies past T arrives twice and
-    completes the phase before another warp has staged its rows); the S issuer waiting for the tile's
-    P.V job n - 2 (else the two-slot S-done / P-written / P.V-done waits can fall two phases behind);
-    and the S issuer waiting for its buffer's previous P.V (else S overwrites P before it is read)."""
+    """Removing any one rule breaks the protocol somewhere: the S issuer waiting for the tile's P.V job
+    n - 2 (else the two-slot S-done / P-written / P.V-done waits can fall two phases behind); the S
+    issuer waiting for its buffer's previous P.V (else S overwrites P before it is read); the S
+    issuer's commit freeing a Q slot after the unit's last S job (else the producer reloads Q^ that S
+    jobs still read); and the softmax warps' arrival after reading a slot's unit (else the producer
+    publishes the unit two ahead before they have read it)."""
     failures = 0
     for D, T, window, causal in ((64, 300, -1, False), (64, 700, 100, True), (128, 513, 0, True),
                                  (64, 129, 5, True)):
