@@ -464,11 +464,11 @@ def test_model_catches_removed_rules(flag):
     publishes the unit two ahead before they have read it)."""
     failures = 0
     for D, T, window, causal in ((64, 300, -1, False), (64, 700, 100, True), (128, 513, 0, True),
-                                 (64, 129, 5, True)):
+                                 (64, 129, 5, True), (64, 600, 0, False)):
         S, NB, QS = CONFIGS[D]
         n_qb = (T + 2 * KT - 1) // (2 * KT)
         units = units_for(1, 3, T, window, causal, list(range(3 * ((n_qb + 1) // 2))), S)
-        for seed in range(15):
+        for seed in range(40):
             try:
                 run_cta(units, S, NB, QS, seed=seed, **{flag: False})
             except (Deadlock, AssertionError):
