@@ -34,6 +34,12 @@ extern "C" {
  * 1024 per matrix), each on a 256-byte boundary. 0 for a non-positive size. */
 size_t pe_workspace_bytes(int batch, int m, int n);
 
+/* pe_step_flops — the FLOPs one pe_step on this shape executes on the tensor cores (2 K per output
+ * element of the tiles its three products compute; A and B only on and above the diagonal), for
+ * roofline accounting on the current device. 0 for an invalid shape or before attn_init. The method's
+ * own count (the listing's products in full) is 4 s^2 l + 2 s^3 per matrix (s, l = min, max of m, n). */
+double pe_step_flops(int batch, int m, int n);
+
 /* pe_normalize — X = G / (||G||_F * 1.02 + 1e-6) per matrix (bf16 steps as above). X may equal G
  * (in place); otherwise G and X must not overlap, and neither may overlap the workspace (at least
  * pe_workspace_bytes(batch, m, n) bytes, 256-byte aligned). The sum of squares is taken in fp32 over
@@ -42,8 +48,11 @@ int pe_normalize(const void* G, void* X, int batch, int m, int n, void* workspac
                  void* stream);
 
 /* pe_step — one step with the listing's coefficient triple number `step` (0..4): Y from X. X and Y
- * must not overlap each other or the workspace. After the call (when the stream reaches it) the
- * workspace starts with that step's A and then B ([batch, s, s] bf16 each, s = min(m, n)). */
+ * must not overlap each other or the workspace. A and B are symmetric: only their 128 x 128 blocks on
+ * and above the diagonal are computed, and the products that read them take a block below the
+ * diagonal as the transpose of its mirror. After the call (when the stream reaches it) the workspace
+ * starts with that step's A and then B ([batch, s, s] bf16 each, s = min(m, n)); their blocks below
+ * the diagonal hold no data. */
 int pe_step(const void* X, void* Y, int batch, int m, int n, int step, void* workspace, size_t workspace_bytes,
             void* stream);
 

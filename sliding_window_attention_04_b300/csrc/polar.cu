@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "attn.h"
@@ -93,50 +94,90 @@ CUresult encode3d(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* map, co
 std::mutex g_pe_mu;
 int g_pe_device = -1;
 
-template <bool A_MN, bool B_MN, int BN>
+template <int A, int B, int BN>
 cudaError_t set_attr_one() {
-  return cudaFuncSetAttribute(swa::gemm_kernel<A_MN, B_MN, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(swa::gemm_kernel<A, B, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               swa::GemmCfg<BN>::kSmemBytes);
 }
 
+using swa::kOpK;
+using swa::kOpMN;
+using swa::kOpSym;
+
 cudaError_t set_attrs() {
-  const cudaError_t e[6] = {set_attr_one<false, false, 128>(), set_attr_one<false, false, 256>(),
-                            set_attr_one<false, true, 128>(),  set_attr_one<false, true, 256>(),
-                            set_attr_one<true, true, 128>(),   set_attr_one<true, true, 256>()};
+  const cudaError_t e[8] = {set_attr_one<kOpK, kOpK, 128>(),    set_attr_one<kOpK, kOpK, 256>(),
+                            set_attr_one<kOpMN, kOpMN, 128>(),  set_attr_one<kOpMN, kOpMN, 256>(),
+                            set_attr_one<kOpSym, kOpSym, 128>(), set_attr_one<kOpSym, kOpMN, 128>(),
+                            set_attr_one<kOpSym, kOpMN, 256>(), set_attr_one<kOpK, kOpSym, 128>()};
   for (cudaError_t x : e)
     if (x != cudaSuccess) return x;
   return cudaSuccess;
 }
 
-template <bool A_MN, bool B_MN>
+template <int A, int B>
 void launch_gemm(int bn, int grid, cudaStream_t st, const swa::GemmParams& gp, const swa::GemmMaps& maps) {
-  if (bn == 256)
-    swa::gemm_kernel<A_MN, B_MN, 256><<<grid, 192, swa::GemmCfg<256>::kSmemBytes, st>>>(gp, maps);
-  else
-    swa::gemm_kernel<A_MN, B_MN, 128><<<grid, 192, swa::GemmCfg<128>::kSmemBytes, st>>>(gp, maps);
+  if constexpr (B == kOpSym) {
+    swa::gemm_kernel<A, B, 128><<<grid, 192, swa::GemmCfg<128>::kSmemBytes, st>>>(gp, maps);
+  } else {
+    if (bn == 256)
+      swa::gemm_kernel<A, B, 256><<<grid, 192, swa::GemmCfg<256>::kSmemBytes, st>>>(gp, maps);
+    else
+      swa::gemm_kernel<A, B, 128><<<grid, 192, swa::GemmCfg<128>::kSmemBytes, st>>>(gp, maps);
+  }
+}
+
+// Output tiles of one M x N matrix with BN-wide tiles (a symmetric output: those reaching the
+// diagonal block or above it, as the kernel counts them).
+long long tiles_per_mat(int M, int N, int bn, bool sym) {
+  const long long tm = (M + 127) / 128, tn = (N + bn - 1) / bn;
+  if (!sym) return tm * tn;
+  long long c = 0;
+  for (long long mt = 0; mt < tm; ++mt) c += tn - (128 * mt) / bn;
+  return c;
 }
 
 // Output tile width: the one whose tiles finish in fewer rounds of the grid, counted in 128-column
-// units of MMA work; 256 on a tie (it reads fewer operand bytes per product).
-int choose_bn(int batch, int M, int N, int sms, int* grid) {
-  const long long tm = (M + 127) / 128;
-  const long long t128 = tm * ((N + 127) / 128) * batch, t256 = tm * ((N + 255) / 256) * batch;
+// units of MMA work; 256 on a tie (it reads fewer operand bytes per product). A symmetric Q operand
+// takes 128 (its major-ness is decided per 128 columns).
+int choose_bn(int batch, int M, int N, bool sym, bool q_sym, int sms, int* grid) {
+  const long long t128 = tiles_per_mat(M, N, 128, sym) * batch, t256 = tiles_per_mat(M, N, 256, sym) * batch;
   const long long c128 = (t128 + sms - 1) / sms, c256 = 2 * ((t256 + sms - 1) / sms);
-  const bool wide = c256 <= c128;
+  const bool wide = !q_sym && c256 <= c128;
   const long long tiles = wide ? t256 : t128;
   *grid = static_cast<int>(tiles < sms ? tiles : sms);
   return wide ? 256 : 128;
 }
 
-// D = alpha * P Q + beta * R over a batch; P is M x K, Q is K x N. p_mn: P stored as [K, M] (read
-// MN-major), else [M, K]; q_mn: Q stored as [K, N], else as [N, K] (Q^T, read K-major).
-int gemm(const swa_host::LibCtx& ctx, cudaStream_t st, int batch, int M, int N, int K, const void* P, bool p_mn,
-         const void* Q, bool q_mn, float alpha, float beta, const void* R, void* D) {
+// FLOPs the tensor cores execute for one GEMM launch: 2 K per in-range output element of the tiles
+// it computes (for a symmetric output, the tiles reaching the diagonal block or above it).
+double executed_flops(int batch, int M, int N, int K, bool sym, bool q_sym, int sms) {
+  int grid = 0;
+  const int bn = choose_bn(batch, M, N, sym, q_sym, sms, &grid);
+  const int tm = (M + 127) / 128, tn = (N + bn - 1) / bn;
+  double elems = 0.0;
+  for (int mt = 0; mt < tm; ++mt)
+    for (int nt = sym ? (128 * mt) / bn : 0; nt < tn; ++nt) {
+      const int rows = M - 128 * mt < 128 ? M - 128 * mt : 128;
+      const int cols = N - bn * nt < bn ? N - bn * nt : bn;
+      elems += static_cast<double>(rows) * cols;
+    }
+  return 2.0 * K * elems * batch;
+}
+
+// D = alpha * P Q + beta * R over a batch; P is M x K, Q is K x N. Operand modes (swa::GemmOperand):
+// P stored as [M, K] (kOpK), as [K, M] (kOpMN), or symmetric upper-block storage (kOpSym, M = K);
+// Q stored as [N, K] (kOpK), as [K, N] (kOpMN), or symmetric (kOpSym, K = N). sym_out: D is symmetric
+// and only its tiles on and above the diagonal are written.
+int gemm(const swa_host::LibCtx& ctx, cudaStream_t st, int batch, int M, int N, int K, const void* P, int p_mode,
+         const void* Q, int q_mode, float alpha, float beta, const void* R, void* D, bool sym_out) {
   swa::GemmMaps maps;
-  if (encode3d(ctx.encode, &maps.p, P, batch, p_mn ? K : M, p_mn ? M : K, p_mn) != CUDA_SUCCESS ||
-      encode3d(ctx.encode, &maps.q, Q, batch, q_mn ? K : N, q_mn ? N : K, q_mn) != CUDA_SUCCESS ||
-      encode3d(ctx.encode, &maps.d, D, batch, M, N, false) != CUDA_SUCCESS)
-    return ATTN_ERR_CUDA;
+  std::memset(&maps, 0, sizeof(maps));
+  // K-major view of P: [M rows, K inner]; MN-major view: [K rows, M inner] (equal shapes when symmetric)
+  if (p_mode != kOpMN && encode3d(ctx.encode, &maps.pk, P, batch, M, K, false) != CUDA_SUCCESS) return ATTN_ERR_CUDA;
+  if (p_mode != kOpK && encode3d(ctx.encode, &maps.pm, P, batch, K, M, true) != CUDA_SUCCESS) return ATTN_ERR_CUDA;
+  if (q_mode != kOpMN && encode3d(ctx.encode, &maps.qk, Q, batch, N, K, false) != CUDA_SUCCESS) return ATTN_ERR_CUDA;
+  if (q_mode != kOpK && encode3d(ctx.encode, &maps.qm, Q, batch, K, N, true) != CUDA_SUCCESS) return ATTN_ERR_CUDA;
+  if (encode3d(ctx.encode, &maps.d, D, batch, M, N, false) != CUDA_SUCCESS) return ATTN_ERR_CUDA;
   swa::GemmParams gp{};
   gp.batch = batch;
   gp.M = M;
@@ -146,11 +187,14 @@ int gemm(const swa_host::LibCtx& ctx, cudaStream_t st, int batch, int M, int N, 
   gp.beta = beta;
   gp.R = static_cast<const __nv_bfloat16*>(R);
   gp.err = ctx.d_err;
+  gp.sym_out = sym_out ? 1 : 0;
   int grid = 0;
-  const int bn = choose_bn(batch, M, N, ctx.sm_count, &grid);
-  if (!p_mn && !q_mn) launch_gemm<false, false>(bn, grid, st, gp, maps);
-  else if (!p_mn && q_mn) launch_gemm<false, true>(bn, grid, st, gp, maps);
-  else if (p_mn && q_mn) launch_gemm<true, true>(bn, grid, st, gp, maps);
+  const int bn = choose_bn(batch, M, N, sym_out, q_mode == kOpSym, ctx.sm_count, &grid);
+  if (p_mode == kOpK && q_mode == kOpK) launch_gemm<kOpK, kOpK>(bn, grid, st, gp, maps);
+  else if (p_mode == kOpMN && q_mode == kOpMN) launch_gemm<kOpMN, kOpMN>(bn, grid, st, gp, maps);
+  else if (p_mode == kOpSym && q_mode == kOpSym) launch_gemm<kOpSym, kOpSym>(bn, grid, st, gp, maps);
+  else if (p_mode == kOpSym && q_mode == kOpMN) launch_gemm<kOpSym, kOpMN>(bn, grid, st, gp, maps);
+  else if (p_mode == kOpK && q_mode == kOpSym) launch_gemm<kOpK, kOpSym>(bn, grid, st, gp, maps);
   else return ATTN_ERR_UNSUPPORTED;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -174,21 +218,38 @@ int step_locked(const swa_host::LibCtx& ctx, cudaStream_t st, const void* X, voi
   void* B = ws + l.b;
   const float a = kCoeffs[step][0], b = kCoeffs[step][1], c = kCoeffs[step][2];
   int rc;
+  // A and B are symmetric: only their 128 x 128 blocks on and above the diagonal are computed and
+  // stored, and the products that read them take each block below the diagonal as its mirror's
+  // transpose.
   if (m <= n) {
     // wide: A = X X^T (m x m, K = n); B = c A A + b A; Y = a X + B X
-    if ((rc = gemm(ctx, st, batch, m, m, n, X, false, X, false, 1.f, 0.f, nullptr, A)) != ATTN_OK) return rc;
-    if ((rc = gemm(ctx, st, batch, m, m, m, A, false, A, true, c, b, A, B)) != ATTN_OK) return rc;
-    return gemm(ctx, st, batch, m, n, m, B, false, X, true, 1.f, a, X, Y);
+    if ((rc = gemm(ctx, st, batch, m, m, n, X, kOpK, X, kOpK, 1.f, 0.f, nullptr, A, true)) != ATTN_OK) return rc;
+    if ((rc = gemm(ctx, st, batch, m, m, m, A, kOpSym, A, kOpSym, c, b, A, B, true)) != ATTN_OK) return rc;
+    return gemm(ctx, st, batch, m, n, m, B, kOpSym, X, kOpMN, 1.f, a, X, Y, false);
   }
   // tall: A = X^T X (n x n, K = m); B = c A A + b A; Y = a X + X B
-  if ((rc = gemm(ctx, st, batch, n, n, m, X, true, X, true, 1.f, 0.f, nullptr, A)) != ATTN_OK) return rc;
-  if ((rc = gemm(ctx, st, batch, n, n, n, A, false, A, true, c, b, A, B)) != ATTN_OK) return rc;
-  return gemm(ctx, st, batch, m, n, n, X, false, B, true, 1.f, a, X, Y);
+  if ((rc = gemm(ctx, st, batch, n, n, m, X, kOpMN, X, kOpMN, 1.f, 0.f, nullptr, A, true)) != ATTN_OK) return rc;
+  if ((rc = gemm(ctx, st, batch, n, n, n, A, kOpSym, A, kOpSym, c, b, A, B, true)) != ATTN_OK) return rc;
+  return gemm(ctx, st, batch, m, n, n, X, kOpK, B, kOpSym, 1.f, a, X, Y, false);
 }
 
 }  // namespace
 
 extern "C" {
+
+double pe_step_flops(int batch, int m, int n) {
+  if (check_shape(batch, m, n) != ATTN_OK) return 0.0;
+  int sms = 0;
+  const int dev_rc = swa_host::locked([&](const swa_host::LibCtx& ctx) -> int {
+    sms = ctx.sm_count;
+    return ATTN_OK;
+  });
+  if (dev_rc != ATTN_OK || sms <= 0) return 0.0;
+  const int s = m < n ? m : n, l = m < n ? n : m;
+  // A = X X^T (or X^T X), B = c A A + b A (both symmetric), Y = a X + B X (or X B)
+  return executed_flops(batch, s, s, l, true, false, sms) + executed_flops(batch, s, s, s, true, true, sms) +
+         executed_flops(batch, m, n, s, false, m > n, sms);
+}
 
 size_t pe_workspace_bytes(int batch, int m, int n) {
   if (batch < 1 || m < 1 || n < 1) return 0;

@@ -12,6 +12,12 @@
 // elements) or MN-major (rows of M / N contiguous elements), so X X^T, X^T X, A A and B X all take
 // their operands straight from the row-major matrices without a transpose.
 //
+// An operand is read K-major, MN-major, or - for the symmetric products A and B of a step, of which
+// only the 128 x 128 blocks on and above the diagonal are stored - block by block: a K slice whose
+// block lies below the diagonal is loaded from the mirrored stored block in the other major-ness
+// (its transpose), and the MMA's descriptors and major bits follow, slice by slice. A symmetric
+// output computes only the tiles that reach the diagonal or above it.
+//
 // Persistent and warp-specialised: each CTA (one per SM) walks the 128 x BN output tiles of the
 // whole batch with a stride of the grid. Warp 0 streams 64-deep K slices of P and Q through a
 // shared-memory ring by TMA; one thread of warp 1 issues the tcgen05 MMAs (M = 128, N = BN, K = 16)
@@ -27,15 +33,23 @@
 
 namespace swa {
 
+// How a GEMM operand is stored: K-major (P as [M, K], Q as [N, K]), MN-major (P as [K, M], Q as
+// [K, N]), or a symmetric square matrix of which only the 128 x 128 blocks on and above the
+// diagonal hold data (either form, block by block).
+enum GemmOperand : int { kOpK = 0, kOpMN = 1, kOpSym = 2 };
+
 struct GemmParams {
   int batch, M, N, K;
   float alpha, beta;
   const __nv_bfloat16* R;  // [batch, M, N] or nullptr (no beta term)
   int* err;
+  int sym_out;             // 1: D is symmetric (M = N); only tiles reaching the diagonal or above are computed
 };
 
 struct GemmMaps {
-  CUtensorMap p, q, d;  // 3-D (inner, rows, batch) views; see the host side for the box of each form
+  // 3-D (inner, rows, batch) views of the operands: *k with 128-row x 64 boxes (K-major tiles), *m
+  // with 64 x 64 boxes (MN-major tiles); a symmetric operand uses both. d: the output, 128 x 64 boxes.
+  CUtensorMap pk, pm, qk, qm, d;
 };
 
 template <int BN>
@@ -73,10 +87,49 @@ __device__ __forceinline__ void bulk_wait_group_read1() {
 // Shared-memory descriptor of K step ks (16 deep) of an operand tile of `rows` M / N rows x 64 K:
 // K-major (rows of 128 bytes, 128-byte swizzle, 8-row groups 1 KB apart) or MN-major (64-wide M / N
 // chunks of 64 K rows, 8 KB apart).
-template <bool MN>
-__device__ __forceinline__ uint64_t gemm_desc(uint32_t tile, int ks) {
-  if constexpr (MN) return make_sdesc(tile + ks * 16 * 128, 8192, 1024, 2);
-  else return make_sdesc(tile + ks * 32, 16, 1024, 2);
+__device__ __forceinline__ uint64_t gemm_desc(bool mn, uint32_t tile, int ks) {
+  return mn ? make_sdesc(tile + ks * 16 * 128, 8192, 1024, 2) : make_sdesc(tile + ks * 32, 16, 1024, 2);
+}
+
+// Output tiles of one matrix: every (mt, nt), or for a symmetric output those with
+// nt >= first_nt(mt) = (128 mt) / BN (the tile reaches the diagonal block or lies above it).
+template <int BN>
+__device__ __forceinline__ int gemm_tiles_per_mat(int tiles_m, int tiles_n, bool sym) {
+  if (!sym) return tiles_m * tiles_n;
+  int c = 0;
+  for (int mt = 0; mt < tiles_m; ++mt) c += tiles_n - (128 * mt) / BN;
+  return c;
+}
+
+template <int BN>
+__device__ __forceinline__ void gemm_decode(int t, int per_mat, int tiles_n, bool sym, int& z, int& m0, int& n0) {
+  z = t / per_mat;
+  int r = t - z * per_mat;
+  if (!sym) {
+    const int mt = r / tiles_n;
+    m0 = mt * 128;
+    n0 = (r - mt * tiles_n) * BN;
+    return;
+  }
+  int mt = 0;
+  for (;; ++mt) {
+    const int cnt = tiles_n - (128 * mt) / BN;
+    if (r < cnt) break;
+    r -= cnt;
+  }
+  m0 = mt * 128;
+  n0 = ((128 * mt) / BN + r) * BN;
+}
+
+// Major-ness of the K slice starting at k0 of P (rows m0..) and of Q (columns n0..): a symmetric
+// operand's block below the diagonal is read as the transpose of its mirror.
+template <int MODE>
+__device__ __forceinline__ bool p_slice_mn(int m0, int k0) {
+  return MODE == kOpMN || (MODE == kOpSym && (k0 >> 7) < (m0 >> 7));
+}
+template <int MODE>
+__device__ __forceinline__ bool q_slice_mn(int n0, int k0) {
+  return MODE == kOpMN || (MODE == kOpSym && (n0 >> 7) >= (k0 >> 7));
 }
 
 // Eight 16-byte pieces of row `row` of R from column c0 (zero past the row's end or the matrix).
@@ -87,8 +140,9 @@ __device__ __forceinline__ void gemm_load_r(uint4 (&v)[8], const __nv_bfloat16* 
                                                : make_uint4(0, 0, 0, 0);
 }
 
-template <bool A_MN, bool B_MN, int BN>
+template <int A_MODE, int B_MODE, int BN>
 __global__ void __launch_bounds__(192, 1) gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
+  static_assert(B_MODE != kOpSym || BN == 128, "a symmetric Q operand decides its major-ness per 128 columns");
   using Cfg = GemmCfg<BN>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -100,15 +154,10 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(const GemmParams p, const 
   volatile int* epi_ok = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tiles_n = (p.N + BN - 1) / BN, tiles_m = (p.M + Cfg::BM - 1) / Cfg::BM;
-  const int per_mat = tiles_m * tiles_n, total = per_mat * p.batch;
+  const bool sym = p.sym_out != 0;
+  const int per_mat = gemm_tiles_per_mat<BN>(tiles_m, tiles_n, sym), total = per_mat * p.batch;
   const int nk = (p.K + Cfg::BK - 1) / Cfg::BK;
-  auto decode = [&](int t, int& z, int& m0, int& n0) {
-    z = t / per_mat;
-    const int r = t - z * per_mat;
-    const int mt = r / tiles_n;
-    m0 = mt * Cfg::BM;
-    n0 = (r - mt * tiles_n) * BN;
-  };
+  auto decode = [&](int t, int& z, int& m0, int& n0) { gemm_decode<BN>(t, per_mat, tiles_n, sym, z, m0, n0); };
 
   if (tid == 0) {
     for (int i = 0; i < 2 * S + 2; ++i) mbar_init(bars + i, 1);
@@ -130,8 +179,10 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(const GemmParams p, const 
   if (warp == 0) {
     if (lane == 0) {
       // ---- producer: K slices of P and Q for every tile of this CTA ----
-      prefetch_tmap(&maps.p);
-      prefetch_tmap(&maps.q);
+      if (A_MODE != kOpMN) prefetch_tmap(&maps.pk);
+      if (A_MODE != kOpK) prefetch_tmap(&maps.pm);
+      if (B_MODE != kOpMN) prefetch_tmap(&maps.qk);
+      if (B_MODE != kOpK) prefetch_tmap(&maps.qm);
       prefetch_tmap(&maps.d);
       uint32_t g = 0;
       bool ok = true;
@@ -148,16 +199,17 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(const GemmParams p, const 
           uint8_t* sp = smem + s * Cfg::kStageBytes;
           uint8_t* sq = sp + Cfg::kTileP;
           mbar_arrive_expect_tx(full, Cfg::kStageBytes);
-          if constexpr (A_MN) {
-            tma_load_3d(sp, &maps.p, full, m0, k0, z);
-            tma_load_3d(sp + 8192, &maps.p, full, m0 + 64, k0, z);
+          if (p_slice_mn<A_MODE>(m0, k0)) {
+            tma_load_3d(sp, &maps.pm, full, m0, k0, z);
+            tma_load_3d(sp + 8192, &maps.pm, full, m0 + 64, k0, z);
           } else {
-            tma_load_3d(sp, &maps.p, full, k0, m0, z);
+            tma_load_3d(sp, &maps.pk, full, k0, m0, z);
           }
+          const bool qmn = q_slice_mn<B_MODE>(n0, k0);
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j) {
-            if constexpr (B_MN) tma_load_3d(sq + 8192 * j, &maps.q, full, n0 + 64 * j, k0, z);
-            else if (j % 2 == 0) tma_load_3d(sq + 8192 * j, &maps.q, full, k0, n0 + 64 * j, z);
+            if (qmn) tma_load_3d(sq + 8192 * j, &maps.qm, full, n0 + 64 * j, k0, z);
+            else if (j % 2 == 0) tma_load_3d(sq + 8192 * j, &maps.qk, full, k0, n0 + 64 * j, z);
           }
         }
       }
@@ -173,11 +225,12 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(const GemmParams p, const 
   } else if (warp == 1) {
     if (lane == 0) {
       // ---- MMA issuer ----
-      constexpr uint32_t idesc = make_idesc_bf16(128, BN, B_MN) | (A_MN ? (1u << 15) : 0u);
       uint32_t g = 0;
       bool ok = true;
       int i = 0;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++i) {
+        int z, m0, n0;
+        decode(t, z, m0, n0);
         const int buf = i & 1;
         if (i >= 2 && !mbar_wait_or_abort(bars + Cfg::kBarAccEmpty + buf, ((i >> 1) - 1) & 1, abort_flag)) {
           ok = false;
@@ -193,9 +246,11 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(const GemmParams p, const 
           }
           tc_fence_after();
           const uint32_t sp = smem_u32(smem + s * Cfg::kStageBytes), sq = sp + Cfg::kTileP;
+          const bool amn = p_slice_mn<A_MODE>(m0, kt * Cfg::BK), bmn = q_slice_mn<B_MODE>(n0, kt * Cfg::BK);
+          const uint32_t idesc = make_idesc_bf16(128, BN, bmn) | (amn ? (1u << 15) : 0u);
 #pragma unroll
           for (int ks = 0; ks < Cfg::BK / 16; ++ks)
-            umma_ss(acc, gemm_desc<A_MN>(sp, ks), gemm_desc<B_MN>(sq, ks), idesc, (kt > 0 || ks > 0) ? 1u : 0u);
+            umma_ss(acc, gemm_desc(amn, sp, ks), gemm_desc(bmn, sq, ks), idesc, (kt > 0 || ks > 0) ? 1u : 0u);
           umma_commit(bars + Cfg::kBarEmpty + s);
         }
         if (ok) umma_commit(bars + Cfg::kBarAccFull + buf);

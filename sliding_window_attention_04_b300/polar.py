@@ -13,11 +13,13 @@ import torch
 
 from .attn import ATTN_OK, AttnError, lib
 
-EXPORTED = ("pe_workspace_bytes", "pe_normalize", "pe_step", "polar_express")
+EXPORTED = ("pe_workspace_bytes", "pe_step_flops", "pe_normalize", "pe_step", "polar_express")
 
 _c = ctypes
 lib.pe_workspace_bytes.argtypes = [_c.c_int, _c.c_int, _c.c_int]
 lib.pe_workspace_bytes.restype = _c.c_size_t
+lib.pe_step_flops.argtypes = [_c.c_int, _c.c_int, _c.c_int]
+lib.pe_step_flops.restype = _c.c_double
 lib.pe_normalize.argtypes = [_c.c_void_p, _c.c_void_p] + [_c.c_int] * 3 + [_c.c_void_p, _c.c_size_t, _c.c_void_p]
 lib.pe_normalize.restype = _c.c_int
 lib.pe_step.argtypes = [_c.c_void_p, _c.c_void_p] + [_c.c_int] * 4 + [_c.c_void_p, _c.c_size_t, _c.c_void_p]
@@ -43,6 +45,11 @@ def _dims(g: torch.Tensor):
 
 def workspace_bytes(batch: int, m: int, n: int) -> int:
     return int(lib.pe_workspace_bytes(batch, m, n))
+
+
+def step_flops(batch: int, m: int, n: int) -> float:
+    """FLOPs one step executes on the tensor cores on the current device (attn_init first)."""
+    return float(lib.pe_step_flops(batch, m, n))
 
 
 def _workspace(ws, nbytes, device):

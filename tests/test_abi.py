@@ -206,7 +206,7 @@ def test_polar_header_and_exports(binding):
     declared = set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*((?:pe_|polar_)\w+)\s*\(", text, flags=re.M))
     out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True, text=True).stdout
     exported = set(re.findall(r" T ((?:pe_|polar_)\w+)", out))
-    assert declared == exported == {"pe_workspace_bytes", "pe_normalize", "pe_step", "polar_express"}
+    assert declared == exported == {"pe_workspace_bytes", "pe_step_flops", "pe_normalize", "pe_step", "polar_express"}
     from sliding_window_attention_04_b300 import polar
 
     assert set(polar.EXPORTED) == exported
@@ -220,6 +220,7 @@ def test_polar_host_validation_codes(binding):
     nb = polar.workspace_bytes(2, 64, 96)
     assert nb >= 2 * 64 * 64 * 2 * 2 + 2 * 64 * 96 * 2 and nb % 256 == 0
     assert polar.workspace_bytes(0, 64, 96) == 0
+    assert polar.step_flops(2, 64, 96) == 0.0  # not initialised
     assert lib.pe_step(x, y, 2, 64, 96, 0, ws, nb, None) == E.ATTN_ERR_NOT_INITIALIZED
     assert lib.pe_step(x, y, 2, 64, 100, 0, ws, nb, None) == E.ATTN_ERR_INVALID_ARG   # n not a multiple of 8
     assert lib.pe_step(x, y, 2, 64, 96, 5, ws, nb, None) == E.ATTN_ERR_INVALID_ARG    # no sixth triple
