@@ -105,10 +105,11 @@ using swa::kOpMN;
 using swa::kOpSym;
 
 cudaError_t set_attrs() {
-  const cudaError_t e[8] = {set_attr_one<kOpK, kOpK, 128>(),    set_attr_one<kOpK, kOpK, 256>(),
-                            set_attr_one<kOpMN, kOpMN, 128>(),  set_attr_one<kOpMN, kOpMN, 256>(),
-                            set_attr_one<kOpSym, kOpSym, 128>(), set_attr_one<kOpSym, kOpMN, 128>(),
-                            set_attr_one<kOpSym, kOpMN, 256>(), set_attr_one<kOpK, kOpSym, 128>()};
+  const cudaError_t e[10] = {set_attr_one<kOpK, kOpK, 128>(),     set_attr_one<kOpK, kOpK, 256>(),
+                             set_attr_one<kOpMN, kOpMN, 128>(),   set_attr_one<kOpMN, kOpMN, 256>(),
+                             set_attr_one<kOpSym, kOpSym, 128>(), set_attr_one<kOpSym, kOpSym, 256>(),
+                             set_attr_one<kOpSym, kOpMN, 128>(),  set_attr_one<kOpSym, kOpMN, 256>(),
+                             set_attr_one<kOpK, kOpSym, 128>(),   set_attr_one<kOpK, kOpSym, 256>()};
   for (cudaError_t x : e)
     if (x != cudaSuccess) return x;
   return cudaSuccess;
@@ -116,14 +117,10 @@ cudaError_t set_attrs() {
 
 template <int A, int B>
 void launch_gemm(int bn, int grid, cudaStream_t st, const swa::GemmParams& gp, const swa::GemmMaps& maps) {
-  if constexpr (B == kOpSym) {
+  if (bn == 256)
+    swa::gemm_kernel<A, B, 256><<<grid, 192, swa::GemmCfg<256>::kSmemBytes, st>>>(gp, maps);
+  else
     swa::gemm_kernel<A, B, 128><<<grid, 192, swa::GemmCfg<128>::kSmemBytes, st>>>(gp, maps);
-  } else {
-    if (bn == 256)
-      swa::gemm_kernel<A, B, 256><<<grid, 192, swa::GemmCfg<256>::kSmemBytes, st>>>(gp, maps);
-    else
-      swa::gemm_kernel<A, B, 128><<<grid, 192, swa::GemmCfg<128>::kSmemBytes, st>>>(gp, maps);
-  }
 }
 
 // Output tiles of one M x N matrix with BN-wide tiles (a symmetric output: those reaching the
@@ -137,12 +134,12 @@ long long tiles_per_mat(int M, int N, int bn, bool sym) {
 }
 
 // Output tile width: the one whose tiles finish in fewer rounds of the grid, counted in 128-column
-// units of MMA work; 256 on a tie (it reads fewer operand bytes per product). A symmetric Q operand
-// takes 128 (its major-ness is decided per 128 columns).
+// units of MMA work; 256 on a tie (it reads fewer operand bytes per product).
 int choose_bn(int batch, int M, int N, bool sym, bool q_sym, int sms, int* grid) {
+  (void)q_sym;
   const long long t128 = tiles_per_mat(M, N, 128, sym) * batch, t256 = tiles_per_mat(M, N, 256, sym) * batch;
   const long long c128 = (t128 + sms - 1) / sms, c256 = 2 * ((t256 + sms - 1) / sms);
-  const bool wide = !q_sym && c256 <= c128;
+  const bool wide = c256 <= c128;
   const long long tiles = wide ? t256 : t128;
   *grid = static_cast<int>(tiles < sms ? tiles : sms);
   return wide ? 256 : 128;

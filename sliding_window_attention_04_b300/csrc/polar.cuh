@@ -142,7 +142,6 @@ __device__ __forceinline__ void gemm_load_r(uint4 (&v)[8], const __nv_bfloat16* 
 
 template <int A_MODE, int B_MODE, int BN>
 __global__ void __launch_bounds__(192, 1) gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
-  static_assert(B_MODE != kOpSym || BN == 128, "a symmetric Q operand decides its major-ness per 128 columns");
   using Cfg = GemmCfg<BN>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -205,11 +204,18 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(const GemmParams p, const 
           } else {
             tma_load_3d(sp, &maps.pk, full, k0, m0, z);
           }
-          const bool qmn = q_slice_mn<B_MODE>(n0, k0);
+          // Q by 128-column halves (a symmetric Q may take the two halves in different forms); either
+          // form puts columns 128 h.. at byte 16384 h of the tile
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j) {
-            if (qmn) tma_load_3d(sq + 8192 * j, &maps.qm, full, n0 + 64 * j, k0, z);
-            else if (j % 2 == 0) tma_load_3d(sq + 8192 * j, &maps.qk, full, k0, n0 + 64 * j, z);
+          for (int hh = 0; hh < BN / 128; ++hh) {
+            uint8_t* sh = sq + 16384 * hh;
+            const int nh = n0 + 128 * hh;
+            if (q_slice_mn<B_MODE>(nh, k0)) {
+              tma_load_3d(sh, &maps.qm, full, nh, k0, z);
+              tma_load_3d(sh + 8192, &maps.qm, full, nh + 64, k0, z);
+            } else {
+              tma_load_3d(sh, &maps.qk, full, k0, nh, z);
+            }
           }
         }
       }
@@ -247,10 +253,22 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(const GemmParams p, const 
           tc_fence_after();
           const uint32_t sp = smem_u32(smem + s * Cfg::kStageBytes), sq = sp + Cfg::kTileP;
           const bool amn = p_slice_mn<A_MODE>(m0, kt * Cfg::BK), bmn = q_slice_mn<B_MODE>(n0, kt * Cfg::BK);
-          const uint32_t idesc = make_idesc_bf16(128, BN, bmn) | (amn ? (1u << 15) : 0u);
+          const bool bmn1 = BN == 256 ? q_slice_mn<B_MODE>(n0 + 128, kt * Cfg::BK) : bmn;
+          if (bmn1 == bmn) {  // one form across the tile: N = BN products
+            const uint32_t idesc = make_idesc_bf16(128, BN, bmn) | (amn ? (1u << 15) : 0u);
 #pragma unroll
-          for (int ks = 0; ks < Cfg::BK / 16; ++ks)
-            umma_ss(acc, gemm_desc(amn, sp, ks), gemm_desc(bmn, sq, ks), idesc, (kt > 0 || ks > 0) ? 1u : 0u);
+            for (int ks = 0; ks < Cfg::BK / 16; ++ks)
+              umma_ss(acc, gemm_desc(amn, sp, ks), gemm_desc(bmn, sq, ks), idesc, (kt > 0 || ks > 0) ? 1u : 0u);
+          } else {  // the halves differ (a symmetric Q across the diagonal): two N = 128 products each
+            const uint32_t id0 = make_idesc_bf16(128, 128, bmn) | (amn ? (1u << 15) : 0u);
+            const uint32_t id1 = make_idesc_bf16(128, 128, bmn1) | (amn ? (1u << 15) : 0u);
+#pragma unroll
+            for (int ks = 0; ks < Cfg::BK / 16; ++ks) {
+              const uint64_t ad = gemm_desc(amn, sp, ks);
+              umma_ss(acc, ad, gemm_desc(bmn, sq, ks), id0, (kt > 0 || ks > 0) ? 1u : 0u);
+              umma_ss(acc + 128, ad, gemm_desc(bmn1, sq + 16384, ks), id1, (kt > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
           umma_commit(bars + Cfg::kBarEmpty + s);
         }
         if (ok) umma_commit(bars + Cfg::kBarAccFull + buf);
