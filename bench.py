@@ -593,19 +593,41 @@ def main():
     peak, peak_sustained, peak_kind = peaks()
 
     # ---- end to end through the public API: pinned host -> device, compute, device -> host ----
+    # Three streams and two device buffer sets, as a caller of the stream-taking API pipelines layers:
+    # layer l + 1's inputs copy in while layer l computes and layer l - 1's results copy out (PCIe
+    # carries both directions at once). Events order each buffer's reuse.
     h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
     h_lse = [torch.empty(l.shape, dtype=l.dtype, pin_memory=True) for l in lses]
-    d_in = [torch.empty_like(dev[0][i]) for i in range(3)]
-    d_out, d_lse = torch.empty_like(outs[0]), torch.empty_like(lses[0])
+    d_in = [[torch.empty_like(dev[0][i]) for i in range(3)] for _ in range(2)]
+    d_out = [torch.empty_like(outs[0]) for _ in range(2)]
+    d_lse = [torch.empty_like(lses[0]) for _ in range(2)]
+    s_in, s_back = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in_ready", "in_free", "out_ready", "out_free")}
+    seq = [0]
 
     def e2e_step():
         for li, layer in enumerate(w.layers):
-            for i in range(3):
-                d_in[i].copy_(host[li][i], non_blocking=True)
-            attn.attn_fwd(d_in[0], d_in[1], d_in[2], window=layer.window, causal=layer.causal,
-                          rope_base=w.rope_base, eps=w.eps, out=d_out, lse=d_lse, stream=stream)
-            h_out[li].copy_(d_out, non_blocking=True)
-            h_lse[li].copy_(d_lse, non_blocking=True)
+            b = seq[0] & 1
+            first_use = seq[0] < 2
+            seq[0] += 1
+            if not first_use:
+                s_in.wait_event(ev["in_free"][b])
+            with torch.cuda.stream(s_in):
+                for i in range(3):
+                    d_in[b][i].copy_(host[li][i], non_blocking=True)
+            ev["in_ready"][b].record(s_in)
+            stream.wait_event(ev["in_ready"][b])
+            if not first_use:
+                stream.wait_event(ev["out_free"][b])
+            attn.attn_fwd(d_in[b][0], d_in[b][1], d_in[b][2], window=layer.window, causal=layer.causal,
+                          rope_base=w.rope_base, eps=w.eps, out=d_out[b], lse=d_lse[b], stream=stream)
+            ev["in_free"][b].record(stream)
+            ev["out_ready"][b].record(stream)
+            s_back.wait_event(ev["out_ready"][b])
+            with torch.cuda.stream(s_back):
+                h_out[li].copy_(d_out[b], non_blocking=True)
+                h_lse[li].copy_(d_lse[b], non_blocking=True)
+            ev["out_free"][b].record(s_back)
 
     e2e_step()
     torch.cuda.synchronize(device)
@@ -613,8 +635,11 @@ def main():
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    s_in.wait_stream(stream)  # the copies start after e0
     for _ in range(args.e2e_steps):
         e2e_step()
+    stream.wait_stream(s_back)  # e1 after the last result has reached the host
+    stream.wait_stream(s_in)
     e1.record(stream)
     torch.cuda.synchronize(device)
     e2e_ms = e0.elapsed_time(e1)
