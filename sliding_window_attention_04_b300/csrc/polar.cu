@@ -135,8 +135,7 @@ long long tiles_per_mat(int M, int N, int bn, bool sym) {
 
 // Output tile width: the one whose tiles finish in fewer rounds of the grid, counted in 128-column
 // units of MMA work; 256 on a tie (it reads fewer operand bytes per product).
-int choose_bn(int batch, int M, int N, bool sym, bool q_sym, int sms, int* grid) {
-  (void)q_sym;
+int choose_bn(int batch, int M, int N, bool sym, int sms, int* grid) {
   const long long t128 = tiles_per_mat(M, N, 128, sym) * batch, t256 = tiles_per_mat(M, N, 256, sym) * batch;
   const long long c128 = (t128 + sms - 1) / sms, c256 = 2 * ((t256 + sms - 1) / sms);
   const bool wide = c256 <= c128;
@@ -147,9 +146,9 @@ int choose_bn(int batch, int M, int N, bool sym, bool q_sym, int sms, int* grid)
 
 // FLOPs the tensor cores execute for one GEMM launch: 2 K per in-range output element of the tiles
 // it computes (for a symmetric output, the tiles reaching the diagonal block or above it).
-double executed_flops(int batch, int M, int N, int K, bool sym, bool q_sym, int sms) {
+double executed_flops(int batch, int M, int N, int K, bool sym, int sms) {
   int grid = 0;
-  const int bn = choose_bn(batch, M, N, sym, q_sym, sms, &grid);
+  const int bn = choose_bn(batch, M, N, sym, sms, &grid);
   const int tm = (M + 127) / 128, tn = (N + bn - 1) / bn;
   double elems = 0.0;
   for (int mt = 0; mt < tm; ++mt)
@@ -186,7 +185,7 @@ int gemm(const swa_host::LibCtx& ctx, cudaStream_t st, int batch, int M, int N, 
   gp.err = ctx.d_err;
   gp.sym_out = sym_out ? 1 : 0;
   int grid = 0;
-  const int bn = choose_bn(batch, M, N, sym_out, q_mode == kOpSym, ctx.sm_count, &grid);
+  const int bn = choose_bn(batch, M, N, sym_out, ctx.sm_count, &grid);
   if (p_mode == kOpK && q_mode == kOpK) launch_gemm<kOpK, kOpK>(bn, grid, st, gp, maps);
   else if (p_mode == kOpMN && q_mode == kOpMN) launch_gemm<kOpMN, kOpMN>(bn, grid, st, gp, maps);
   else if (p_mode == kOpSym && q_mode == kOpSym) launch_gemm<kOpSym, kOpSym>(bn, grid, st, gp, maps);
@@ -244,8 +243,8 @@ double pe_step_flops(int batch, int m, int n) {
   if (dev_rc != ATTN_OK || sms <= 0) return 0.0;
   const int s = m < n ? m : n, l = m < n ? n : m;
   // A = X X^T (or X^T X), B = c A A + b A (both symmetric), Y = a X + B X (or X B)
-  return executed_flops(batch, s, s, l, true, false, sms) + executed_flops(batch, s, s, s, true, true, sms) +
-         executed_flops(batch, m, n, s, false, m > n, sms);
+  return executed_flops(batch, s, s, l, true, sms) + executed_flops(batch, s, s, s, true, sms) +
+         executed_flops(batch, m, n, s, false, sms);
 }
 
 size_t pe_workspace_bytes(int batch, int m, int n) {
