@@ -36,7 +36,9 @@
 // half h is rewritten by half h + 4, whose softmax starts after S^T of h + 4, i.e. after the
 // products of iteration N(h) + 1 (in issue order) have completed. Every barrier's waiter is at
 // most one phase behind (two-slot p_full because softmax B may finish half (N+1, B) before the
-// issuer has consumed (N, B)); every wait is bounded and gives up with the error word set.
+// issuer has consumed (N, B); two-slot dq_full because the CTA's last dQ^ product follows the one
+// before it with no S^T of a next iteration in between, so both can complete while the dQ warps are
+// still writing out the previous tile); every wait is bounded and gives up with the error word set.
 #pragma once
 #include "attn_bwd.cuh"
 
@@ -68,8 +70,8 @@ struct BwdWsCfg {
   static constexpr int kBarSdp = kBarQEmpty + kStages;   // [3] S^T, dP^T of a half in the buffer
   static constexpr int kBarBufFree = kBarSdp + 3;        // [3]
   static constexpr int kBarPFull = kBarBufFree + 3;      // [2 halves][2 slots]
-  static constexpr int kBarDq = kBarPFull + 4;
-  static constexpr int kBarFinal = kBarDq + 1;           // [2] a tile's accumulators complete
+  static constexpr int kBarDq = kBarPFull + 4;          // [2] dQ^ of iteration N in its buffer (slot N & 1)
+  static constexpr int kBarFinal = kBarDq + 2;           // [2] a tile's accumulators complete
   static constexpr int kBarAccFree = kBarFinal + 2;      // the accumulators have been read
   static constexpr int kNumBars = kBarAccFree + 1;
   static constexpr int kTileConsumers = 1 + 8 + 1;      // issuer, softmax warps, dQ warpgroup
@@ -219,6 +221,7 @@ __global__ void __launch_bounds__(512, 1)
     }
     for (int i = 0; i < 4; ++i) mbar_init(bar(Cfg::kBarPFull + i), 4);
     mbar_init(bar(Cfg::kBarDq), 1);
+    mbar_init(bar(Cfg::kBarDq + 1), 1);
     mbar_init(bar(Cfg::kBarAccFree), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -344,7 +347,7 @@ __global__ void __launch_bounds__(512, 1)
           umma_ss(tmem + Cfg::col_buf(h % 3) + 64, da, kb, idesc_q, ks > 0 ? 1u : 0u);
         }
         umma_commit(bar(Cfg::kBarQEmpty + s));
-        umma_commit(bar(Cfg::kBarDq));
+        umma_commit(bar(Cfg::kBarDq + (m & 1)));
         if (closes) {
           umma_commit(bar(Cfg::kBarKVFree + kvs));
           umma_commit(bar(Cfg::kBarFinal + (tl & 1)));
@@ -463,7 +466,7 @@ __global__ void __launch_bounds__(512, 1)
       for (int n = 0; n < w.n_iter; ++n, ++N) {
         // one thread waits (bounded) and hands the outcome to the others through the warpgroup barrier,
         // so that all four warps leave together on a timeout and no bar.sync is left waiting
-        if (leader) *wg_ok = wait(Cfg::kBarDq, N & 1) ? 1 : 0;
+        if (leader) *wg_ok = wait(Cfg::kBarDq + (N & 1), (N >> 1) & 1) ? 1 : 0;
         named_barrier(1, 128);
         if (*wg_ok == 0) {
           ok = false;
