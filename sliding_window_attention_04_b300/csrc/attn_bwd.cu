@@ -65,11 +65,32 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 std::mutex g_attr_mu;
 int g_attr_device = -1;  // device whose kernel attributes have been set
 
+// Resident CTAs per SM of the prep and finalize passes (by their shared-memory rings and registers),
+// indexed by D / 64 (D = 32, 64, 128 -> 0, 1, 2); set with the attributes.
+int g_prep_ctas_per_sm[3] = {1, 1, 1};
+int g_fin_ctas_per_sm[3] = {1, 1, 1};
+
 template <int D>
 cudaError_t set_bwd_attrs() {
   cudaError_t e = cudaFuncSetAttribute(swa::attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        swa::BwdCfg<D>::kSmemBytes);
-  if (e != cudaSuccess || D == 128) return e;
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(swa::attn_bwd_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           swa::PrepCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(swa::attn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           swa::FinCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, swa::attn_bwd_prep_kernel<D>, 256, swa::PrepCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  if (n < 1) return cudaErrorInvalidConfiguration;
+  g_prep_ctas_per_sm[D / 64] = n;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, swa::attn_bwd_dq_kernel<D>, 256, swa::FinCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  if (n < 1) return cudaErrorInvalidConfiguration;
+  g_fin_ctas_per_sm[D / 64] = n;
+  if (D == 128) return e;
   return cudaFuncSetAttribute(swa::attn_bwd_ws_kernel<D == 128 ? 64 : D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               swa::BwdWsCfg<D == 128 ? 64 : D>::kSmemBytes);
 }
@@ -85,10 +106,16 @@ int launch_bwd(const swa::BwdParams& p, const swa_host::LibCtx& ctx, cudaStream_
       encode_f32_map(ctx.encode, &maps.dk, p.dk, p.B, p.Hkv, p.T, D) != CUDA_SUCCESS ||
       encode_f32_map(ctx.encode, &maps.dv, p.dv, p.B, p.Hkv, p.T, D) != CUDA_SUCCESS)
     return ATTN_ERR_CUDA;
-  const long long rows = static_cast<long long>(p.B) * p.T * (p.H + p.Hkv);
-  const long long prep_blocks = (rows * 2 + 255) / 256;  // two lanes per row, 16 rows per warp
-  const int prep_grid = static_cast<int>(prep_blocks < 8L * ctx.sm_count ? prep_blocks : 8L * ctx.sm_count);
-  swa::attn_bwd_prep_kernel<D><<<prep_grid, 256, 0, st>>>(p);
+  // prep and finalize: one group of rows per warp step, eight warps per CTA, as many CTAs as stay
+  // resident (each warp then strides over the groups)
+  const long long nq = static_cast<long long>(p.B) * p.T * p.H, nk = static_cast<long long>(p.B) * p.T * p.Hkv;
+  using PC = swa::PrepCfg<D>;
+  using FC = swa::FinCfg<D>;
+  const long long prep_groups = (nq + PC::kQRows - 1) / PC::kQRows + (nk + PC::kKRows - 1) / PC::kKRows;
+  const long long prep_cap = static_cast<long long>(g_prep_ctas_per_sm[D / 64]) * ctx.sm_count;
+  const long long prep_need = (prep_groups + PC::kWarps - 1) / PC::kWarps;
+  const int prep_grid = static_cast<int>(prep_need < prep_cap ? prep_need : prep_cap);
+  swa::attn_bwd_prep_kernel<D><<<prep_grid, PC::kWarps * 32, PC::kSmemBytes, st>>>(p);
   const long long ctas = static_cast<long long>(p.B) * p.Hkv * p.n_ktiles;
   if constexpr (D <= 64) {
     // persistent warp-specialised pipeline: one CTA per SM takes key tiles from the ticket counter
@@ -100,10 +127,11 @@ int launch_bwd(const swa::BwdParams& p, const swa_host::LibCtx& ctx, cudaStream_
     swa::attn_bwd_kernel<D><<<static_cast<unsigned>(ctas), swa::BwdCfg<D>::kThreads, swa::BwdCfg<D>::kSmemBytes,
                               st>>>(p, maps);
   }
-  const long long fin_rows = static_cast<long long>(p.B) * p.T * (p.H + p.Hkv);  // q rows, then k rows
-  const long long dq_blocks = (fin_rows * (D / 8) + 255) / 256;
-  const int dq_grid = static_cast<int>(dq_blocks < 8L * ctx.sm_count ? dq_blocks : 8L * ctx.sm_count);
-  swa::attn_bwd_dq_kernel<D><<<dq_grid, 256, 0, st>>>(p);
+  const long long fin_groups = (nq + FC::kRows - 1) / FC::kRows + (nk + FC::kRows - 1) / FC::kRows;
+  const long long fin_cap = static_cast<long long>(g_fin_ctas_per_sm[D / 64]) * ctx.sm_count;
+  const long long fin_need = (fin_groups + FC::kWarps - 1) / FC::kWarps;
+  const int fin_grid = static_cast<int>(fin_need < fin_cap ? fin_need : fin_cap);
+  swa::attn_bwd_dq_kernel<D><<<fin_grid, FC::kWarps * 32, FC::kSmemBytes, st>>>(p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

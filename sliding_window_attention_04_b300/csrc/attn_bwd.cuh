@@ -98,113 +98,207 @@ __device__ __forceinline__ void stage_row32(uint8_t* box, int row, const uint32_
 
 // ------------------------------------------------------------------------------------------------
 // 1. prep
+//
+// Both passes around the main kernel stream rows and are bound by memory latency. Every warp owns a
+// ring of shared-memory stages and fills them with cp.async (16-byte chunks, each copy instruction
+// covering contiguous bytes), kStages - 1 groups of rows ahead of the group it computes, so the
+// next group's loads are in flight without being held in registers. A warp touches only its own
+// stages: cp.async.wait_group then __syncwarp() publishes a stage to the warp's lanes, and a
+// __syncwarp() after the computation ends their reads before the stage is refilled. There is no
+// wait on another warp.
 
 template <int D>
-__device__ __forceinline__ void load_row_words(const __nv_bfloat16* src, uint32_t (&w)[D / 2]) {
-  const uint4* s4 = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int c = 0; c < D / 8; ++c) set_chunk<D>(w, c, __ldg(s4 + c));
+struct PrepCfg {
+  static constexpr int kWarps = 8;
+  static constexpr int kStages = 2;                 // one group in flight while one is computed
+  static constexpr int kMinCtas = 2;                // 16 warps per SM at D <= 64 (shared memory)
+  static constexpr int kQRows = 16;                 // rows of a q group: q, out, dout and lse
+  static constexpr int kKRows = 48;                 // rows of a k group (the same bytes per stage)
+  static constexpr int kArr = kQRows * 2 * D;       // 16 bf16 rows
+  static constexpr int kStageBytes = 3 * kArr + kQRows * 4;
+  static constexpr int kSmemBytes = kWarps * kStages * kStageBytes;
+};
+
+// Byte offset of 16-byte chunk c of staged bf16 row r. Rows are 2D bytes apart and the chunk index
+// is XOR-swizzled per row, so that the two-lanes-per-row reads below (16 rows, 8 bytes per lane)
+// take the minimum two shared-memory wavefronts.
+template <int D>
+__device__ __forceinline__ uint32_t prep_pos(int r, int c) {
+  const int sw = D == 32 ? ((r >> 1) & 3) : (r & 7);
+  return static_cast<uint32_t>(r * 2 * D + 16 * (c ^ sw));
 }
 
-// Two lanes per row, as the forward's prologue splits a row: lane e owns, in every 16-byte chunk c,
-// the 8 bytes at 8e (elements 8c + 4e .. 8c + 4e + 3). A RoPE pair (i, i + D/2) keeps i mod 8, so
-// both elements of a pair belong to one lane; the eight partial sums of squares P_m (m = d mod 8)
-// run over the chunks in increasing order, four per lane, and combine with one shuffle in the tree
-// ((P0 + P2) + (P4 + P6), (P1 + P3) + (P5 + P7)) of the forward's qk_row_transform_packed, so q^ and
-// k^ are bit-identical to the forward's.
+// Fill one stage with group `grp` (q groups first, then k groups) and commit it; past the last group
+// the commit is empty, which keeps one commit per iteration.
 template <int D>
-__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
-  constexpr int NC = D / 8;  // 16-byte chunks per row
-  const int e = threadIdx.x & 1;
-  if (blockIdx.x == 0 && threadIdx.x == 0) *p.tickets = 0;
-  const long long nq = static_cast<long long>(p.B) * p.T * p.H;
-  const long long nk = static_cast<long long>(p.B) * p.T * p.Hkv;
-  // the loop runs per warp (16 rows a step) so that every lane takes part in the shuffles
-  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
-  for (long long base = (static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * 16;
-       base < nq + nk; base += warps * 16) {
-    const long long row = base + (threadIdx.x & 31) / 2;
-    const bool valid = row < nq + nk;
-    const bool isq = row < nq;
-    const long long r = valid ? (isq ? row : row - nq) : 0;
-    const int heads = isq ? p.H : p.Hkv;
-    const int t = static_cast<int>((r / heads) % p.T);
-    const uint2* src = reinterpret_cast<const uint2*>((isq ? p.q : p.k) + r * D) + e;
-    uint64_t x[2 * NC];  // x[2c], x[2c + 1]: elements 8c + 4e + {0, 1} and {2, 3}
+__device__ __forceinline__ void prep_issue(const BwdParams& p, uint8_t* sb, long long grp, long long nqg, long long nkg,
+                                           long long nq, long long nk, int lane) {
+  using C = PrepCfg<D>;
+  constexpr int NC = D / 8;
+  if (grp < nqg) {
+    const long long row0 = grp * C::kQRows;
+    for (int i = lane; i < C::kQRows * NC; i += 32) {
+      const int r = i / NC, c = i % NC;
+      const long long row = row0 + r;
+      const bool v = row < nq;
+      const size_t off = static_cast<size_t>(v ? row : 0) * D + 8 * c;
+      const uint32_t pos = prep_pos<D>(r, c), n = v ? 16u : 0u;
+      cp_async16(sb + pos, p.q + off, n);
+      cp_async16(sb + C::kArr + pos, p.out + off, n);
+      cp_async16(sb + 2 * C::kArr + pos, p.dout + off, n);
+    }
+    if (lane < C::kQRows) {
+      const long long row = row0 + lane;
+      if (row < nq) {
+        const long long bt = row / p.H;
+        const int h = static_cast<int>(row - bt * p.H);
+        const int t = static_cast<int>(bt % p.T);
+        const long long b = bt / p.T;
+        cp_async4(sb + 3 * C::kArr + 4 * lane, p.lse + (b * p.H + h) * p.T + t);
+      }
+    }
+  } else if (grp < nqg + nkg) {
+    const long long row0 = (grp - nqg) * C::kKRows;
+    for (int i = lane; i < C::kKRows * NC; i += 32) {
+      const int r = i / NC, c = i % NC;
+      const long long row = row0 + r;
+      const bool v = row < nk;
+      cp_async16(sb + prep_pos<D>(r, c), p.k + static_cast<size_t>(v ? row : 0) * D + 8 * c, v ? 16u : 0u);
+    }
+  }
+  cp_async_commit();
+}
+
+// QK-norm + RoPE of one staged row, two lanes per row as the forward's prologue splits a row: lane e
+// owns, in every 16-byte chunk c, the 8 bytes at 8e (elements 8c + 4e .. 8c + 4e + 3). A RoPE pair
+// (i, i + D/2) keeps i mod 8, so both elements of a pair belong to one lane; the eight partial sums
+// of squares P_m (m = d mod 8) run over the chunks in increasing order, four per lane, and combine
+// with one shuffle in the tree ((P0 + P2) + (P4 + P6), (P1 + P3) + (P5 + P7)) of the forward's
+// qk_row_transform_packed, so q^ and k^ are bit-identical to the forward's. Every lane of the warp
+// calls it (the shuffle); `valid` gates the store.
+template <int D>
+__device__ __forceinline__ void prep_row(const BwdParams& p, const uint8_t* rows, int rr, int e, bool valid, int t,
+                                         __nv_bfloat16* dst_row) {
+  constexpr int NC = D / 8;
+  uint64_t x[2 * NC];  // x[2c], x[2c + 1]: elements 8c + 4e + {0, 1} and {2, 3}
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const uint2 u = *reinterpret_cast<const uint2*>(rows + prep_pos<D>(rr, c) + 8 * e);
+    x[2 * c] = bf16x2_to_f2<D>(u.x);
+    x[2 * c + 1] = bf16x2_to_f2<D>(u.y);
+  }
+  float rs = 1.0f;
+  if (p.use_norm) {
+    uint64_t acc0 = 0, acc1 = 0;  // (P_4e, P_4e+1), (P_4e+2, P_4e+3)
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-      const uint2 u = valid ? __ldg(src + 2 * c) : make_uint2(0, 0);
-      x[2 * c] = bf16x2_to_f2<D>(u.x);
-      x[2 * c + 1] = bf16x2_to_f2<D>(u.y);
+      acc0 = f2_fma(x[2 * c], x[2 * c], acc0);
+      acc1 = f2_fma(x[2 * c + 1], x[2 * c + 1], acc1);
     }
-    float rs = 1.0f;
-    if (p.use_norm) {
-      uint64_t acc0 = 0, acc1 = 0;  // (P_4e, P_4e+1), (P_4e+2, P_4e+3)
+    const uint64_t mine = f2_add(acc0, acc1);  // e=0: (P0+P2, P1+P3); e=1: (P4+P6, P5+P7)
+    const uint64_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
+    const uint64_t tot = e == 0 ? f2_add(mine, other) : f2_add(other, mine);
+    const float ss = __fadd_rn(f2_lo(tot), f2_hi(tot));
+    const float ms = __fmul_rn(ss, 1.0f / D);
+    rs = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, p.eps)));
+  }
+  const uint64_t r2 = f2_pack(rs, rs);
+  uint2* dst = reinterpret_cast<uint2*>(dst_row) + e;
+  if (p.rope != nullptr) {
+    const uint64_t nr2 = f2_pack(-rs, -rs);
+    const float4* tab = p.rope + t;
+#pragma unroll
+    for (int c = 0; c < NC / 2; ++c) {
+      uint32_t wa[2], wb[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        // pairs 8c + 4e + 2q + {0, 1}: table entry 4c + 2e + q
+        const float4 tt = __ldg(tab + static_cast<size_t>(4 * c + 2 * e + q) * p.rope_T);
+        const uint64_t cos2 = f2_pack(tt.x, tt.y), sin2 = f2_pack(tt.z, tt.w);
+        const uint64_t c2 = f2_mul(cos2, r2), s2 = f2_mul(sin2, r2), sn2 = f2_mul(sin2, nr2);
+        const uint64_t x1 = x[2 * c + q], x2 = x[2 * (c + NC / 2) + q];
+        wa[q] = f2_to_bf16x2(f2_fma(x1, c2, f2_mul(x2, s2)));
+        wb[q] = f2_to_bf16x2(f2_fma(x2, c2, f2_mul(x1, sn2)));
+      }
+      if (valid) {
+        dst[2 * c] = make_uint2(wa[0], wa[1]);
+        dst[2 * (c + NC / 2)] = make_uint2(wb[0], wb[1]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+      if (valid) dst[2 * c] = make_uint2(f2_to_bf16x2(f2_mul(x[2 * c], r2)), f2_to_bf16x2(f2_mul(x[2 * c + 1], r2)));
+  }
+}
+
+// q^, k^ into the workspace; per q row delta = rowsum(dO * out) (fp32, any order) and -lse log2(e)
+// into the padded [B, H, Tp] rows; the dq^ accumulator of the q rows cleared; the ticket counter reset.
+template <int D>
+__global__ void __launch_bounds__(256, PrepCfg<D>::kMinCtas) attn_bwd_prep_kernel(const BwdParams p) {
+  using C = PrepCfg<D>;
+  constexpr int NC = D / 8;
+  extern __shared__ __align__(16) uint8_t prep_smem[];
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.tickets = 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e = lane & 1, rl = lane >> 1;  // this lane's half and row of a 16-row step
+  const long long nq = static_cast<long long>(p.B) * p.T * p.H;
+  const long long nk = static_cast<long long>(p.B) * p.T * p.Hkv;
+  const long long nqg = (nq + C::kQRows - 1) / C::kQRows, nkg = (nk + C::kKRows - 1) / C::kKRows;
+  const long long gw = static_cast<long long>(blockIdx.x) * C::kWarps + warp;
+  const long long nw = static_cast<long long>(gridDim.x) * C::kWarps;
+  uint8_t* ring = prep_smem + warp * C::kStages * C::kStageBytes;
+#pragma unroll
+  for (int s = 0; s < C::kStages - 1; ++s) prep_issue<D>(p, ring + s * C::kStageBytes, gw + s * nw, nqg, nkg, nq, nk, lane);
+  int it = 0;
+  for (long long grp = gw; grp < nqg + nkg; grp += nw, ++it) {
+    prep_issue<D>(p, ring + ((it + C::kStages - 1) % C::kStages) * C::kStageBytes, grp + (C::kStages - 1) * nw, nqg,
+                  nkg, nq, nk, lane);
+    cp_async_wait<C::kStages - 1>();
+    __syncwarp();
+    const uint8_t* sb = ring + (it % C::kStages) * C::kStageBytes;
+    if (grp < nqg) {
+      const long long row0 = grp * C::kQRows, row = row0 + rl;
+      const bool valid = row < nq;
+      const long long bt = row / p.H;
+      const int t = static_cast<int>(bt % p.T);
+      prep_row<D>(p, sb, rl, e, valid, t, p.qh + (valid ? row : 0) * D);
+      uint64_t acc = 0;
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        acc0 = f2_fma(x[2 * c], x[2 * c], acc0);
-        acc1 = f2_fma(x[2 * c + 1], x[2 * c + 1], acc1);
-      }
-      const uint64_t mine = f2_add(acc0, acc1);  // e=0: (P0+P2, P1+P3); e=1: (P4+P6, P5+P7)
-      const uint64_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
-      const uint64_t tot = e == 0 ? f2_add(mine, other) : f2_add(other, mine);
-      const float ss = __fadd_rn(f2_lo(tot), f2_hi(tot));
-      const float ms = __fmul_rn(ss, 1.0f / D);
-      rs = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, p.eps)));
-    }
-    const uint64_t r2 = f2_pack(rs, rs);
-    uint2* dst = reinterpret_cast<uint2*>((isq ? p.qh : p.kh) + r * D) + e;
-    if (p.rope != nullptr) {
-      const uint64_t nr2 = f2_pack(-rs, -rs);
-      const float4* tab = p.rope + t;
-#pragma unroll
-      for (int c = 0; c < NC / 2; ++c) {
-        uint32_t wa[2], wb[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          // pairs 8c + 4e + 2q + {0, 1}: table entry 4c + 2e + q
-          const float4 tt = __ldg(tab + static_cast<size_t>(4 * c + 2 * e + q) * p.rope_T);
-          const uint64_t cos2 = f2_pack(tt.x, tt.y), sin2 = f2_pack(tt.z, tt.w);
-          const uint64_t c2 = f2_mul(cos2, r2), s2 = f2_mul(sin2, r2), sn2 = f2_mul(sin2, nr2);
-          const uint64_t x1 = x[2 * c + q], x2 = x[2 * (c + NC / 2) + q];
-          wa[q] = f2_to_bf16x2(f2_fma(x1, c2, f2_mul(x2, s2)));
-          wb[q] = f2_to_bf16x2(f2_fma(x2, c2, f2_mul(x1, sn2)));
-        }
-        if (valid) {
-          dst[2 * c] = make_uint2(wa[0], wa[1]);
-          dst[2 * (c + NC / 2)] = make_uint2(wb[0], wb[1]);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int c = 0; c < NC; ++c)
-        if (valid) dst[2 * c] = make_uint2(f2_to_bf16x2(f2_mul(x[2 * c], r2)), f2_to_bf16x2(f2_mul(x[2 * c + 1], r2)));
-    }
-    // delta = rowsum(dO * out) (fp32, any order) and -lse log2(e) of q rows; the dq^ accumulator cleared
-    const bool qrow = valid && isq;
-    uint64_t acc = 0;
-    if (qrow) {
-      const uint2* o2 = reinterpret_cast<const uint2*>(p.out + r * D) + e;
-      const uint2* g2 = reinterpret_cast<const uint2*>(p.dout + r * D) + e;
-#pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        const uint2 uo = __ldg(o2 + 2 * c), ug = __ldg(g2 + 2 * c);
+        const uint32_t pos = prep_pos<D>(rl, c) + 8 * e;
+        const uint2 uo = *reinterpret_cast<const uint2*>(sb + C::kArr + pos);
+        const uint2 ug = *reinterpret_cast<const uint2*>(sb + 2 * C::kArr + pos);
         acc = f2_fma(bf16x2_to_f2<D>(ug.x), bf16x2_to_f2<D>(uo.x), acc);
         acc = f2_fma(bf16x2_to_f2<D>(ug.y), bf16x2_to_f2<D>(uo.y), acc);
       }
-      float4* z = reinterpret_cast<float4*>(p.dqh + r * D) + e;
-#pragma unroll
-      for (int c = 0; c < NC; ++c) z[2 * c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      float d = f2_lo(acc) + f2_hi(acc);
+      d += __shfl_xor_sync(0xffffffffu, d, 1);
+      if (valid && e == 0) {
+        const int h = static_cast<int>(row - bt * p.H);
+        const long long b = bt / p.T;
+        const float lse = *reinterpret_cast<const float*>(sb + 3 * C::kArr + 4 * rl);
+        p.delta[(b * p.H + h) * p.Tp + t] = d;
+        p.nlse[(b * p.H + h) * p.Tp + t] = -lse * 1.4426950408889634f;
+      }
+      // the group's dq^ rows are contiguous: cleared by coalesced 16-byte stores
+      float4* z = reinterpret_cast<float4*>(p.dqh + row0 * D);
+      for (int i = lane; i < C::kQRows * D / 4; i += 32)
+        if (row0 + i / (D / 4) < nq) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      const long long row0 = (grp - nqg) * C::kKRows;
+#pragma unroll 1
+      for (int s = 0; s < C::kKRows / 16; ++s) {
+        const int rr = 16 * s + rl;
+        const long long row = row0 + rr;
+        const bool valid = row < nk;
+        const int t = static_cast<int>((row / p.Hkv) % p.T);
+        prep_row<D>(p, sb, rr, e, valid, t, p.kh + (valid ? row : 0) * D);
+      }
     }
-    float d = f2_lo(acc) + f2_hi(acc);
-    d += __shfl_xor_sync(0xffffffffu, d, 1);
-    if (qrow && e == 0) {
-      const int h = static_cast<int>(r % p.H);
-      const long long b = r / (static_cast<long long>(p.T) * p.H);
-      p.delta[(b * p.H + h) * p.Tp + t] = d;
-      p.nlse[(b * p.H + h) * p.Tp + t] = -__ldg(p.lse + (b * p.H + h) * p.T + t) * 1.4426950408889634f;
-    }
+    __syncwarp();
   }
+  cp_async_wait<0>();
   // padding of delta / nlse past T
   const int pad = p.Tp - p.T;
   if (pad > 0) {
@@ -220,88 +314,176 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
 
 // ------------------------------------------------------------------------------------------------
 // 3. finalize: the norm and RoPE backward of dq^ / sqrt(D) (q rows, from the accumulator) and of
-//    dk^ / sqrt(D) (k rows, in place in dk)
+//    dk^ / sqrt(D) (k rows, in place in dk); rows staged as in the prep pass
 
-// Lanes per row as in the prep kernel (lane c: elements 8c .. 8c + 7), sums across a row's lanes by
-// shuffles, the rotation partner (chunk c xor D/16) by a shuffle.
 template <int D>
-__global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const BwdParams p) {
+struct FinCfg {
+  static constexpr int kWarps = 8;
+  static constexpr int kStages = 2;              // one group in flight while one is computed
+  static constexpr int kMinCtas = 4;             // 32 warps per SM: 3 KB stages, at most 64 registers
+  static constexpr int kRows = 512 / D;          // rows of a group (q rows, then k rows): 3 KB per stage
+  static constexpr int kGBytes = kRows * 4 * D;  // the fp32 gradient rows
+  static constexpr int kXBytes = kRows * 2 * D;  // the bf16 q or k rows
+  static constexpr int kStageBytes = kGBytes + kXBytes;
+  static constexpr int kSmemBytes = kWarps * kStages * kStageBytes;
+};
+
+// Lane c of a row owns the RoPE pairs (i, i + D/2) for i = 4c .. 4c + 3: elements 4c .. 4c + 3 of
+// both halves of the row, so the rotation and its transpose need no shuffle. In shared memory an odd
+// row (at D = 32: a row with bit 1 set) has its two halves swapped, so that the lanes of the rows one
+// 32-lane step covers read their first (second) halves in the minimum number of wavefronts.
+template <int D>
+__device__ __forceinline__ int fin_swap(int r) {
+  return D == 32 ? (r >> 1) & 1 : r & 1;
+}
+// 16-byte unit u (elements 4u .. 4u + 3) of staged fp32 row r
+template <int D>
+__device__ __forceinline__ uint32_t fin_gpos(int r, int u) {
+  return static_cast<uint32_t>(r * 4 * D + 16 * (u ^ ((r & 1) * (D / 8))));
+}
+// 8-byte unit j (elements 4j .. 4j + 3) of staged bf16 row r
+template <int D>
+__device__ __forceinline__ uint32_t fin_xpos(int r, int j) {
+  return static_cast<uint32_t>(FinCfg<D>::kGBytes + r * 2 * D + 8 * (j ^ (fin_swap<D>(r) * (D / 8))));
+}
+
+template <int D>
+__device__ __forceinline__ void fin_issue(const BwdParams& p, uint8_t* sb, long long grp, long long nqg, long long nkg,
+                                          long long nq, long long nk, int lane) {
+  using C = FinCfg<D>;
+  constexpr int NC = D / 8, NU = D / 4;
+  if (grp < nqg + nkg) {
+    const bool isq = grp < nqg;
+    const long long row0 = (isq ? grp : grp - nqg) * C::kRows, n = isq ? nq : nk;
+    const float* gsrc = isq ? p.dqh : p.dk;
+    const __nv_bfloat16* xsrc = isq ? p.q : p.k;
+    for (int i = lane; i < C::kRows * NU; i += 32) {
+      const int r = i / NU, u = i % NU;
+      const long long row = row0 + r;
+      const bool v = row < n;
+      cp_async16(sb + fin_gpos<D>(r, u), gsrc + static_cast<size_t>(v ? row : 0) * D + 4 * u, v ? 16u : 0u);
+    }
+    // 16-byte chunk k of a bf16 row = 8-byte units 2k, 2k + 1 (the swap keeps them adjacent)
+    for (int i = lane; i < C::kRows * NC; i += 32) {
+      const int r = i / NC, k = i % NC;
+      const long long row = row0 + r;
+      const bool v = row < n;
+      cp_async16(sb + fin_xpos<D>(r, 2 * k), xsrc + static_cast<size_t>(v ? row : 0) * D + 8 * k, v ? 16u : 0u);
+    }
+  }
+  cp_async_commit();
+}
+
+// NC = D/8 lanes per row, RPW rows per 32-lane step; the row sums by shuffles among a row's lanes.
+template <int D>
+__global__ void __launch_bounds__(256, FinCfg<D>::kMinCtas) attn_bwd_dq_kernel(const BwdParams p) {
+  using C = FinCfg<D>;
   constexpr int NC = D / 8, RPW = 32 / NC;
-  const int lane = threadIdx.x & 31;
+  extern __shared__ __align__(16) uint8_t fin_smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = lane % NC, sub = lane / NC;
   const long long nq = static_cast<long long>(p.B) * p.T * p.H;
   const long long nk = static_cast<long long>(p.B) * p.T * p.Hkv;
-  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
-  for (long long base = (static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * RPW;
-       base < nq + nk; base += warps * RPW) {
-    const long long row = base + sub;
-    const bool valid = row < nq + nk;
-    const bool isq = row < nq;
-    const long long r = valid ? (isq ? row : row - nq) : 0;
-    const int t = valid ? static_cast<int>((r / (isq ? p.H : p.Hkv)) % p.T) : 0;
-    float* gsrc = isq ? p.dqh + r * D : p.dk + r * D;
-    float* gdst = isq ? p.dq + r * D : p.dk + r * D;
+  const long long nqg = (nq + C::kRows - 1) / C::kRows, nkg = (nk + C::kRows - 1) / C::kRows;
+  const long long gw = static_cast<long long>(blockIdx.x) * C::kWarps + warp;
+  const long long nw = static_cast<long long>(gridDim.x) * C::kWarps;
+  uint8_t* ring = fin_smem + warp * C::kStages * C::kStageBytes;
+#pragma unroll
+  for (int s = 0; s < C::kStages - 1; ++s) fin_issue<D>(p, ring + s * C::kStageBytes, gw + s * nw, nqg, nkg, nq, nk, lane);
+  int it = 0;
+  for (long long grp = gw; grp < nqg + nkg; grp += nw, ++it) {
+    fin_issue<D>(p, ring + ((it + C::kStages - 1) % C::kStages) * C::kStageBytes, grp + (C::kStages - 1) * nw, nqg, nkg,
+                 nq, nk, lane);
+    cp_async_wait<C::kStages - 1>();
+    __syncwarp();
+    const uint8_t* sb = ring + (it % C::kStages) * C::kStageBytes;
+    const bool isq = grp < nqg;
+    const long long row0 = (isq ? grp : grp - nqg) * C::kRows, n = isq ? nq : nk;
+    float* gdst = isq ? p.dq : p.dk;
     const float gscale = isq ? p.scale : 1.0f;  // dk^ arrives already divided by sqrt(D)
-    float g[8], x[8];
-    if (valid) {
-      const float4* a4 = reinterpret_cast<const float4*>(gsrc) + 2 * c;
-      const float4 u0 = a4[0], u1 = a4[1];
-      g[0] = u0.x; g[1] = u0.y; g[2] = u0.z; g[3] = u0.w; g[4] = u1.x; g[5] = u1.y; g[6] = u1.z; g[7] = u1.w;
-      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>((isq ? p.q : p.k) + r * D) + c), x);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) g[e] = x[e] = 0.f;
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) g[e] *= gscale;
-    const bool first = c < NC / 2;
-    const int c1 = c % (NC / 2);
-    float cs[8], sn[8];
-    if (p.rope != nullptr) {
-      const float4* tab = p.rope + t;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float4 tt = __ldg(tab + static_cast<size_t>(4 * c1 + k) * p.rope_T);
-        cs[2 * k] = tt.x; cs[2 * k + 1] = tt.y; sn[2 * k] = tt.z; sn[2 * k + 1] = tt.w;
+    const int heads = isq ? p.H : p.Hkv;
+#pragma unroll 1
+    for (int s = 0; s < C::kRows / RPW; ++s) {
+      const int rr = s * RPW + sub;
+      const long long row = row0 + rr;
+      const bool valid = row < n;
+      const int t = static_cast<int>((row / heads) % p.T);
+      // g1, x1: elements 4c .. 4c + 3; g2, x2: elements D/2 + 4c .. D/2 + 4c + 3
+      float g1[4], g2[4], x1[4], x2[4];
+      {
+        const float4 a = *reinterpret_cast<const float4*>(sb + fin_gpos<D>(rr, c));
+        const float4 b = *reinterpret_cast<const float4*>(sb + fin_gpos<D>(rr, c + NC));
+        g1[0] = a.x * gscale; g1[1] = a.y * gscale; g1[2] = a.z * gscale; g1[3] = a.w * gscale;
+        g2[0] = b.x * gscale; g2[1] = b.y * gscale; g2[2] = b.z * gscale; g2[3] = b.w * gscale;
+        const uint2 xa = *reinterpret_cast<const uint2*>(sb + fin_xpos<D>(rr, c));
+        const uint2 xb = *reinterpret_cast<const uint2*>(sb + fin_xpos<D>(rr, c + NC));
+        x1[0] = __uint_as_float(xa.x << 16); x1[1] = __uint_as_float(xa.x & 0xFFFF0000u);
+        x1[2] = __uint_as_float(xa.y << 16); x1[3] = __uint_as_float(xa.y & 0xFFFF0000u);
+        x2[0] = __uint_as_float(xb.x << 16); x2[1] = __uint_as_float(xb.x & 0xFFFF0000u);
+        x2[2] = __uint_as_float(xb.y << 16); x2[3] = __uint_as_float(xb.y & 0xFFFF0000u);
       }
-      // x <- RoPE(x): first half x1 c + x2 s, second half x2 c - x1 s
-      float o[8];
+      float cs[4], sn[4];
+      if (p.rope != nullptr) {
+        // table entry m holds the cos, sin of pairs 2m, 2m + 1: pairs 4c .. 4c + 3 are entries 2c, 2c + 1
+        const float4* tab = p.rope + t;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = __shfl_xor_sync(0xffffffffu, x[e], NC / 2);
+        for (int k = 0; k < 2; ++k) {
+          const float4 tt = __ldg(tab + static_cast<size_t>(2 * c + k) * p.rope_T);
+          cs[2 * k] = tt.x; cs[2 * k + 1] = tt.y; sn[2 * k] = tt.z; sn[2 * k + 1] = tt.w;
+        }
+        // x <- RoPE(x): first half x1 c + x2 s, second half x2 c - x1 s
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = first ? fmaf(x[e], cs[e], o[e] * sn[e]) : fmaf(x[e], cs[e], -(o[e] * sn[e]));
-    }
-    if (p.use_norm) {
-      float ss = 0.f, dot = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        ss = fmaf(x[e], x[e], ss);
-        dot = fmaf(x[e], g[e], dot);
+        for (int k = 0; k < 4; ++k) {
+          const float y1 = fmaf(x1[k], cs[k], x2[k] * sn[k]);
+          const float y2 = fmaf(x2[k], cs[k], -(x1[k] * sn[k]));
+          x1[k] = y1;
+          x2[k] = y2;
+        }
       }
+      if (p.use_norm) {
+        float ss = 0.f, dot = 0.f;
 #pragma unroll
-      for (int off = 1; off < NC; off <<= 1) {
-        ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        for (int k = 0; k < 4; ++k) {
+          ss = fmaf(x1[k], x1[k], ss);
+          dot = fmaf(x1[k], g1[k], dot);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          ss = fmaf(x2[k], x2[k], ss);
+          dot = fmaf(x2[k], g2[k], dot);
+        }
+#pragma unroll
+        for (int off = 1; off < NC; off <<= 1) {
+          ss += __shfl_xor_sync(0xffffffffu, ss, off);
+          dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        }
+        const float r1 = 1.0f / sqrtf(ss * (1.0f / D) + p.eps);
+        const float c3 = r1 * r1 * r1 * (1.0f / D) * dot;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          g1[k] = fmaf(r1, g1[k], -(c3 * x1[k]));
+          g2[k] = fmaf(r1, g2[k], -(c3 * x2[k]));
+        }
       }
-      const float rr = 1.0f / sqrtf(ss * (1.0f / D) + p.eps);
-      const float c3 = rr * rr * rr * (1.0f / D) * dot;
+      if (p.rope != nullptr) {
+        // transpose of the rotation: dx1 = g1 c - g2 s, dx2 = g1 s + g2 c
 #pragma unroll
-      for (int e = 0; e < 8; ++e) g[e] = fmaf(rr, g[e], -(c3 * x[e]));
+        for (int k = 0; k < 4; ++k) {
+          const float d1 = fmaf(g1[k], cs[k], -(g2[k] * sn[k]));
+          const float d2 = fmaf(g1[k], sn[k], g2[k] * cs[k]);
+          g1[k] = d1;
+          g2[k] = d2;
+        }
+      }
+      if (valid) {
+        float4* o4 = reinterpret_cast<float4*>(gdst + row * D);
+        o4[c] = make_float4(g1[0], g1[1], g1[2], g1[3]);
+        o4[c + NC] = make_float4(g2[0], g2[1], g2[2], g2[3]);
+      }
     }
-    if (p.rope != nullptr) {
-      // transpose of the rotation: dx1 = g1 c - g2 s, dx2 = g1 s + g2 c
-      float o[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = __shfl_xor_sync(0xffffffffu, g[e], NC / 2);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) g[e] = first ? fmaf(g[e], cs[e], -(o[e] * sn[e])) : fmaf(o[e], sn[e], g[e] * cs[e]);
-    }
-    if (valid) {
-      float4* o4 = reinterpret_cast<float4*>(gdst) + 2 * c;
-      o4[0] = make_float4(g[0], g[1], g[2], g[3]);
-      o4[1] = make_float4(g[4], g[5], g[6], g[7]);
-    }
+    __syncwarp();
   }
+  cp_async_wait<0>();
 }
 
 // ------------------------------------------------------------------------------------------------

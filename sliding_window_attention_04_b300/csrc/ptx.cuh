@@ -136,6 +136,22 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
 // Wait until every committed bulk store has completed (global writes done).
 __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Per-thread asynchronous copies global -> shared (cp.async, completed by wait_group; no barrier).
+// 16 bytes through L2 only; with src_bytes = 0 nothing is read and the 16 bytes are zeroed.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's committed groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // TMA load with an L2 eviction-priority hint (createpolicy.fractional policies).
 __device__ __forceinline__ void tma_load_4d_hint(void* dst, const void* tmap, uint64_t* bar, int x, int y, int z,
                                                  int w, uint64_t policy) {
