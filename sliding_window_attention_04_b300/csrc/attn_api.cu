@@ -143,8 +143,12 @@ CUresult encode_tile_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* 
 // cos / sin of t * base^(-2i/D) for t < T, i < D/2, evaluated in double and rounded to fp32.
 // Layout [D/4][T] of float4 (cos_2m, cos_2m+1, sin_2m, sin_2m+1): for a fixed pair group the
 // positions are contiguous, so a warp whose threads hold consecutive rows loads whole lines.
+// One allocation: [D/4][T] (entry m of position t at m T + t: consecutive positions side by side, as
+// the forward's prologue reads a tile of rows), then the same entries [T][D/4] (at T D/4 + t D/4 + m:
+// one position's entries side by side, as the backward's passes read them).
 cudaError_t build_table(int D, float base, int T, float4** out) {
-  std::vector<float4> h(static_cast<size_t>(T) * (D / 4));
+  const size_t n = static_cast<size_t>(T) * (D / 4);
+  std::vector<float4> h(2 * n);
   for (int t = 0; t < T; ++t)
     for (int m = 0; m < D / 4; ++m) {
       float cs[4];
@@ -155,6 +159,7 @@ cudaError_t build_table(int D, float base, int T, float4** out) {
         cs[2 * k + 1] = static_cast<float>(std::sin(theta));
       }
       h[static_cast<size_t>(m) * T + t] = make_float4(cs[0], cs[2], cs[1], cs[3]);
+      h[n + static_cast<size_t>(t) * (D / 4) + m] = make_float4(cs[0], cs[2], cs[1], cs[3]);
     }
   float4* d = nullptr;
   cudaError_t e = cudaMalloc(&d, h.size() * sizeof(float4));
@@ -323,7 +328,7 @@ int locked(const std::function<int(const LibCtx&)>& f) {
   return f(ctx);
 }
 
-int rope_table_locked(int D, float base, int T, const float4** table, int* table_T) {
+int rope_table_locked(int D, float base, int T, const float4** table, int* table_T, const float4** rows) {
   State& s = state();
   RopeTable& t = s.tables[std::make_pair(D, base)];
   if (t.T < T) {
@@ -335,6 +340,7 @@ int rope_table_locked(int D, float base, int T, const float4** table, int* table
   }
   *table = t.ptr;
   *table_T = t.T;
+  if (rows != nullptr) *rows = t.ptr + static_cast<size_t>(t.T) * (D / 4);
   return ATTN_OK;
 }
 

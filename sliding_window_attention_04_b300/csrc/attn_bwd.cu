@@ -194,8 +194,9 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
       }
     }
     const float4* table = nullptr;
+    const float4* rows = nullptr;
     int table_T = 0;
-    if (rope_base > 0.f && swa_host::rope_table_locked(D, rope_base, T, &table, &table_T) != ATTN_OK)
+    if (rope_base > 0.f && swa_host::rope_table_locked(D, rope_base, T, &table, &table_T, &rows) != ATTN_OK)
       return ATTN_ERR_CUDA;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     swa::BwdParams p{};
@@ -214,8 +215,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
     p.nlse = reinterpret_cast<float*>(ws + l.nlse);
     p.tickets = reinterpret_cast<int*>(ws + l.tickets);
     p.dqh = reinterpret_cast<float*>(ws + l.dqh);
-    p.rope = table;
-    p.rope_T = table_T;
+    p.rope = rows;
     p.err = ctx.d_err;
     p.B = B;
     p.H = H;

@@ -53,8 +53,8 @@ struct BwdParams {
   float* nlse;                // workspace: -lse log2(e), [B, H, Tp] (padding: -inf)
   float* dqh;                 // workspace: dq^ accumulator (unscaled) [B, T, H, D]
   int* tickets;               // workspace: work counter of the persistent kernel (cleared by the prologue)
-  const float4* rope;         // cos/sin table as in AttnParams, or nullptr
-  int rope_T;
+  const float4* rope;         // cos/sin table position-major: entry m of position t at rope[t * D/4 + m]
+                              // (cos_2m, cos_2m+1, sin_2m, sin_2m+1), or nullptr
   int* err;
   int B, H, Hkv, kv_group, T;
   int window, causal, use_norm;
@@ -206,14 +206,14 @@ __device__ __forceinline__ void prep_row(const BwdParams& p, const uint8_t* rows
   uint2* dst = reinterpret_cast<uint2*>(dst_row) + e;
   if (p.rope != nullptr) {
     const uint64_t nr2 = f2_pack(-rs, -rs);
-    const float4* tab = p.rope + t;
+    const float4* tab = p.rope + static_cast<size_t>(t) * (D / 4);
 #pragma unroll
     for (int c = 0; c < NC / 2; ++c) {
       uint32_t wa[2], wb[2];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         // pairs 8c + 4e + 2q + {0, 1}: table entry 4c + 2e + q
-        const float4 tt = __ldg(tab + static_cast<size_t>(4 * c + 2 * e + q) * p.rope_T);
+        const float4 tt = __ldg(tab + 4 * c + 2 * e + q);
         const uint64_t cos2 = f2_pack(tt.x, tt.y), sin2 = f2_pack(tt.z, tt.w);
         const uint64_t c2 = f2_mul(cos2, r2), s2 = f2_mul(sin2, r2), sn2 = f2_mul(sin2, nr2);
         const uint64_t x1 = x[2 * c + q], x2 = x[2 * (c + NC / 2) + q];
@@ -425,10 +425,10 @@ __global__ void __launch_bounds__(256, FinCfg<D>::kMinCtas) attn_bwd_dq_kernel(c
       float cs[4], sn[4];
       if (p.rope != nullptr) {
         // table entry m holds the cos, sin of pairs 2m, 2m + 1: pairs 4c .. 4c + 3 are entries 2c, 2c + 1
-        const float4* tab = p.rope + t;
+        const float4* tab = p.rope + static_cast<size_t>(t) * (D / 4);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          const float4 tt = __ldg(tab + static_cast<size_t>(2 * c + k) * p.rope_T);
+          const float4 tt = __ldg(tab + 2 * c + k);
           cs[2 * k] = tt.x; cs[2 * k + 1] = tt.y; sn[2 * k] = tt.z; sn[2 * k + 1] = tt.w;
         }
         // x <- RoPE(x): first half x1 c + x2 s, second half x2 c - x1 s

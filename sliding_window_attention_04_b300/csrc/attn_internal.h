@@ -22,8 +22,9 @@ struct LibCtx {
 int locked(const std::function<int(const LibCtx&)>& f);
 
 // Inside `locked`: the cached fp32 cos/sin table of (D, base) covering at least T positions, laid out
-// [D/4][table_T] of float4 (cos_2m, cos_2m+1, sin_2m, sin_2m+1). Returns ATTN_OK or ATTN_ERR_CUDA.
-int rope_table_locked(int D, float base, int T, const float4** table, int* table_T);
+// [D/4][table_T] of float4 (cos_2m, cos_2m+1, sin_2m, sin_2m+1), and the same entries position-major,
+// [table_T][D/4] (`rows`, may be null if not wanted). Returns ATTN_OK or ATTN_ERR_CUDA.
+int rope_table_locked(int D, float base, int T, const float4** table, int* table_T, const float4** rows = nullptr);
 
 // The 4-D (d, h, t, b) tensor map of a [B, T, H, D] bf16 tensor whose box is one 128-row tile of one
 // head in the tensor core's swizzled layout (64-column boxes for D = 128; rows past T read as zero).
