@@ -131,15 +131,15 @@ __device__ __forceinline__ uint32_t prep_pos(int r, int c) {
 // Fill one stage with group `grp` (q groups first, then k groups) and commit it; past the last group
 // the commit is empty, which keeps one commit per iteration.
 template <int D>
-__device__ __forceinline__ void prep_issue(const BwdParams& p, uint8_t* sb, long long grp, long long nqg, long long nkg,
-                                           long long nq, long long nk, int lane) {
+__device__ __forceinline__ void prep_issue(const BwdParams& p, uint8_t* sb, uint32_t grp, uint32_t nqg, uint32_t nkg,
+                                           uint32_t nq, uint32_t nk, int lane) {
   using C = PrepCfg<D>;
   constexpr int NC = D / 8;
   if (grp < nqg) {
-    const long long row0 = grp * C::kQRows;
+    const uint32_t row0 = grp * C::kQRows;
     for (int i = lane; i < C::kQRows * NC; i += 32) {
       const int r = i / NC, c = i % NC;
-      const long long row = row0 + r;
+      const uint32_t row = row0 + r;
       const bool v = row < nq;
       const size_t off = static_cast<size_t>(v ? row : 0) * D + 8 * c;
       const uint32_t pos = prep_pos<D>(r, c), n = v ? 16u : 0u;
@@ -148,20 +148,18 @@ __device__ __forceinline__ void prep_issue(const BwdParams& p, uint8_t* sb, long
       cp_async16(sb + 2 * C::kArr + pos, p.dout + off, n);
     }
     if (lane < C::kQRows) {
-      const long long row = row0 + lane;
+      const uint32_t row = row0 + lane;
       if (row < nq) {
-        const long long bt = row / p.H;
-        const int h = static_cast<int>(row - bt * p.H);
-        const int t = static_cast<int>(bt % p.T);
-        const long long b = bt / p.T;
-        cp_async4(sb + 3 * C::kArr + 4 * lane, p.lse + (b * p.H + h) * p.T + t);
+        const uint32_t bt = row / static_cast<uint32_t>(p.H);
+        const uint32_t h = row - bt * p.H, t = bt % static_cast<uint32_t>(p.T), b = bt / static_cast<uint32_t>(p.T);
+        cp_async4(sb + 3 * C::kArr + 4 * lane, p.lse + (static_cast<size_t>(b) * p.H + h) * p.T + t);
       }
     }
   } else if (grp < nqg + nkg) {
-    const long long row0 = (grp - nqg) * C::kKRows;
+    const uint32_t row0 = (grp - nqg) * C::kKRows;
     for (int i = lane; i < C::kKRows * NC; i += 32) {
       const int r = i / NC, c = i % NC;
-      const long long row = row0 + r;
+      const uint32_t row = row0 + r;
       const bool v = row < nk;
       cp_async16(sb + prep_pos<D>(r, c), p.k + static_cast<size_t>(v ? row : 0) * D + 8 * c, v ? 16u : 0u);
     }
@@ -242,27 +240,26 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::kMinCtas) attn_bwd_prep_kerne
   if (blockIdx.x == 0 && threadIdx.x == 0) *p.tickets = 0;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int e = lane & 1, rl = lane >> 1;  // this lane's half and row of a 16-row step
-  const long long nq = static_cast<long long>(p.B) * p.T * p.H;
-  const long long nk = static_cast<long long>(p.B) * p.T * p.Hkv;
-  const long long nqg = (nq + C::kQRows - 1) / C::kQRows, nkg = (nk + C::kKRows - 1) / C::kKRows;
-  const long long gw = static_cast<long long>(blockIdx.x) * C::kWarps + warp;
-  const long long nw = static_cast<long long>(gridDim.x) * C::kWarps;
+  // row and group indices fit 32 bits: the host admits B T H D < 2^31
+  const uint32_t nq = static_cast<uint32_t>(p.B) * p.T * p.H, nk = static_cast<uint32_t>(p.B) * p.T * p.Hkv;
+  const uint32_t nqg = (nq + C::kQRows - 1) / C::kQRows, nkg = (nk + C::kKRows - 1) / C::kKRows;
+  const uint32_t gw = blockIdx.x * C::kWarps + warp, nw = gridDim.x * C::kWarps;
   uint8_t* ring = prep_smem + warp * C::kStages * C::kStageBytes;
 #pragma unroll
   for (int s = 0; s < C::kStages - 1; ++s) prep_issue<D>(p, ring + s * C::kStageBytes, gw + s * nw, nqg, nkg, nq, nk, lane);
   int it = 0;
-  for (long long grp = gw; grp < nqg + nkg; grp += nw, ++it) {
+  for (uint32_t grp = gw; grp < nqg + nkg; grp += nw, ++it) {
     prep_issue<D>(p, ring + ((it + C::kStages - 1) % C::kStages) * C::kStageBytes, grp + (C::kStages - 1) * nw, nqg,
                   nkg, nq, nk, lane);
     cp_async_wait<C::kStages - 1>();
     __syncwarp();
     const uint8_t* sb = ring + (it % C::kStages) * C::kStageBytes;
     if (grp < nqg) {
-      const long long row0 = grp * C::kQRows, row = row0 + rl;
+      const uint32_t row0 = grp * C::kQRows, row = row0 + rl;
       const bool valid = row < nq;
-      const long long bt = row / p.H;
-      const int t = static_cast<int>(bt % p.T);
-      prep_row<D>(p, sb, rl, e, valid, t, p.qh + (valid ? row : 0) * D);
+      const uint32_t bt = row / static_cast<uint32_t>(p.H);
+      const uint32_t t = bt % static_cast<uint32_t>(p.T);
+      prep_row<D>(p, sb, rl, e, valid, static_cast<int>(t), p.qh + static_cast<size_t>(valid ? row : 0) * D);
       uint64_t acc = 0;
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
@@ -275,25 +272,25 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::kMinCtas) attn_bwd_prep_kerne
       float d = f2_lo(acc) + f2_hi(acc);
       d += __shfl_xor_sync(0xffffffffu, d, 1);
       if (valid && e == 0) {
-        const int h = static_cast<int>(row - bt * p.H);
-        const long long b = bt / p.T;
+        const uint32_t h = row - bt * p.H, b = bt / static_cast<uint32_t>(p.T);
         const float lse = *reinterpret_cast<const float*>(sb + 3 * C::kArr + 4 * rl);
-        p.delta[(b * p.H + h) * p.Tp + t] = d;
-        p.nlse[(b * p.H + h) * p.Tp + t] = -lse * 1.4426950408889634f;
+        const size_t o = (static_cast<size_t>(b) * p.H + h) * p.Tp + t;
+        p.delta[o] = d;
+        p.nlse[o] = -lse * 1.4426950408889634f;
       }
       // the group's dq^ rows are contiguous: cleared by coalesced 16-byte stores
-      float4* z = reinterpret_cast<float4*>(p.dqh + row0 * D);
+      float4* z = reinterpret_cast<float4*>(p.dqh + static_cast<size_t>(row0) * D);
       for (int i = lane; i < C::kQRows * D / 4; i += 32)
         if (row0 + i / (D / 4) < nq) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     } else {
-      const long long row0 = (grp - nqg) * C::kKRows;
+      const uint32_t row0 = (grp - nqg) * C::kKRows;
 #pragma unroll 1
       for (int s = 0; s < C::kKRows / 16; ++s) {
         const int rr = 16 * s + rl;
-        const long long row = row0 + rr;
+        const uint32_t row = row0 + rr;
         const bool valid = row < nk;
-        const int t = static_cast<int>((row / p.Hkv) % p.T);
-        prep_row<D>(p, sb, rr, e, valid, t, p.kh + (valid ? row : 0) * D);
+        const uint32_t t = (row / static_cast<uint32_t>(p.Hkv)) % static_cast<uint32_t>(p.T);
+        prep_row<D>(p, sb, rr, e, valid, static_cast<int>(t), p.kh + static_cast<size_t>(valid ? row : 0) * D);
       }
     }
     __syncwarp();
@@ -348,25 +345,25 @@ __device__ __forceinline__ uint32_t fin_xpos(int r, int j) {
 }
 
 template <int D>
-__device__ __forceinline__ void fin_issue(const BwdParams& p, uint8_t* sb, long long grp, long long nqg, long long nkg,
-                                          long long nq, long long nk, int lane) {
+__device__ __forceinline__ void fin_issue(const BwdParams& p, uint8_t* sb, uint32_t grp, uint32_t nqg, uint32_t nkg,
+                                          uint32_t nq, uint32_t nk, int lane) {
   using C = FinCfg<D>;
   constexpr int NC = D / 8, NU = D / 4;
   if (grp < nqg + nkg) {
     const bool isq = grp < nqg;
-    const long long row0 = (isq ? grp : grp - nqg) * C::kRows, n = isq ? nq : nk;
+    const uint32_t row0 = (isq ? grp : grp - nqg) * C::kRows, n = isq ? nq : nk;
     const float* gsrc = isq ? p.dqh : p.dk;
     const __nv_bfloat16* xsrc = isq ? p.q : p.k;
     for (int i = lane; i < C::kRows * NU; i += 32) {
       const int r = i / NU, u = i % NU;
-      const long long row = row0 + r;
+      const uint32_t row = row0 + r;
       const bool v = row < n;
       cp_async16(sb + fin_gpos<D>(r, u), gsrc + static_cast<size_t>(v ? row : 0) * D + 4 * u, v ? 16u : 0u);
     }
     // 16-byte chunk k of a bf16 row = 8-byte units 2k, 2k + 1 (the swap keeps them adjacent)
     for (int i = lane; i < C::kRows * NC; i += 32) {
       const int r = i / NC, k = i % NC;
-      const long long row = row0 + r;
+      const uint32_t row = row0 + r;
       const bool v = row < n;
       cp_async16(sb + fin_xpos<D>(r, 2 * k), xsrc + static_cast<size_t>(v ? row : 0) * D + 8 * k, v ? 16u : 0u);
     }
@@ -382,32 +379,30 @@ __global__ void __launch_bounds__(256, FinCfg<D>::kMinCtas) attn_bwd_dq_kernel(c
   extern __shared__ __align__(16) uint8_t fin_smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = lane % NC, sub = lane / NC;
-  const long long nq = static_cast<long long>(p.B) * p.T * p.H;
-  const long long nk = static_cast<long long>(p.B) * p.T * p.Hkv;
-  const long long nqg = (nq + C::kRows - 1) / C::kRows, nkg = (nk + C::kRows - 1) / C::kRows;
-  const long long gw = static_cast<long long>(blockIdx.x) * C::kWarps + warp;
-  const long long nw = static_cast<long long>(gridDim.x) * C::kWarps;
+  const uint32_t nq = static_cast<uint32_t>(p.B) * p.T * p.H, nk = static_cast<uint32_t>(p.B) * p.T * p.Hkv;
+  const uint32_t nqg = (nq + C::kRows - 1) / C::kRows, nkg = (nk + C::kRows - 1) / C::kRows;
+  const uint32_t gw = blockIdx.x * C::kWarps + warp, nw = gridDim.x * C::kWarps;
   uint8_t* ring = fin_smem + warp * C::kStages * C::kStageBytes;
 #pragma unroll
   for (int s = 0; s < C::kStages - 1; ++s) fin_issue<D>(p, ring + s * C::kStageBytes, gw + s * nw, nqg, nkg, nq, nk, lane);
   int it = 0;
-  for (long long grp = gw; grp < nqg + nkg; grp += nw, ++it) {
+  for (uint32_t grp = gw; grp < nqg + nkg; grp += nw, ++it) {
     fin_issue<D>(p, ring + ((it + C::kStages - 1) % C::kStages) * C::kStageBytes, grp + (C::kStages - 1) * nw, nqg, nkg,
                  nq, nk, lane);
     cp_async_wait<C::kStages - 1>();
     __syncwarp();
     const uint8_t* sb = ring + (it % C::kStages) * C::kStageBytes;
     const bool isq = grp < nqg;
-    const long long row0 = (isq ? grp : grp - nqg) * C::kRows, n = isq ? nq : nk;
+    const uint32_t row0 = (isq ? grp : grp - nqg) * C::kRows, n = isq ? nq : nk;
     float* gdst = isq ? p.dq : p.dk;
     const float gscale = isq ? p.scale : 1.0f;  // dk^ arrives already divided by sqrt(D)
-    const int heads = isq ? p.H : p.Hkv;
+    const uint32_t heads = static_cast<uint32_t>(isq ? p.H : p.Hkv);
 #pragma unroll 1
     for (int s = 0; s < C::kRows / RPW; ++s) {
       const int rr = s * RPW + sub;
-      const long long row = row0 + rr;
+      const uint32_t row = row0 + rr;
       const bool valid = row < n;
-      const int t = static_cast<int>((row / heads) % p.T);
+      const int t = static_cast<int>((row / heads) % static_cast<uint32_t>(p.T));
       // g1, x1: elements 4c .. 4c + 3; g2, x2: elements D/2 + 4c .. D/2 + 4c + 3
       float g1[4], g2[4], x1[4], x2[4];
       {
@@ -476,7 +471,7 @@ __global__ void __launch_bounds__(256, FinCfg<D>::kMinCtas) attn_bwd_dq_kernel(c
         }
       }
       if (valid) {
-        float4* o4 = reinterpret_cast<float4*>(gdst + row * D);
+        float4* o4 = reinterpret_cast<float4*>(gdst + static_cast<size_t>(row) * D);
         o4[c] = make_float4(g1[0], g1[1], g1[2], g1[3]);
         o4[c + NC] = make_float4(g2[0], g2[1], g2[2], g2[3]);
       }
