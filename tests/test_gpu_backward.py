@@ -73,6 +73,9 @@ CASES = [  # (B, T, H, Hkv, D, window, causal, rope_base, eps)
     (1, 130, 2, 2, 64, -1, True, 0.0, -1.0),
     (1, 640, 2, 2, 64, 0, True, 10000.0, 1e-6),
     (1, 520, 4, 1, 128, 200, True, 500.0, 1e-6),
+    # odd row counts (111 q rows, 37 k rows): ragged last groups of the staged prologue and finalize
+    (1, 37, 3, 1, 32, 16, True, 10000.0, 1e-6),
+    (3, 45, 3, 3, 64, 20, True, 10000.0, 1e-6),
 ]
 
 
