@@ -99,8 +99,8 @@ __device__ __forceinline__ void stage_row32(uint8_t* box, int row, const uint32_
 // ------------------------------------------------------------------------------------------------
 // 1. prep
 //
-// Both passes around the main kernel stream rows and are bound by memory latency. Every warp owns a
-// ring of shared-memory stages and fills them with cp.async (16-byte chunks, each copy instruction
+// Both passes around the main kernel stream rows; with plain loads they were bound by memory latency
+// (few bytes in flight per warp). Every warp owns a ring of shared-memory stages and fills them with cp.async (16-byte chunks, each copy instruction
 // covering contiguous bytes), kStages - 1 groups of rows ahead of the group it computes, so the
 // next group's loads are in flight without being held in registers. A warp touches only its own
 // stages: cp.async.wait_group then __syncwarp() publishes a stage to the warp's lanes, and a
@@ -111,7 +111,8 @@ template <int D>
 struct PrepCfg {
   static constexpr int kWarps = 8;
   static constexpr int kStages = 2;                 // one group in flight while one is computed
-  static constexpr int kMinCtas = 2;                // 16 warps per SM at D <= 64 (shared memory)
+  static constexpr int kMinCtas = 2;                // registers for two CTAs (16 warps) per SM; at D = 128
+                                                    // shared memory holds one
   static constexpr int kQRows = 16;                 // rows of a q group: q, out, dout and lse
   static constexpr int kKRows = 48;                 // rows of a k group (the same bytes per stage)
   static constexpr int kArr = kQRows * 2 * D;       // 16 bf16 rows
