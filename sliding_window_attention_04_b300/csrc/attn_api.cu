@@ -107,18 +107,29 @@ cudaError_t set_kernel_attrs() {
 
 // The warp-specialised kernel re-divides its registers at run time (setmaxnreg); that split adds
 // up to the registers of the launch only if the kernel was compiled to exactly kLaunchRegs per
-// thread. With any other count the kernel is not used.
-template <int D>
-cudaError_t set_ws_attrs(bool* usable) {
+// thread. With any other count the kernel is not used. Both instantiations (the general one and the
+// one for calls with the QK-norm on and no gate) must pass.
+template <int D, bool kCommon>
+cudaError_t set_ws_attrs_one(bool* usable) {
   *usable = false;
   cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, swa::attn_fwd_ws_kernel<D>);
+  cudaError_t e = cudaFuncGetAttributes(&fa, swa::attn_fwd_ws_kernel<D, kCommon>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != swa::WsCfg<D>::kLaunchRegs) return cudaSuccess;
-  e = cudaFuncSetAttribute(swa::attn_fwd_ws_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(swa::attn_fwd_ws_kernel<D, kCommon>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            swa::WsCfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
   *usable = true;
+  return cudaSuccess;
+}
+
+template <int D>
+cudaError_t set_ws_attrs(bool* usable) {
+  bool general = false, common = false;
+  cudaError_t e = set_ws_attrs_one<D, false>(&general);
+  if (e != cudaSuccess) return e;
+  if ((e = set_ws_attrs_one<D, true>(&common)) != cudaSuccess) return e;
+  *usable = general && common;
   return cudaSuccess;
 }
 
@@ -227,8 +238,14 @@ int launch_ws(const swa::AttnParams& p, std::map<MapKey, CUtensorMap>& cache,
   const long long chunks = static_cast<long long>(p.B) * p.H * ((n_qb + 1) / 2);
   if (chunks >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
   const int grid = static_cast<int>(chunks < sm_count ? chunks : sm_count);
-  swa::attn_fwd_ws_kernel<D><<<grid, swa::WsCfg<D>::kThreads, swa::WsCfg<D>::kSmemBytes, stream>>>(
-      pk, maps, sched, static_cast<int>(chunks));
+  // QK-norm on, no gate: the instantiation without the other modes' code
+  const bool common = p.use_norm && p.ve == nullptr;
+  if (common)
+    swa::attn_fwd_ws_kernel<D, true><<<grid, swa::WsCfg<D>::kThreads, swa::WsCfg<D>::kSmemBytes, stream>>>(
+        pk, maps, sched, static_cast<int>(chunks));
+  else
+    swa::attn_fwd_ws_kernel<D, false><<<grid, swa::WsCfg<D>::kThreads, swa::WsCfg<D>::kSmemBytes, stream>>>(
+        pk, maps, sched, static_cast<int>(chunks));
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -227,10 +227,11 @@ struct RopeHalf {
 // the fp32 row and the cos/sin entries never need to be live at once: the sum of squares chunk by
 // chunk (the same per-residue order as below), then the rotation in two groups of four chunk pairs
 // (c, c + 8), each with its eight table entries.
+template <bool kCommon>
 __device__ __forceinline__ void transform_half_row_d128(uint8_t* tile, int row, int h, int pos, const AttnParams& p) {
   constexpr int D = 128, NC = D / 8;
   float r = 1.0f;
-  if (p.use_norm) {
+  if (kCommon || p.use_norm) {
     uint64_t acc0 = 0, acc1 = 0;  // (P_{4h}, P_{4h+1}), (P_{4h+2}, P_{4h+3})
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
@@ -289,11 +290,14 @@ __device__ __forceinline__ void transform_half_row_d128(uint8_t* tile, int row, 
   }
 }
 
-template <int D>
+// kCommon: the call has the QK-norm on (the common case), so it is not tested at run time. (The RoPE
+// test stays a run-time branch: with it compiled out the D = 64 kernel spills at the prologue's
+// register share.)
+template <int D, bool kCommon>
 __device__ __forceinline__ void transform_half_row_inplace(uint8_t* tile, int row, int h, int pos, RopeHalf<D>& tab,
                                                            const AttnParams& p) {
   if constexpr (D == 128) {
-    transform_half_row_d128(tile, row, h, pos, p);
+    transform_half_row_d128<kCommon>(tile, row, h, pos, p);
     return;
   }
   constexpr int NC = D / 8;  // chunks per row; this thread owns 2 words (4 elements) of each
@@ -305,7 +309,7 @@ __device__ __forceinline__ void transform_half_row_inplace(uint8_t* tile, int ro
     x[2 * c + 1] = bf16x2_to_f2<D>(u.y);
   }
   float r = 1.0f;
-  if (p.use_norm) {
+  if (kCommon || p.use_norm) {
     uint64_t acc0 = 0, acc1 = 0;  // (P_{4h}, P_{4h+1}), (P_{4h+2}, P_{4h+3})
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
@@ -577,7 +581,10 @@ __device__ __forceinline__ float softmax_tile_fixed(bool masked, uint32_t tS, in
   return rowsum;
 }
 
-template <int D>
+// kCommon: the call has the QK-norm on and no value-embedding gate (the common case); that
+// instantiation carries no code for the other modes (the raw softmax with a running maximum and
+// its O rescale, the prologue without the norm, the gate), which keeps the hot loops' code small.
+template <int D, bool kCommon>
 __global__ void __launch_bounds__(640, 1)
     attn_fwd_ws_kernel(const AttnParams p, const __grid_constant__ WsMaps maps, int* sched, int n_chunks) {
   using Cfg = WsCfg<D>;
@@ -854,7 +861,7 @@ __global__ void __launch_bounds__(640, 1)
           // Every load's V phase is observed (and released, at its last use) by both issuers, active
           // or not, so the stage's barriers never run two phases ahead of either of them.
           // a gated call's V tile is read once the prologue has applied the gate to it
-          if (!mbar_wait_or_abort(bar((p.ve != nullptr ? Cfg::kBarVReady : Cfg::kBarVFull) + st), (pos / S) & 1,
+          if (!mbar_wait_or_abort(bar((!kCommon && p.ve != nullptr ? Cfg::kBarVReady : Cfg::kBarVFull) + st), (pos / S) & 1,
                                   abort_flag)) {
             ok = false;
             break;
@@ -925,14 +932,14 @@ __global__ void __launch_bounds__(640, 1)
           ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarKFull + st), (kcnt / S) & 1, abort_flag));
           if (!ok) break;
         }
-        transform_half_row_inplace<D>(tile, r, h, pos < p.T ? pos : 0, tab, p);
+        transform_half_row_inplace<D, kCommon>(tile, r, h, pos < p.T ? pos : 0, tab, p);
         fence_proxy_async_smem();
         __syncwarp();
         if (is_q) {
           if (jb == 1 && lane == 0) mbar_arrive(bar(Cfg::kBarQReady + slot));
         } else {
           if (lane == 0) mbar_arrive(bar(Cfg::kBarKReady + st));
-          if (p.ve != nullptr) {
+          if (!kCommon && p.ve != nullptr) {
             // the value-embedding gate on the same step's V tile, in place
             ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(Cfg::kBarVFull + st), (kcnt / S) & 1, abort_flag));
             if (!ok) break;
@@ -955,7 +962,7 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t tO = tmem + lane_base + Cfg::col_o(t);
     const float scale = p.scale_log2;
     const uint64_t scale2 = f2_pack(scale, scale);
-    const bool fixed_ref = p.ref_log2 > 0.f;
+    const bool fixed_ref = kCommon || p.ref_log2 > 0.f;
     const uint64_t negr2 = f2_pack(-p.ref_log2, -p.ref_log2);
     uint32_t n = 0;   // P tiles written so far by this warpgroup (all units)
     uint32_t gS = 0;  // global S-job index, counted over both query tiles (as the MMA issuer does)
