@@ -149,16 +149,18 @@ def build_inputs(w, device):
 
 def oracle_sample_rows(w, budget_s: float) -> int:
     """How many batch rows of every layer the float64 oracle can do in about `budget_s` seconds:
-    calibrated on one batch row of the first layer (a second, warm call), scaled to every layer by its
-    unmasked score entries."""
+    calibrated on up to four batch rows of the first layer (a second, warm call; one row alone keeps
+    too few of the oracle's threads busy and overestimates the time per row), scaled to every layer by
+    its unmasked score entries."""
     import oracle
 
-    q, k, v = make_qkv(1, w.T, w.H, w.D, seed=layer_seed(w.index, 0))
+    nc = min(w.B, 4)
+    q, k, v = make_qkv(nc, w.T, w.H, w.D, seed=layer_seed(w.index, 0))
     w0 = w.layers[0].window
     oracle.attn_fwd(q, k, v, window=w0, causal=True, rope_base=w.rope_base, eps=w.eps)  # warm-up
     t0 = time.perf_counter()
     oracle.attn_fwd(q, k, v, window=w0, causal=True, rope_base=w.rope_base, eps=w.eps)
-    per_row = time.perf_counter() - t0
+    per_row = (time.perf_counter() - t0) / nc
     weight = sum(configs.n_unmasked(w.T, l.window) for l in w.layers) / configs.n_unmasked(w.T, w0)
     return int(max(1, min(w.B, budget_s / max(per_row * weight, 1e-9))))
 
