@@ -149,12 +149,12 @@ def build_inputs(w, device):
 
 def oracle_sample_rows(w, budget_s: float) -> int:
     """How many batch rows of every layer the float64 oracle can do in about `budget_s` seconds:
-    calibrated on up to four batch rows of the first layer (a second, warm call; one row alone keeps
-    too few of the oracle's threads busy and overestimates the time per row), scaled to every layer by
-    its unmasked score entries."""
+    calibrated on up to sixteen batch rows of the first layer (a second, warm call; fewer rows keep too
+    few of the oracle's threads busy and overestimate the time per row), scaled to every layer by its
+    unmasked score entries."""
     import oracle
 
-    nc = min(w.B, 4)
+    nc = min(w.B, 16)
     q, k, v = make_qkv(nc, w.T, w.H, w.D, seed=layer_seed(w.index, 0))
     w0 = w.layers[0].window
     oracle.attn_fwd(q, k, v, window=w0, causal=True, rope_base=w.rope_base, eps=w.eps)  # warm-up
