@@ -228,14 +228,23 @@ int launch_ws(const swa::AttnParams& p, std::map<MapKey, CUtensorMap>& cache,
   maps.k = *mk;
   maps.v = *mv;
   maps.out = *mo;
-  // work is handed out in chunks of two 256-row query blocks of one head (see the kernel), heads in
-  // groups whose K and V fit in half of L2 together, so a group's blocks share them there
+  // Work is handed out in chunks of 256-row query blocks of one head (see the kernel). Where
+  // consecutive blocks of a head can share key tiles through the ring (causal, window at most the
+  // ring's depth in key tiles), all but the last heads run as one chunk each (all their blocks, so
+  // every K^ tile is loaded and transformed once or twice instead of up to three times); the last
+  // heads, about two waves of tickets, run as pairs of blocks, heaviest first, which balances the
+  // tail. Pairs take heads in groups whose K and V fit in half of L2 together.
   const long long n_qb = (p.T + 2 * swa::kTile - 1) / (2 * swa::kTile);
+  const long long n_bh = static_cast<long long>(p.B) * p.H;
+  const long long cpb = (n_qb + 1) / 2;  // pairs per head
   swa::AttnParams pk = p;
   const long long kv_head_bytes = 2LL * p.T * D * 2 / p.kv_group;  // K + V per query head (a group shares them)
   const long long hg = (64LL << 20) / kv_head_bytes;
   pk.head_group = static_cast<int>(hg < 1 ? 1 : (hg > (1 << 20) ? (1 << 20) : hg));
-  const long long chunks = static_cast<long long>(p.B) * p.H * ((n_qb + 1) / 2);
+  const bool chains = p.causal && p.window >= 0 && p.window <= swa::WsCfg<D>::kStages * swa::kTile && n_qb > 1;
+  const long long tail = 2 * ((sm_count + cpb - 1) / cpb);  // heads run as pairs
+  pk.n_long = chains && n_bh > tail ? static_cast<int>(n_bh - tail) : 0;
+  const long long chunks = pk.n_long + (n_bh - pk.n_long) * cpb;
   if (chunks >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
   const int grid = static_cast<int>(chunks < sm_count ? chunks : sm_count);
   // QK-norm on, no gate: the instantiation without the other modes' code

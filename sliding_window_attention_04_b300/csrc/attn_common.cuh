@@ -34,6 +34,8 @@ struct AttnParams {
                            // reference; 0: no bound known (QK-norm off), running maximum instead
   int n_qtiles;            // ceil(T / 128)
   int head_group;          // persistent kernel: heads per ticket group (their K/V fit in L2 together)
+  int n_long;              // persistent kernel: heads 0 .. n_long - 1 run as one ticket each (all their
+                           // query blocks); the others as tickets of two query blocks
   // value-embedding gate (nullptr ve: none): v <- v + gate[b, t, hk] ve, where the gate factor
   // 2 sigmoid(xg[b, t, 0:32] . wg[hk, 0:32]) is computed once per (b, t, hk) by ve_gate_kernel
   const __nv_bfloat16* ve;  // [B, T, Hkv, D]

@@ -669,11 +669,13 @@ __global__ void __launch_bounds__(640, 1)
       int q_armed[2] = {-1, -1};  // parity of the last armed phase of each Q barrier (for draining)
       uint32_t kcnt = 0;          // K/V stage loads issued
       bool ok = true;
-      // A ticket is a chunk: query blocks qb and qb - 1 of one head, heaviest chunks of every head
-      // first. The two units of a chunk run back to back on this CTA and share the key tiles both
-      // need through the ring (shared_steps).
+      // A ticket is a chunk of consecutive query blocks of one head, taken top down: all of them for
+      // heads 0 .. n_long - 1, then blocks qb and qb - 1 of the other heads, heaviest pairs of every
+      // head first. The units of a chunk run back to back on this CTA, and each shares the key tiles
+      // that it and the next one need through the ring (shared_steps).
       const int n_bh = p.B * p.H;
       int c_bh = 0, c_qb = -1, c_left = 0;  // the current chunk: head, next query block, units left
+      bool c_first = false;                 // the next unit is the first of its chunk
       UnitGeom g;
       g.r_out = 0;
       for (uint32_t ul = 0;; ++ul) {
@@ -686,25 +688,33 @@ __global__ void __launch_bounds__(640, 1)
         int unit = -1;
         if (c_left == 0) {
           const int c = atomicAdd(sched, 1);
-          if (c < n_chunks) {
-            // groups of head_group heads in turn; inside a group the heaviest pair of every head
-            // first, then the next pair of every head, ...
+          if (c < p.n_long) {
+            // a whole head, every query block top down
+            c_bh = c;
+            c_qb = n_qb - 1;
+            c_left = n_qb;
+          } else if (c < n_chunks) {
+            // pairs of the other heads: groups of head_group heads in turn; inside a group the
+            // heaviest pair of every head first, then the next pair of every head, ...
+            const int cp = c - p.n_long;
             const int cpb = (n_qb + 1) / 2;  // pairs per head
-            const int grp = c / (p.head_group * cpb);
-            const int rem = c - grp * p.head_group * cpb;
-            const int gsize = min(p.head_group, n_bh - grp * p.head_group);
+            const int grp = cp / (p.head_group * cpb);
+            const int rem = cp - grp * p.head_group * cpb;
+            const int gsize = min(p.head_group, n_bh - p.n_long - grp * p.head_group);
             const int rank = rem / gsize;
-            c_bh = grp * p.head_group + (rem - rank * gsize);
+            c_bh = p.n_long + grp * p.head_group + (rem - rank * gsize);
             c_qb = n_qb - 1 - 2 * rank;
             c_left = c_qb >= 1 ? 2 : 1;
           }
+          c_first = true;
         }
         if (c_left > 0) {
           const int r_in = g.r_out;  // the previous unit (same chunk) left that many steps
           unit_geom(p, c_bh, c_qb, g);
           unit = c_bh * n_qb + c_qb;
-          g.r_in = c_left == 1 ? r_in : 0;
-          if (c_left == 2) {
+          g.r_in = c_first ? 0 : r_in;
+          c_first = false;
+          if (c_left >= 2) {
             UnitGeom nb;
             unit_geom(p, c_bh, c_qb - 1, nb);
             g.r_out = shared_steps<S>(g, nb);

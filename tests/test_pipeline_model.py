@@ -51,18 +51,19 @@ class Bar:
             self.pending = self.count
 
 
-def units_for(B, H, T, window, causal, tickets, S):
+def units_for(B, H, T, window, causal, tickets, S, n_long=0):
     """The CTA's units in order, with r_in / r_out (the producer's decode and reuse rule)."""
     n_qb = (T + 2 * KT - 1) // (2 * KT)
     out = []
     for c in tickets:
-        bh, qb = ticket_decode(c, B * H, n_qb, 1 << 20)
-        left, r_prev = (2 if qb >= 1 else 1), 0
+        bh, qb, left = ticket_decode(c, B * H, n_qb, 1 << 20, n_long)
+        first, r_prev = True, 0
         while left:
             g = unit_geom(T, window, causal, bh, qb)
-            g["r_in"] = r_prev if left == 1 else 0
+            g["r_in"] = 0 if first else r_prev
+            first = False
             g["r_out"] = 0
-            if left == 2:
+            if left >= 2:
                 nb = unit_geom(T, window, causal, bh, qb - 1)
                 R = nb["ke_all"] - g["kb_all"] + 1
                 g["r_out"] = R if (shared_steps(g, nb) and R <= S) else 0
@@ -451,6 +452,26 @@ def test_protocol_has_no_deadlock_and_exact_waits(D, T, window, causal):
         tickets = sorted(rnd.sample(range(n_tickets), k=max(1, min(n_tickets, rnd.randint(1, 4)))))
         units = units_for(B, H, T, window, causal, tickets, S)
         c = run_cta(units, S, NB, QS, seed=1000 * trial + T + window)
+        assert all(b.completed == 1 for b in c.b["Final"])
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("T,window", [(1024, 512), (1024, 256), (1024, 128), (1500, 300), (2048, 200)])
+def test_protocol_with_whole_head_tickets(D, T, window):
+    """Tickets of all the blocks of a head (every unit keeps tiles resident for the next; a tile can
+    serve three units), mixed with pair tickets of another head."""
+    S, NB, QS = CONFIGS[D]
+    if window > S * KT:
+        pytest.skip("no key tiles shared at this ring depth")
+    B, H, n_long = 1, 2, 1
+    n_qb = (T + 2 * KT - 1) // (2 * KT)
+    n_tickets = n_long + (B * H - n_long) * ((n_qb + 1) // 2)
+    rnd = random.Random(T * 3 + window)
+    for trial in range(4):
+        tickets = [0] + sorted(rnd.sample(range(1, n_tickets), k=min(n_tickets - 1, rnd.randint(0, 3))))
+        units = units_for(B, H, T, window, True, tickets, S, n_long)
+        assert sum(1 for g in units if g["r_in"] > 0) >= n_qb - 1  # the whole head chains its units
+        c = run_cta(units, S, NB, QS, seed=7000 * trial + T + window)
         assert all(b.completed == 1 for b in c.b["Final"])
 
 

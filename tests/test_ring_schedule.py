@@ -1,8 +1,9 @@
 """Host-side model of the persistent kernel's K/V ring bookkeeping (runs without a GPU).
 
-The kernel hands out tickets of two query blocks (qb, qb - 1) of one head, heaviest first, streams
-each unit's key tiles downwards and keeps the last R tiles of the first unit resident for the
-second (R = ke_all(second) - kb_all(first) + 1 when 1 <= R <= ring depth). Every role derives the
+The kernel hands out tickets of consecutive query blocks of one head: all the blocks of heads
+0 .. n_long - 1 (one ticket each), then pairs (qb, qb - 1) of the other heads, heaviest first. It
+streams each unit's key tiles downwards and keeps the last R tiles of a unit resident for the next
+unit of its ticket (R = ke_all(next) - kb_all(unit) + 1 when 1 <= R <= ring depth). Every role derives the
 ring position of a key step with the same arithmetic: the producer and the prologue take fresh
 positions in order for the non-resident steps; the MMA issuers and the softmax use position
 `kc - r_in + i` for resident step i and the next fresh position otherwise; a stage is released
@@ -47,28 +48,48 @@ def shared_steps(a, nb):
     return R if (1 <= R <= S and R <= a["n"] and R <= nb["n"]) else 0
 
 
-def ticket_decode(c, n_bh, n_qb, head_group):
-    """Ticket c -> (head, highest query block of its pair): groups of head_group heads in turn, inside a
-    group the heaviest pair of every head first (the producer's decode in attn_fwd_ws.cuh)."""
+def ticket_decode(c, n_bh, n_qb, head_group, n_long=0):
+    """Ticket c -> (head, highest query block, units): heads below n_long whole, then pairs of the other
+    heads in groups of head_group heads, inside a group the heaviest pair of every head first (the
+    producer's decode in attn_fwd_ws.cuh)."""
+    if c < n_long:
+        return c, n_qb - 1, n_qb
     cpb = (n_qb + 1) // 2
-    grp, rem = divmod(c, head_group * cpb)
-    gsize = min(head_group, n_bh - grp * head_group)
+    grp, rem = divmod(c - n_long, head_group * cpb)
+    gsize = min(head_group, n_bh - n_long - grp * head_group)
     rank, i = divmod(rem, gsize)
-    return grp * head_group + i, n_qb - 1 - 2 * rank
+    qb = n_qb - 1 - 2 * rank
+    return n_long + grp * head_group + i, qb, (2 if qb >= 1 else 1)
 
 
-def cta_units(B, H, T, window, causal, tickets, head_group=1 << 20):
+def n_long_heads(B, H, T, window, causal, sm_count=148):
+    """Heads that run as one ticket each (attn_api.cu, launch_ws): all but about two waves of pair
+    tickets, where consecutive blocks can share key tiles (causal, window within the ring's depth)."""
+    n_qb = (T + 2 * KT - 1) // (2 * KT)
+    cpb = (n_qb + 1) // 2
+    tail = 2 * ((sm_count + cpb - 1) // cpb)
+    chains = causal and 0 <= window <= S * KT and n_qb > 1
+    return B * H - tail if chains and B * H > tail else 0
+
+
+def n_tickets(B, H, T, n_long):
+    n_qb = (T + 2 * KT - 1) // (2 * KT)
+    return n_long + (B * H - n_long) * ((n_qb + 1) // 2)
+
+
+def cta_units(B, H, T, window, causal, tickets, head_group=1 << 20, n_long=0):
     """The units one CTA runs for the given tickets, with r_in / r_out as the producer sets them."""
     n_qb = (T + 2 * KT - 1) // (2 * KT)
     n_bh = B * H
     units = []
     for c in tickets:
-        bh, qb = ticket_decode(c, n_bh, n_qb, head_group)
-        left, r_prev = (2 if qb >= 1 else 1), 0
+        bh, qb, left = ticket_decode(c, n_bh, n_qb, head_group, n_long)
+        first, r_prev = True, 0
         while left:
             g = unit_geom(T, window, causal, bh, qb)
-            g["r_in"] = r_prev if left == 1 else 0
-            if left == 2:
+            g["r_in"] = 0 if first else r_prev
+            first = False
+            if left >= 2:
                 g["r_out"] = shared_steps(g, unit_geom(T, window, causal, bh, qb - 1))
             r_prev = g["r_out"]
             units.append(g)
@@ -119,20 +140,52 @@ def test_ring_positions_releases_and_order(B, H, T):
                 check_ring(cta_units(B, H, T, window, causal, tickets, head_group))
 
 
-@pytest.mark.parametrize("n_bh,n_qb,head_group", [(384, 4, 256), (512, 8, 64), (192, 4, 512), (7, 3, 2),
-                                                  (5, 1, 3), (6, 5, 4)])
-def test_tickets_cover_every_pair_once_heaviest_first_in_a_group(n_bh, n_qb, head_group):
-    n_tickets = n_bh * ((n_qb + 1) // 2)
-    seen = [ticket_decode(c, n_bh, n_qb, head_group) for c in range(n_tickets)]
-    assert sorted(seen) == sorted((bh, n_qb - 1 - 2 * r) for bh in range(n_bh) for r in range((n_qb + 1) // 2))
-    for c in range(1, n_tickets):  # inside a group the pairs come heaviest (highest query block) first
-        (b0, q0), (b1, q1) = seen[c - 1], seen[c]
-        if b0 // head_group == b1 // head_group:
+@pytest.mark.parametrize("n_bh,n_qb,head_group,n_long", [(384, 4, 256, 0), (512, 8, 64, 0), (192, 4, 512, 0),
+                                                         (7, 3, 2, 0), (5, 1, 3, 0), (6, 5, 4, 0), (384, 4, 256, 236),
+                                                         (40, 8, 16, 21), (9, 3, 2, 4), (6, 5, 4, 5)])
+def test_tickets_cover_every_block_once_heaviest_pairs_first(n_bh, n_qb, head_group, n_long):
+    n_t = n_long + (n_bh - n_long) * ((n_qb + 1) // 2)
+    seen = [ticket_decode(c, n_bh, n_qb, head_group, n_long) for c in range(n_t)]
+    blocks = sorted((bh, qb - i) for bh, qb, units in seen for i in range(units))
+    assert blocks == sorted((bh, qb) for bh in range(n_bh) for qb in range(n_qb))
+    assert all(units == n_qb and qb == n_qb - 1 for bh, qb, units in seen[:n_long])
+    pairs = seen[n_long:]
+    for c in range(1, len(pairs)):  # inside a group the pairs come heaviest (highest query block) first
+        (b0, q0, _), (b1, q1, _) = pairs[c - 1], pairs[c]
+        if (b0 - n_long) // head_group == (b1 - n_long) // head_group:
             assert q1 <= q0
 
 
 def test_reuse_on_the_120m_shape():
-    """S layers (W = 512) load and transform 2/3 of the K tiles their key steps visit, L layers 90 %."""
+    """With pairs alone, S layers (W = 512) load and transform 2/3 of the K tiles their key steps visit
+    and L layers 90 %. With whole-head tickets for all but two waves of pairs (148 SMs: 236 of the 384
+    heads), S layers load 8 of a head's 18 visited tiles there and 12 in the pair heads."""
     for W, frac in ((512, 2 / 3), (1024, 0.9)):
         fresh, steps = check_ring(cta_units(32, 12, 1024, W, True, list(range(32 * 12 * 2))))
         assert abs(fresh / steps - frac) < 1e-9
+    n_long = n_long_heads(32, 12, 1024, 512, True)
+    assert n_long == 236 and n_long_heads(32, 12, 1024, 1024, True) == 0
+    tickets = list(range(n_tickets(32, 12, 1024, n_long)))
+    fresh, steps = check_ring(cta_units(32, 12, 1024, 512, True, tickets, n_long=n_long))
+    assert (fresh, steps) == (236 * 8 + 148 * 12, 384 * 18)
+
+
+@pytest.mark.parametrize("B,H,T", [(2, 80, 1024), (1, 160, 2048), (1, 200, 513), (4, 40, 1024)])
+def test_whole_head_tickets_ring_positions_and_releases(B, H, T):
+    """Chunks of all the blocks of a head: every unit shares with the next, a key tile can serve three
+    units; positions, single releases at the last use and load order still hold under random
+    assignments of tickets to CTAs."""
+    for window in (0, 100, 127, 128, 255, 256, 383, 384, 511, 512):
+        n_long = n_long_heads(B, H, T, window, True)
+        assert n_long > 0
+        n_t = n_tickets(B, H, T, n_long)
+        rnd = random.Random(T + window + H)
+        parts = [list(range(n_t))]
+        for _ in range(2):
+            per = {}
+            for c in range(n_t):
+                per.setdefault(rnd.randrange(4), []).append(c)
+            parts += list(per.values())
+        for tickets in parts:
+            for head_group in (1, 3, 1 << 20):
+                check_ring(cta_units(B, H, T, window, True, tickets, head_group, n_long))
