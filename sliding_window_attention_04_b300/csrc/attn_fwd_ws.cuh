@@ -1,10 +1,10 @@
 // Attention forward, warp-specialised persistent version (D = 32, 64, 128).
 //
 // One CTA per SM (640 threads = five warpgroups, up to ~200 KB shared memory, all 512 TMEM columns).
-// A work unit is (b, h, 256-row query block) = two 128-row query tiles that share one stream of
-// 128-key K/V tiles. A global ticket counter hands out pairs of units (query blocks qb and qb - 1 of
-// one head), the heaviest pair of every head first, so the cheap blocks finish the queue; the two
-// units of a pair run back to back and share the key tiles both need through the ring.
+// A work unit is (b, h, 256-row query block) = two 128-row query tiles sharing one stream of 128-key
+// K/V tiles. A ticket counter hands out chunks of one head's units, run back to back and sharing key
+// tiles through the ring: all of a head's blocks where consecutive blocks share tiles (all but the
+// last heads), else pairs (blocks qb, qb - 1), heaviest first, so the cheap blocks end the queue.
 //
 // Roles (warp index: role):
 //   0-3    softmax of query tile 0   (thread = query row = TMEM lane)
