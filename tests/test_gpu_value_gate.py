@@ -98,6 +98,13 @@ def test_value_gate_forward_120m_layer_sampled_heads(attn):
     check(attn, 8, 1024, 12, 12, 64, 768, 512, True, 10000.0, 1e-6, heads=[(0, 0), (3, 5), (7, 11)])
 
 
+def test_value_gate_forward_whole_head_tickets(attn):
+    """B = 16, H = 12, T = 1024, W = 512: 192 heads, so the kernel runs the first 44 as whole-head tickets
+    (every query block of the head on one CTA, key tiles shared across its blocks) and the rest as pairs;
+    the first and the last whole-head ticket's heads and the last head (a pair) are compared whole."""
+    check(attn, 16, 1024, 12, 12, 64, 768, 512, True, 10000.0, 1e-6, heads=[(0, 0), (3, 7), (15, 11)], seed=5)
+
+
 def test_value_gate_leaves_inputs_and_plain_path_unchanged(attn):
     q, k, v, ve, x, w = gate_inputs(1, 256, 2, 2, 64, 32, 99)
     qc, kc, vc, vec = q.cuda(), k.cuda(), v.cuda(), ve.cuda()
